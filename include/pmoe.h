@@ -1,0 +1,292 @@
+/*
+ * pmoe.h -- C ABI of libpmoe.so: the active-expert-chunked low-precision
+ * MoE layer with a block-diagonal orthogonal (OFT-style) adapter, for one
+ * GB300 (sm_103a).
+ *
+ * The operation follows the "Active-expert-chunked dequantization" and
+ * "bypass-base-weight-grad GEMM backward" passages of the Orbit
+ * announcement (page 1, section 技艺细节), the OFT adapter of the Orbit
+ * analysis (page 2, sections 机制拆解 and 术语), and the block-scaled FP8
+ * weight format of the NeMo RL FP8 blog (page 3, Table 1).
+ *
+ * Conventions for every entry point:
+ *  - Ownership: the caller allocates every buffer.  The library never
+ *    allocates device or pinned memory; scratch lives in the caller's
+ *    workspace (see moe_workspace_bytes).
+ *  - Pointers are DEVICE pointers unless stated otherwise; they must be
+ *    16-byte aligned.  Matrices are row-major and dense.
+ *  - Ordering: every call is asynchronous on `stream` (no host sync) except
+ *    moe_query_status, which synchronizes the stream.
+ *  - Errors: argument checks run on the host before anything is launched
+ *    and return PMOE_ERR_INVALID_ARG / PMOE_ERR_UNSUPPORTED /
+ *    PMOE_ERR_WORKSPACE with nothing enqueued.  A launch failure returns
+ *    PMOE_ERR_CUDA.  Errors found on the device (an expert id out of range,
+ *    a bounded wait that ran out) are recorded in the error word at the
+ *    start of the workspace and read back by moe_query_status; the kernels
+ *    never trap.
+ *  - Threading: the library holds no state between calls; calls with
+ *    distinct workspaces may run concurrently.
+ *  - Numerics: inputs must be finite.  BF16 values are raw uint16 bit
+ *    patterns (IEEE binary32 upper half).
+ *
+ * Notation: T tokens, d hidden size, E experts, k experts per token,
+ * I = inter (expert hidden size), b adapter block size, P = T*k pairs,
+ * a pair p = t*k + j is token t in slot j.
+ */
+#ifndef PMOE_H
+#define PMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PMOE_OK = 0,
+    PMOE_ERR_INVALID_ARG = 1,   /* bad shape, NULL pointer, misalignment */
+    PMOE_ERR_UNSUPPORTED = 2,   /* valid request this build does not handle */
+    PMOE_ERR_WORKSPACE = 3,     /* workspace missing or smaller than moe_workspace_bytes */
+    PMOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    PMOE_ERR_BAD_INDEX = 5,     /* device: an expert id outside [0, E) */
+    PMOE_ERR_TIMEOUT = 6        /* device: a bounded wait gave up */
+} pmoe_status;
+
+/* Frozen-base weight formats ("INT4 base", "FP4 base" on page 1; FP8 E4M3
+ * with [128,128] FP32 block scales, page 3 Table 1).  Every weight matrix
+ * is stored in the linear convention [N_out, K_in]:
+ *   INT4  : q u8 [N, K/2] (element 2i = low nibble of byte i, two's
+ *           complement in [-8, 7]); s bf16 [N, K/32].  W = bf16(q*s).
+ *   MXFP4 : q u8 [N, K/2] of E2M1 nibbles (same packing); s u8 [N, K/32]
+ *           of E8M0 exponents.  W = bf16(e2m1 * 2^(s-127)).
+ *   FP8   : q u8 [N, K] of E4M3 codes; s f32 [N/128, K/128].
+ *           W = bf16(fp32(e4m3 * s)). */
+typedef enum {
+    PMOE_W_INT4_G32_BF16 = 0,
+    PMOE_W_MXFP4_G32_E8M0 = 1,
+    PMOE_W_FP8_B128_F32 = 2
+} pmoe_wfmt;
+
+/* Layer shape.  Requirements: d % 64 == 0, inter % 64 == 0, d <= 8192,
+ * inter <= 8192, d % block == 0, inter % block == 0, block in
+ * {16, 32, 64, 128}, 1 <= k <= min(E, 32), E <= 4096, T >= 0; FP8
+ * additionally needs d % 128 == 0 and inter % 128 == 0. */
+typedef struct {
+    int32_t T, d, E, k, inter, block;
+} pmoe_dims;
+
+/* The frozen experts.  w13 holds, per expert, the gate rows 0..I-1 then the
+ * up rows I..2I-1 of the [2I, d] gate/up projection; w2 holds the [d, I]
+ * down projection.  Experts are consecutive along the leading axis. */
+typedef struct {
+    pmoe_wfmt fmt;
+    const void *w13, *s13;
+    const void *w2, *s2;
+} pmoe_weights;
+
+/* The orthogonal adapter: per expert, R_up [d/b, b, b] rotates the input of
+ * the gate/up projection (x~ = x blockdiag(R_up)) and R_down [I/b, b, b]
+ * the input of the down projection (h~ = h blockdiag(R_down)), BF16.
+ * stride_* = elements between consecutive experts' block sets; 0 means one
+ * set shared by all experts.  R_up == NULL disables the whole adapter (the
+ * reference policy: the frozen base alone); R_down may be NULL alone. */
+typedef struct {
+    const void *R_up, *R_down;
+    int64_t stride_up, stride_down;
+} pmoe_adapter;
+
+/* Routing and its grouping by expert (all device int32 / float):
+ * idx [T,k], w [T,k], counts [E], offsets [E+1], perm [P] (pair id at each
+ * expert-sorted position), inv_perm [P], active [E] (active experts
+ * ascending, -1 padded), num_active [1]. */
+typedef struct {
+    int32_t *idx;
+    float *w;
+    int32_t *counts, *offsets, *perm, *inv_perm, *active, *num_active;
+} pmoe_routing;
+
+/* Forward modes. */
+enum {
+    PMOE_MODE_FUSED = 0,   /* dequantize tile by tile in shared memory inside the GEMM */
+    PMOE_MODE_SCRATCH = 1  /* dequantize C experts into a global BF16 scratch, GEMM, reuse */
+};
+
+/* Router modes. */
+enum {
+    PMOE_ROUTE_FAST = 0    /* FP32 logits from an exact 3-term BF16 split of Wr on tensor cores */
+};
+
+/* Ops for moe_workspace_bytes. */
+enum { PMOE_OP_PERMUTE = 0, PMOE_OP_FORWARD = 1, PMOE_OP_BACKWARD = 2 };
+
+/*
+ * moe_route -- router top-k (page 1, 技艺细节: "router 选中的 experts").
+ * logits = fp32(X Wr) + bias; the k experts with the largest logits are
+ * selected (ties to the lower expert id), slots in descending logit order;
+ * w = softmax over the k selected logits (FP32).
+ *   X      bf16 [T, d]          Wr  f32 [d, E]       bias f32 [E] or NULL
+ *   logits f32 [T, E] or NULL (written when given)
+ *   idx    int32 [T, k] (out)   w   f32 [T, k] (out)
+ *   ws     workspace of moe_workspace_bytes(dims, PMOE_OP_PERMUTE, 0, 0)
+ *          bytes or more (holds the split router weights and the error word)
+ * Requires E <= 4096 and k <= 32.
+ */
+pmoe_status moe_route(pmoe_dims dims, const void *X, const float *Wr, const float *bias,
+                      float *logits, int32_t *idx, float *w, int mode,
+                      void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * moe_permute -- groups the (token, slot) pairs by expert (page 1, 技艺细节:
+ * the selected experts are gathered into batches): histogram of idx,
+ * exclusive-scan offsets and a stable scatter.  Bit-exact and
+ * deterministic: perm lists pair ids by (expert, pair id).
+ *   idx    int32 [T, k] (device, in); out->idx may alias it
+ *   out    host struct of device pointers (counts, offsets, perm, inv_perm,
+ *          active, num_active written; idx and w untouched)
+ *   ws     >= moe_workspace_bytes(dims, PMOE_OP_PERMUTE, 0, 0) bytes
+ * An id outside [0, E) sets PMOE_ERR_BAD_INDEX in the error word and the
+ * pair is left out of every count.
+ */
+pmoe_status moe_permute(pmoe_dims dims, const int32_t *idx, const pmoe_routing *out,
+                        void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * moe_chunked_forward -- the layer (page 1, 技艺细节): active experts are
+ * taken C at a time in ascending id order; each chunk's experts are
+ * dequantized to BF16 (FUSED: tile by tile in shared memory, no global
+ * scratch; SCRATCH: into a C-expert global BF16 buffer that the next chunk
+ * reuses), then for every pair of expert e:
+ *   x~ = bf16(x blockdiag(R_up[e]))             (adapter on the activations)
+ *   g, u = x~ W_gate[e]^T, x~ W_up[e]^T          (FP32 accumulate)
+ *   h  = bf16(silu(g) u);  h~ = bf16(h blockdiag(R_down[e]))
+ *   o  = h~ W_down[e]^T
+ * and finally Y_t = bf16(sum_j w[t,j] o_(t,j)), slots summed in order.
+ *   X   bf16 [T, d] (in)         Y bf16 [T, d] (out)
+ *   ctx bf16 [P, 2I] or NULL: when given, receives [g | u] per pair in
+ *       expert-sorted order (row i = pair perm[i]) for moe_backward_data
+ *   chunk_C >= 1 experts per chunk (>= E means one chunk)
+ *   ws  >= moe_workspace_bytes(dims, PMOE_OP_FORWARD, chunk_C, mode)
+ * The result does not depend on chunk_C or mode (bit-identical).
+ */
+pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const pmoe_adapter *adp,
+                                const pmoe_routing *rt, const void *X, int32_t chunk_C, int mode,
+                                void *Y, void *ctx, void *ws, size_t ws_bytes,
+                                cudaStream_t stream);
+
+/*
+ * moe_backward_data -- backward through the frozen experts with no base
+ * weight gradient (page 1, 技艺细节: bypass-base-weight-grad GEMM backward;
+ * page 2, 机制拆解: the base takes no backward update cost).  Routing and
+ * w are held fixed.  Per pair (t, j), e = idx[t, j]:
+ *   G = dY_t W_down[e]          d_topk_w[t,j] = G . h~
+ *   dh~ = w[t,j] G              dR_down[e] += h_blk^T dh~_blk
+ *   dh = dh~ R_down^T;  dg = dh u s(g)(1 + g(1 - s(g)));  du = dh silu(g)
+ *   dx~ = dg W_gate + du W_up   dR_up[e] += x_blk^T dx~_blk
+ *   dx_pair = dx~ R_up^T        dX_t = bf16(sum_j dx_pair), slots in order
+ *   X, dY   bf16 [T, d] (in)    ctx bf16 [P, 2I] from the forward (in)
+ *   dX      bf16 [T, d] (out)
+ *   d_topk_w f32 [T, k] or NULL (out)
+ *   dR_up   f32 shaped like R_up, dR_down f32 shaped like R_down (out,
+ *           overwritten; NULL iff the matching rotation is NULL); with a
+ *           shared adapter they hold the sum over all experts
+ *   ws  >= moe_workspace_bytes(dims, PMOE_OP_BACKWARD, chunk_C, 0)
+ * Reductions run in a fixed order: results are run-to-run identical.
+ */
+pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmoe_adapter *adp,
+                              const pmoe_routing *rt, const void *X, const void *dY,
+                              const void *ctx, int32_t chunk_C, void *dX, float *d_topk_w,
+                              float *dR_up, float *dR_down, void *ws, size_t ws_bytes,
+                              cudaStream_t stream);
+
+/*
+ * moe_dequant -- the dequantization step alone (page 1, 技艺细节:
+ * "临时反量化"): one [N, K] weight matrix in `fmt` to BF16 [N, K].
+ * Bit-exact with the format definitions above.  N >= 0, K % 32 == 0
+ * (INT4 / MXFP4) or N % 128 == 0 and K % 128 == 0 (FP8).
+ */
+pmoe_status moe_dequant(pmoe_wfmt fmt, const void *q, const void *s, int64_t N, int64_t K,
+                        void *out, cudaStream_t stream);
+
+/*
+ * adapter_apply -- Xr = bf16(X blockdiag(R)) (page 2, 机制拆解: the OFT
+ * adapter as a local orthogonal transform).  X bf16 [rows, dim], R bf16
+ * [dim/b, b, b], Xr bf16 [rows, dim] (must not alias X).  dim % b == 0,
+ * b in {16, 32, 64, 128}.
+ */
+pmoe_status adapter_apply(int32_t rows, int32_t dim, int32_t b, const void *X, const void *R,
+                          void *Xr, cudaStream_t stream);
+
+/*
+ * adapter_grad -- backward of adapter_apply: dX = bf16(dXr blockdiag(R)^T)
+ * (skipped when dX is NULL) and dR[beta] = sum_i X_blk[i]^T dXr_blk[i]
+ * (f32 [dim/b, b, b], overwritten, fixed summation order).
+ */
+pmoe_status adapter_grad(int32_t rows, int32_t dim, int32_t b, const void *X, const void *dXr,
+                         const void *R, void *dX, float *dR, cudaStream_t stream);
+
+/*
+ * adapter_cayley -- R = (I + S)(I - S)^{-1} for nblk skew-symmetric b x b
+ * blocks S (f32 [nblk, b, b]); R written as bf16 (R_bf16, nullable) and
+ * f32 (R_f32, nullable).  b <= 128.
+ */
+pmoe_status adapter_cayley(int32_t nblk, int32_t b, const float *S, void *R_bf16, float *R_f32,
+                           cudaStream_t stream);
+
+/*
+ * adapter_cayley_grad -- dS = M - M^T with M = (I + R)^T dR (I - S)^{-T},
+ * the gradient with respect to the skew parameter of each block.
+ * S, R_f32 (from adapter_cayley), dR: f32 [nblk, b, b]; dS f32 out.
+ */
+pmoe_status adapter_cayley_grad(int32_t nblk, int32_t b, const float *S, const float *R_f32,
+                                const float *dR, float *dS, cudaStream_t stream);
+
+/* Bytes of device workspace an op needs (op = PMOE_OP_*).  Includes the
+ * 256-byte error word at the start.  In SCRATCH mode this includes the
+ * C-expert BF16 dequant buffer, reported separately by
+ * moe_scratch_bytes. */
+size_t moe_workspace_bytes(pmoe_dims dims, int op, int32_t chunk_C, int mode);
+
+/* Bytes of the bounded dequant scratch of one chunk in SCRATCH mode:
+ * min(C, E) experts x 3 x I x d BF16; 0 in FUSED mode. */
+size_t moe_scratch_bytes(pmoe_dims dims, int32_t chunk_C, int mode);
+
+/* Clear the device error word at the start of `ws` (asynchronous). */
+pmoe_status moe_clear_status(void *ws, cudaStream_t stream);
+
+/* Synchronize `stream`, read the device error word of `ws`, clear it and
+ * return it (PMOE_OK when no device error was recorded). */
+pmoe_status moe_query_status(void *ws, cudaStream_t stream);
+
+/* Static description of a status code. */
+const char *pmoe_status_string(pmoe_status s);
+
+/* Number of kernels the library has enqueued since load (all entry
+ * points, all streams); a diagnostic counter for launch accounting. */
+uint64_t pmoe_launch_count(void);
+
+/* Kernel classes of the diagnostic timer. */
+enum {
+    PMOE_KT_GEMM_GATE_UP = 0,   /* forward gate/up grouped GEMM (+ SwiGLU epilogue) */
+    PMOE_KT_GEMM_DOWN = 1,      /* forward down grouped GEMM */
+    PMOE_KT_GEMM_BWD_G = 2,     /* backward dY W_down grouped GEMM */
+    PMOE_KT_GEMM_BWD_DX = 3,    /* backward [dg du] W13 grouped GEMM */
+    PMOE_KT_ROUTER = 4,         /* router logits */
+    PMOE_KT_COUNT = 5
+};
+
+/* Diagnostic per-kernel timing.  While enabled, every launch of a timed
+ * kernel class is bracketed by two CUDA events recorded on the launch
+ * stream (events come from a host-side pool; no device memory is
+ * allocated).  Enabling or disabling clears the records. */
+pmoe_status pmoe_kernel_timing(int enable);
+
+/* Total device time (ms) and number of launches of kernel class `which`
+ * recorded since timing was enabled; waits for the recorded events. */
+pmoe_status pmoe_kernel_time(int which, double *ms_total, int *launches);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PMOE_H */

@@ -613,26 +613,37 @@ void or_forward(const or_layer *L, const uint16_t *X, const double *X64, const i
                 double *Y64, double *o_out)
 {
     int d = L->d, k = L->k;
+    int64_t np = (int64_t)n_toks * k;
+    double *o_all = malloc(sizeof(double) * (size_t)(np > 0 ? np * d : 1));
+    /* every (token, slot) pair independently */
 #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t p = 0; p < np; ++p) {
+        int t = toks ? toks[p / k] : (int)(p / k);
+        int e = idx[(int64_t)t * k + p % k];
+        pair_buf pb = pb_alloc(d, L->I);
+        expert_forward(L, e, X + (int64_t)t * d, X64 ? X64 + (int64_t)t * d : NULL, flags, &pb);
+        memcpy(o_all + p * d, pb.o, sizeof(double) * (size_t)d);
+        free(pb.x);
+    }
+    /* Y_t = sum over the slots in order of w_tj o_j */
+#pragma omp parallel for schedule(static)
     for (int it = 0; it < n_toks; ++it) {
         int t = toks ? toks[it] : it;
-        pair_buf pb = pb_alloc(d, L->I);
         double *acc = calloc((size_t)d, sizeof(double));
         for (int j = 0; j < k; ++j) {
-            int e = idx[(int64_t)t * k + j];
-            expert_forward(L, e, X + (int64_t)t * d, X64 ? X64 + (int64_t)t * d : NULL, flags, &pb);
+            const double *o = o_all + ((int64_t)it * k + j) * d;
             for (int c = 0; c < d; ++c)
-                acc[c] += (double)w[(int64_t)t * k + j] * pb.o[c];
+                acc[c] += (double)w[(int64_t)t * k + j] * o[c];
             if (o_out)
-                memcpy(o_out + ((int64_t)t * k + j) * d, pb.o, sizeof(double) * (size_t)d);
+                memcpy(o_out + ((int64_t)t * k + j) * d, o, sizeof(double) * (size_t)d);
         }
         for (int c = 0; c < d; ++c) {
             if (Y) Y[(int64_t)t * d + c] = or_bf16_round(acc[c]);
             if (Y64) Y64[(int64_t)t * d + c] = acc[c];
         }
         free(acc);
-        free(pb.x);
     }
+    free(o_all);
 }
 
 /*
@@ -660,15 +671,15 @@ void or_backward(const or_layer *L, const uint16_t *X, const double *X64, const 
     double *dxts = malloc(sizeof(double) * (size_t)(np * d));
     double *hs = malloc(sizeof(double) * (size_t)(np * I));
     double *dhts = malloc(sizeof(double) * (size_t)(np * I));
+    double *dxps = malloc(sizeof(double) * (size_t)(np > 0 ? np * d : 1));
 #pragma omp parallel for schedule(dynamic, 1)
-    for (int it = 0; it < n_toks; ++it) {
-        int t = toks ? toks[it] : it;
+    for (int64_t p = 0; p < np; ++p) {
+        int t = toks ? toks[p / k] : (int)(p / k);
+        int j = (int)(p % k);
         pair_buf pb = pb_alloc(d, I);
         double *G = malloc(sizeof(double) * (size_t)(2 * I + 2 * d + 2 * I));
         double *dh = G + I, *dxt = dh + I, *dxp = dxt + d, *dg = dxp + d, *du = dg + I;
-        double *acc = calloc((size_t)d, sizeof(double));
-        for (int j = 0; j < k; ++j) {
-            int64_t p = (int64_t)it * k + j;
+        {
             int e = idx[(int64_t)t * k + j];
             double wt = (double)w[(int64_t)t * k + j];
             expert_forward(L, e, X + (int64_t)t * d, X64 ? X64 + (int64_t)t * d : NULL, flags, &pb);
@@ -692,9 +703,9 @@ void or_backward(const or_layer *L, const uint16_t *X, const double *X64, const 
             if (L->R_down) {
                 int64_t o = (int64_t)e * L->stride_down;
                 rotate_row_t64(dht, L->R_down + o, L->R_down64 ? L->R_down64 + o : NULL, I, b, dh);
-            }
-            else
+            } else {
                 memcpy(dh, dht, sizeof(double) * (size_t)I);
+            }
             for (int n = 0; n < I; ++n) {
                 double g = pb.g[n], u = pb.u[n], sg = sigm(g);
                 dg[n] = dh[n] * u * sg * (1.0 + g * (1.0 - sg));
@@ -714,20 +725,29 @@ void or_backward(const or_layer *L, const uint16_t *X, const double *X64, const 
             if (L->R_up) {
                 int64_t o = (int64_t)e * L->stride_up;
                 rotate_row_t64(dxt, L->R_up + o, L->R_up64 ? L->R_up64 + o : NULL, d, b, dxp);
-            }
-            else
+            } else {
                 memcpy(dxp, dxt, sizeof(double) * (size_t)d);
-            for (int c = 0; c < d; ++c)
-                acc[c] += dxp[c];
+            }
+            memcpy(dxps + p * d, dxp, sizeof(double) * (size_t)d);
         }
+        free(G);
+        free(pb.x);
+    }
+    /* dX_t = bf16(sum over the slots in order of dx_pair) */
+#pragma omp parallel for schedule(static)
+    for (int it = 0; it < n_toks; ++it) {
+        int t = toks ? toks[it] : it;
+        double *acc = calloc((size_t)d, sizeof(double));
+        for (int j = 0; j < k; ++j)
+            for (int c = 0; c < d; ++c)
+                acc[c] += dxps[((int64_t)it * k + j) * d + c];
         for (int c = 0; c < d; ++c) {
             if (dX) dX[(int64_t)t * d + c] = or_bf16_round(acc[c]);
             if (dX64) dX64[(int64_t)t * d + c] = acc[c];
         }
         free(acc);
-        free(G);
-        free(pb.x);
     }
+    free(dxps);
     /* ordered reduction of the adapter gradients: one expert (block set)
      * per task, pairs in token-list then slot order */
     int nset_up = L->stride_up ? L->E : 1, nset_dn = L->stride_down ? L->E : 1;

@@ -1,0 +1,611 @@
+// api.cu -- the extern "C" entry points of libpmoe (declared in pmoe.h):
+// host-side validation, workspace layout and the order of launches.
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace pmoe {
+
+static std::atomic<uint64_t> g_launches{0};
+void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+// ------------------------------------------------------------------ timer
+// Event pairs around launches of the timed kernel classes (diagnostic).
+struct TimerRec {
+    int cls;
+    cudaEvent_t a, b;
+};
+static std::mutex g_tmu;
+static bool g_timing = false;
+static std::vector<TimerRec> g_recs;
+static std::vector<cudaEvent_t> g_pool;
+
+static cudaEvent_t pool_event()
+{
+    if (!g_pool.empty()) {
+        cudaEvent_t e = g_pool.back();
+        g_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+struct ScopedTimer {
+    bool on = false;
+    TimerRec rec{};
+    cudaStream_t st;
+    ScopedTimer(int cls, cudaStream_t s) : st(s)
+    {
+        std::lock_guard<std::mutex> g(g_tmu);
+        if (!g_timing) return;
+        rec.cls = cls;
+        rec.a = pool_event();
+        rec.b = pool_event();
+        on = rec.a && rec.b;
+        if (on) cudaEventRecord(rec.a, st);
+    }
+    ~ScopedTimer()
+    {
+        if (!on) return;
+        cudaEventRecord(rec.b, st);
+        std::lock_guard<std::mutex> g(g_tmu);
+        g_recs.push_back(rec);
+    }
+};
+
+static void clear_records()
+{
+    for (auto &r : g_recs) {
+        g_pool.push_back(r.a);
+        g_pool.push_back(r.b);
+    }
+    g_recs.clear();
+}
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Sequential carving of a workspace into 256-byte aligned regions.
+struct Carver {
+    uint8_t *base;
+    size_t off = 0;
+    explicit Carver(void *b) : base((uint8_t *)b) {}
+    template <class T>
+    T *take(size_t count)
+    {
+        T *p = base ? (T *)(base + off) : nullptr;
+        off = up256(off + count * sizeof(T));
+        return p;
+    }
+};
+
+static bool dims_ok(const pmoe_dims &d)
+{
+    if (d.T < 0 || d.d <= 0 || d.inter <= 0 || d.E <= 0 || d.k <= 0) return false;
+    if (d.k > d.E || d.E > 4096 || d.k > 32) return false;
+    if (d.d % 64 || d.inter % 64) return false;
+    if (d.d > 8192 || d.inter > 8192) return false;   // row buffers live in shared memory
+    if (!(d.block == 16 || d.block == 32 || d.block == 64 || d.block == 128)) return false;
+    if (d.d % d.block || d.inter % d.block) return false;
+    if ((int64_t)d.T * d.k > (int64_t)INT32_MAX / 2) return false;
+    return true;
+}
+
+static bool fmt_ok(const pmoe_dims &d, int fmt)
+{
+    if (fmt == PMOE_W_INT4_G32_BF16 || fmt == PMOE_W_MXFP4_G32_E8M0) return true;
+    if (fmt == PMOE_W_FP8_B128_F32) return d.d % 128 == 0 && d.inter % 128 == 0;
+    return false;
+}
+
+static int nchunks_of(const pmoe_dims &d, int C) { return (int)cdiv(d.E, C); }
+static int max_tiles_of(const pmoe_dims &d) { return (int)(cdiv((int64_t)d.T * d.k, 16) + d.E); }
+
+// Tile rows of the CUDA-core grouped GEMM.
+constexpr int kSimpleRows = 64;
+
+struct FwdWs {
+    DevErr *err;
+    Tile *tiles;
+    int32_t *chunk_tiles, *chunk_rows;
+    uint16_t *xt, *h, *ht, *o, *scratch;
+};
+static FwdWs carve_fwd(void *ws, const pmoe_dims &d, int C, int mode, size_t *bytes)
+{
+    Carver c(ws);
+    FwdWs w;
+    int64_t P = (int64_t)d.T * d.k;
+    w.err = c.take<DevErr>(kHdrBytes / sizeof(DevErr));
+    w.tiles = c.take<Tile>(max_tiles_of(d));
+    w.chunk_tiles = c.take<int32_t>(nchunks_of(d, C) + 2);
+    w.chunk_rows = c.take<int32_t>(nchunks_of(d, C) + 2);
+    w.xt = c.take<uint16_t>(P * d.d);
+    w.h = c.take<uint16_t>(P * d.inter);
+    w.ht = c.take<uint16_t>(P * d.inter);
+    w.o = c.take<uint16_t>(P * d.d);
+    int64_t slots = mode == PMOE_MODE_SCRATCH ? std::min(C, d.E) : 0;
+    w.scratch = c.take<uint16_t>(slots * 3 * (int64_t)d.inter * d.d);
+    if (bytes) *bytes = c.off;
+    return w;
+}
+
+struct BwdWs {
+    DevErr *err;
+    Tile *tiles;
+    int32_t *chunk_tiles, *chunk_rows;
+    uint16_t *dyp, *h, *ht, *dht, *dgu, *dxt;
+    float *dtw_part;
+};
+static BwdWs carve_bwd(void *ws, const pmoe_dims &d, int C, size_t *bytes)
+{
+    Carver c(ws);
+    BwdWs w;
+    int64_t P = (int64_t)d.T * d.k;
+    w.err = c.take<DevErr>(kHdrBytes / sizeof(DevErr));
+    w.tiles = c.take<Tile>(max_tiles_of(d));
+    w.chunk_tiles = c.take<int32_t>(nchunks_of(d, C) + 2);
+    w.chunk_rows = c.take<int32_t>(nchunks_of(d, C) + 2);
+    w.dyp = c.take<uint16_t>(P * d.d);
+    w.h = c.take<uint16_t>(P * d.inter);
+    w.ht = c.take<uint16_t>(P * d.inter);
+    w.dht = c.take<uint16_t>(P * d.inter);
+    w.dgu = c.take<uint16_t>(P * 2 * d.inter);
+    w.dxt = c.take<uint16_t>(P * d.d);
+    w.dtw_part = c.take<float>(P * (d.inter / 64));
+    if (bytes) *bytes = c.off;
+    return w;
+}
+
+struct PermWs {
+    DevErr *err;
+    int32_t *hist;
+    float *logits;
+};
+static PermWs carve_perm(void *ws, const pmoe_dims &d, size_t *bytes)
+{
+    Carver c(ws);
+    PermWs w;
+    w.err = c.take<DevErr>(kHdrBytes / sizeof(DevErr));
+    w.hist = c.take<int32_t>(permute_ws_bytes(d.T * d.k, d.E) / sizeof(int32_t));
+    w.logits = c.take<float>((int64_t)d.T * d.E);
+    if (bytes) *bytes = c.off;
+    return w;
+}
+
+static pmoe_status launched(cudaStream_t st)
+{
+    (void)st;
+    return cudaPeekAtLastError() == cudaSuccess ? PMOE_OK : PMOE_ERR_CUDA;
+}
+
+}  // namespace pmoe
+
+using namespace pmoe;
+
+extern "C" {
+
+const char *pmoe_status_string(pmoe_status s)
+{
+    switch (s) {
+    case PMOE_OK: return "ok";
+    case PMOE_ERR_INVALID_ARG: return "invalid argument";
+    case PMOE_ERR_UNSUPPORTED: return "unsupported";
+    case PMOE_ERR_WORKSPACE: return "workspace too small";
+    case PMOE_ERR_CUDA: return "CUDA error";
+    case PMOE_ERR_BAD_INDEX: return "expert index out of range";
+    case PMOE_ERR_TIMEOUT: return "bounded wait timed out";
+    }
+    return "unknown status";
+}
+
+uint64_t pmoe_launch_count(void) { return g_launches.load(); }
+
+pmoe_status pmoe_kernel_timing(int enable)
+{
+    std::lock_guard<std::mutex> g(g_tmu);
+    clear_records();
+    g_timing = enable != 0;
+    return PMOE_OK;
+}
+
+pmoe_status pmoe_kernel_time(int which, double *ms_total, int *launches)
+{
+    if (which < 0 || which >= PMOE_KT_COUNT || !ms_total || !launches)
+        return PMOE_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> g(g_tmu);
+    double tot = 0;
+    int n = 0;
+    for (auto &r : g_recs) {
+        if (r.cls != which) continue;
+        if (cudaEventSynchronize(r.b) != cudaSuccess) return PMOE_ERR_CUDA;
+        float ms = 0;
+        if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) return PMOE_ERR_CUDA;
+        tot += ms;
+        ++n;
+    }
+    *ms_total = tot;
+    *launches = n;
+    return PMOE_OK;
+}
+
+size_t moe_workspace_bytes(pmoe_dims dims, int op, int32_t chunk_C, int mode)
+{
+    if (!dims_ok(dims)) return 0;
+    int C = chunk_C < 1 ? 1 : std::min(chunk_C, dims.E);
+    size_t b = 0;
+    if (op == PMOE_OP_PERMUTE) carve_perm(nullptr, dims, &b);
+    else if (op == PMOE_OP_FORWARD) carve_fwd(nullptr, dims, C, mode, &b);
+    else if (op == PMOE_OP_BACKWARD) carve_bwd(nullptr, dims, C, &b);
+    return b;
+}
+
+size_t moe_scratch_bytes(pmoe_dims dims, int32_t chunk_C, int mode)
+{
+    if (!dims_ok(dims) || mode != PMOE_MODE_SCRATCH || chunk_C < 1) return 0;
+    return (size_t)std::min(chunk_C, dims.E) * 3 * (size_t)dims.inter * dims.d * 2;
+}
+
+pmoe_status moe_clear_status(void *ws, cudaStream_t stream)
+{
+    if (!ws) return PMOE_ERR_INVALID_ARG;
+    return cudaMemsetAsync(ws, 0, sizeof(DevErr), stream) == cudaSuccess ? PMOE_OK : PMOE_ERR_CUDA;
+}
+
+pmoe_status moe_query_status(void *ws, cudaStream_t stream)
+{
+    if (!ws) return PMOE_ERR_INVALID_ARG;
+    DevErr e;
+    if (cudaMemcpyAsync(&e, ws, sizeof e, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return PMOE_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return PMOE_ERR_CUDA;
+    if (cudaMemsetAsync(ws, 0, sizeof e, stream) != cudaSuccess) return PMOE_ERR_CUDA;
+    return (pmoe_status)e.code;
+}
+
+pmoe_status moe_route(pmoe_dims dims, const void *X, const float *Wr, const float *bias,
+                      float *logits, int32_t *idx, float *w, int mode, void *ws, size_t ws_bytes,
+                      cudaStream_t stream)
+{
+    if (!dims_ok(dims) || mode != PMOE_ROUTE_FAST) return PMOE_ERR_INVALID_ARG;
+    if (dims.T > 0 && (!X || !Wr || !idx || !w)) return PMOE_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Wr) || !aligned16(idx) || !aligned16(w) || !aligned16(bias) ||
+        !aligned16(logits))
+        return PMOE_ERR_INVALID_ARG;
+    size_t need;
+    PermWs pw = carve_perm(ws, dims, &need);
+    if (!ws || ws_bytes < need || !aligned16(ws)) return PMOE_ERR_WORKSPACE;
+    if (dims.T == 0) return PMOE_OK;
+    {
+        ScopedTimer tm(PMOE_KT_ROUTER, stream);
+        launch_logits_f32(dims.T, dims.d, dims.E, (const uint16_t *)X, Wr, pw.logits, stream);
+    }
+    launch_route_topk(dims.T, dims.E, dims.k, pw.logits, bias, idx, w, logits, stream);
+    return launched(stream);
+}
+
+pmoe_status moe_permute(pmoe_dims dims, const int32_t *idx, const pmoe_routing *out, void *ws,
+                        size_t ws_bytes, cudaStream_t stream)
+{
+    if (!dims_ok(dims) || !out) return PMOE_ERR_INVALID_ARG;
+    if ((dims.T > 0 && (!idx || !out->perm || !out->inv_perm)) || !out->counts ||
+        !out->offsets || !out->active || !out->num_active)
+        return PMOE_ERR_INVALID_ARG;
+    size_t need;
+    PermWs pw = carve_perm(ws, dims, &need);
+    if (!ws || ws_bytes < need || !aligned16(ws)) return PMOE_ERR_WORKSPACE;
+    launch_permute(dims.T * dims.k, dims.E, idx, out->counts, out->offsets, out->perm,
+                   out->inv_perm, out->active, out->num_active, pw.hist, pw.err, stream);
+    return launched(stream);
+}
+
+static bool routing_ok(const pmoe_routing *rt, const pmoe_dims &d)
+{
+    if (!rt) return false;
+    if (!rt->counts || !rt->offsets || !rt->active || !rt->num_active) return false;
+    if (d.T > 0 && (!rt->idx || !rt->w || !rt->perm || !rt->inv_perm)) return false;
+    return true;
+}
+
+static bool weights_ok(const pmoe_weights *wt, const pmoe_dims &d)
+{
+    if (!wt || !fmt_ok(d, wt->fmt)) return false;
+    if (!wt->w13 || !wt->s13 || !wt->w2 || !wt->s2) return false;
+    return aligned16(wt->w13) && aligned16(wt->w2) && aligned16(wt->s13) && aligned16(wt->s2);
+}
+
+static bool adapter_ok(const pmoe_adapter *ad)
+{
+    if (!ad) return true;
+    if (!ad->R_up && ad->R_down) return false;
+    if (ad->stride_up < 0 || ad->stride_down < 0) return false;
+    return aligned16(ad->R_up) && aligned16(ad->R_down);
+}
+
+pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const pmoe_adapter *adp,
+                                const pmoe_routing *rt, const void *X, int32_t chunk_C, int mode,
+                                void *Y, void *ctx, void *ws, size_t ws_bytes,
+                                cudaStream_t stream)
+{
+    if (!dims_ok(dims) || !weights_ok(wts, dims) || !adapter_ok(adp) || !routing_ok(rt, dims))
+        return PMOE_ERR_INVALID_ARG;
+    if (chunk_C < 1 || (mode != PMOE_MODE_FUSED && mode != PMOE_MODE_SCRATCH))
+        return PMOE_ERR_INVALID_ARG;
+    if (dims.T > 0 && (!X || !Y)) return PMOE_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Y) || !aligned16(ctx)) return PMOE_ERR_INVALID_ARG;
+    const int C = std::min(chunk_C, dims.E);
+    size_t need;
+    FwdWs w = carve_fwd(ws, dims, C, mode, &need);
+    if (!ws || ws_bytes < need || !aligned16(ws)) return PMOE_ERR_WORKSPACE;
+    if (dims.T == 0) return PMOE_OK;
+
+    const int d = dims.d, I = dims.inter, b = dims.block, k = dims.k, E = dims.E;
+    const int P = dims.T * k;
+    const int fmt = wts->fmt;
+    const uint16_t *R_up = adp ? (const uint16_t *)adp->R_up : nullptr;
+    const uint16_t *R_dn = adp && R_up ? (const uint16_t *)adp->R_down : nullptr;
+    const int64_t su = adp ? adp->stride_up : 0, sd = adp ? adp->stride_down : 0;
+    const int nch = nchunks_of(dims, C);
+    const int maxt = max_tiles_of(dims);
+
+    launch_build_tiles(E, C, kSimpleRows, 1, rt->counts, rt->offsets, rt->active, rt->num_active,
+                       w.tiles, w.chunk_tiles, w.chunk_rows, stream);
+    // x~ for every pair, in expert-sorted order (gather + up rotation)
+    launch_rotate_rows(P, d, b, (const uint16_t *)X, true, rt->perm, k, rt->idx, R_up, su, w.xt,
+                       nullptr, stream);
+
+    GemmArgs gu{};
+    gu.kind = GK_FWD_GU;
+    gu.A = w.xt;
+    gu.K = d;
+    gu.Nout = I;
+    gu.Nst = 2 * (int64_t)I;
+    gu.Kst = d;
+    gu.tiles = w.tiles;
+    gu.chunk_tiles = w.chunk_tiles;
+    gu.out = w.h;
+    gu.ctx = (uint16_t *)ctx;
+    gu.I = I;
+    GemmArgs dn{};
+    dn.kind = GK_FWD_DOWN;
+    dn.A = w.ht;
+    dn.K = I;
+    dn.Nout = d;
+    dn.Nst = d;
+    dn.Kst = I;
+    dn.tiles = w.tiles;
+    dn.chunk_tiles = w.chunk_tiles;
+    dn.out = w.o;
+    dn.I = I;
+
+    if (mode == PMOE_MODE_FUSED) {
+        gu.fmt = dn.fmt = fmt;
+        gu.wq = (const uint8_t *)wts->w13;
+        gu.ws = (const uint8_t *)wts->s13;
+        gu.wq_stride = wq_bytes(fmt, 2 * (int64_t)I, d);
+        gu.ws_stride = ws_bytes_of(fmt, 2 * (int64_t)I, d);
+        dn.wq = (const uint8_t *)wts->w2;
+        dn.ws = (const uint8_t *)wts->s2;
+        dn.wq_stride = wq_bytes(fmt, d, I);
+        dn.ws_stride = ws_bytes_of(fmt, d, I);
+        gu.c0 = dn.c0 = 0;
+        gu.c1 = dn.c1 = nch;
+        {
+            ScopedTimer tm(PMOE_KT_GEMM_GATE_UP, stream);
+            launch_gemm_simple(gu, maxt, stream);
+        }
+        launch_rotate_rows(P, I, b, w.h, false, rt->perm, k, rt->idx, R_dn, sd, w.ht, nullptr,
+                           stream);
+        {
+            ScopedTimer tm(PMOE_KT_GEMM_DOWN, stream);
+            launch_gemm_simple(dn, maxt, stream);
+        }
+    } else {
+        const int64_t slot_bytes = 3 * (int64_t)I * d * 2;
+        gu.fmt = dn.fmt = kFmtBF16;
+        gu.wq = dn.wq = (const uint8_t *)w.scratch;
+        gu.ws = dn.ws = nullptr;
+        gu.wq_stride = dn.wq_stride = slot_bytes;
+        gu.w_off_elems = 0;
+        dn.w_off_elems = 2 * (int64_t)I * d;
+        gu.slot_index = dn.slot_index = true;
+        for (int c = 0; c < nch; ++c) {
+            launch_dequant_chunk(fmt, d, I, C, c, rt->active, rt->num_active, wts->w13, wts->s13,
+                                 wts->w2, wts->s2, w.scratch, stream);
+            gu.c0 = dn.c0 = c;
+            gu.c1 = dn.c1 = c + 1;
+            {
+                ScopedTimer tm(PMOE_KT_GEMM_GATE_UP, stream);
+                launch_gemm_simple(gu, maxt, stream);
+            }
+            launch_rotate_rows(P, I, b, w.h, false, rt->perm, k, rt->idx, R_dn, sd, w.ht,
+                               w.chunk_rows + c, stream);
+            {
+                ScopedTimer tm(PMOE_KT_GEMM_DOWN, stream);
+                launch_gemm_simple(dn, maxt, stream);
+            }
+        }
+    }
+    launch_combine(dims.T, d, k, w.o, rt->inv_perm, rt->w, (uint16_t *)Y, stream);
+    return launched(stream);
+}
+
+pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmoe_adapter *adp,
+                              const pmoe_routing *rt, const void *X, const void *dY,
+                              const void *ctx, int32_t chunk_C, void *dX, float *d_topk_w,
+                              float *dR_up, float *dR_down, void *ws, size_t ws_bytes,
+                              cudaStream_t stream)
+{
+    if (!dims_ok(dims) || !weights_ok(wts, dims) || !adapter_ok(adp) || !routing_ok(rt, dims))
+        return PMOE_ERR_INVALID_ARG;
+    if (chunk_C < 1) return PMOE_ERR_INVALID_ARG;
+    const uint16_t *R_up = adp ? (const uint16_t *)adp->R_up : nullptr;
+    const uint16_t *R_dn = adp && R_up ? (const uint16_t *)adp->R_down : nullptr;
+    if ((R_up && !dR_up) || (R_dn && !dR_down)) return PMOE_ERR_INVALID_ARG;
+    if (dims.T > 0 && (!X || !dY || !ctx || !dX)) return PMOE_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(dY) || !aligned16(ctx) || !aligned16(dX) ||
+        !aligned16(d_topk_w) || !aligned16(dR_up) || !aligned16(dR_down))
+        return PMOE_ERR_INVALID_ARG;
+    const int C = std::min(chunk_C, dims.E);
+    size_t need;
+    BwdWs w = carve_bwd(ws, dims, C, &need);
+    if (!ws || ws_bytes < need || !aligned16(ws)) return PMOE_ERR_WORKSPACE;
+
+    const int d = dims.d, I = dims.inter, b = dims.block, k = dims.k, E = dims.E;
+    const int P = dims.T * k;
+    const int fmt = wts->fmt;
+    const int64_t su = adp ? adp->stride_up : 0, sd = adp ? adp->stride_down : 0;
+    const int nch = nchunks_of(dims, C);
+    const int maxt = max_tiles_of(dims);
+    const int nsets_up = su ? E : 1, nsets_dn = sd ? E : 1;
+
+    if (dims.T == 0) {
+        // empty batch: adapter gradients are zero
+        if (R_up && cudaMemsetAsync(dR_up, 0, (size_t)nsets_up * d * b * sizeof(float), stream))
+            return PMOE_ERR_CUDA;
+        if (R_dn && cudaMemsetAsync(dR_down, 0, (size_t)nsets_dn * I * b * sizeof(float), stream))
+            return PMOE_ERR_CUDA;
+        return PMOE_OK;
+    }
+
+    launch_build_tiles(E, C, kSimpleRows, 1, rt->counts, rt->offsets, rt->active, rt->num_active,
+                       w.tiles, w.chunk_tiles, w.chunk_rows, stream);
+    launch_gather_rows(P, d, k, (const uint16_t *)dY, rt->perm, w.dyp, stream);
+    launch_bwd_prep(P, I, b, (const uint16_t *)ctx, rt->perm, rt->idx, R_dn, sd, w.h, w.ht, stream);
+
+    GemmArgs g{};
+    g.kind = GK_BWD_G;
+    g.fmt = fmt;
+    g.wq = (const uint8_t *)wts->w2;
+    g.ws = (const uint8_t *)wts->s2;
+    g.wq_stride = wq_bytes(fmt, d, I);
+    g.ws_stride = ws_bytes_of(fmt, d, I);
+    g.Nst = d;
+    g.Kst = I;
+    g.A = w.dyp;
+    g.K = d;
+    g.Nout = I;
+    g.tiles = w.tiles;
+    g.chunk_tiles = w.chunk_tiles;
+    g.c0 = 0;
+    g.c1 = nch;
+    g.out = w.dht;
+    g.I = I;
+    g.w = rt->w;
+    g.perm = rt->perm;
+    g.ht = w.ht;
+    g.dtw_part = w.dtw_part;
+    {
+        ScopedTimer tm(PMOE_KT_GEMM_BWD_G, stream);
+        launch_gemm_simple(g, maxt, stream);
+    }
+    if (d_topk_w) launch_dtw_reduce(P, I / 64, w.dtw_part, rt->perm, d_topk_w, stream);
+    launch_bwd_mid(P, I, b, (const uint16_t *)ctx, w.dht, rt->perm, rt->idx, R_dn, sd, w.dgu,
+                   stream);
+    if (R_dn)
+        launch_block_outer(nsets_dn, P, I, b, w.h, nullptr, k, w.dht, sd ? rt->offsets : nullptr,
+                           dR_down, stream);
+
+    GemmArgs x{};
+    x.kind = GK_BWD_DX;
+    x.fmt = fmt;
+    x.wq = (const uint8_t *)wts->w13;
+    x.ws = (const uint8_t *)wts->s13;
+    x.wq_stride = wq_bytes(fmt, 2 * (int64_t)I, d);
+    x.ws_stride = ws_bytes_of(fmt, 2 * (int64_t)I, d);
+    x.Nst = 2 * (int64_t)I;
+    x.Kst = d;
+    x.A = w.dgu;
+    x.K = 2 * I;
+    x.Nout = d;
+    x.tiles = w.tiles;
+    x.chunk_tiles = w.chunk_tiles;
+    x.c0 = 0;
+    x.c1 = nch;
+    x.out = w.dxt;
+    x.I = I;
+    {
+        ScopedTimer tm(PMOE_KT_GEMM_BWD_DX, stream);
+        launch_gemm_simple(x, maxt, stream);
+    }
+    if (R_up)
+        launch_block_outer(nsets_up, P, d, b, (const uint16_t *)X, rt->perm, k, w.dxt,
+                           su ? rt->offsets : nullptr, dR_up, stream);
+    launch_combine_bwd(dims.T, d, k, b, w.dxt, rt->inv_perm, rt->idx, R_up, su, (uint16_t *)dX,
+                       stream);
+    return launched(stream);
+}
+
+pmoe_status moe_dequant(pmoe_wfmt fmt, const void *q, const void *s, int64_t N, int64_t K,
+                        void *out, cudaStream_t stream)
+{
+    if (N < 0 || K <= 0) return PMOE_ERR_INVALID_ARG;
+    if (fmt == PMOE_W_FP8_B128_F32) {
+        if (N % 128 || K % 128) return PMOE_ERR_INVALID_ARG;
+    } else if (fmt == PMOE_W_INT4_G32_BF16 || fmt == PMOE_W_MXFP4_G32_E8M0) {
+        if (K % 32) return PMOE_ERR_INVALID_ARG;
+    } else {
+        return PMOE_ERR_INVALID_ARG;
+    }
+    if (N == 0) return PMOE_OK;
+    if (!q || !s || !out || !aligned16(q) || !aligned16(s) || !aligned16(out))
+        return PMOE_ERR_INVALID_ARG;
+    launch_dequant(fmt, q, s, N, K, (uint16_t *)out, stream);
+    return launched(stream);
+}
+
+static bool block_ok(int b) { return b == 16 || b == 32 || b == 64 || b == 128; }
+
+pmoe_status adapter_apply(int32_t rows, int32_t dim, int32_t b, const void *X, const void *R,
+                          void *Xr, cudaStream_t stream)
+{
+    if (rows < 0 || dim <= 0 || !block_ok(b) || dim % b || dim % 8) return PMOE_ERR_INVALID_ARG;
+    if (rows == 0) return PMOE_OK;
+    if (!X || !R || !Xr || X == Xr || !aligned16(X) || !aligned16(R) || !aligned16(Xr))
+        return PMOE_ERR_INVALID_ARG;
+    launch_rotate_rows(rows, dim, b, (const uint16_t *)X, false, nullptr, 1, nullptr,
+                       (const uint16_t *)R, 0, (uint16_t *)Xr, nullptr, stream);
+    return launched(stream);
+}
+
+pmoe_status adapter_grad(int32_t rows, int32_t dim, int32_t b, const void *X, const void *dXr,
+                         const void *R, void *dX, float *dR, cudaStream_t stream)
+{
+    if (rows < 0 || dim <= 0 || !block_ok(b) || dim % b || dim % 8) return PMOE_ERR_INVALID_ARG;
+    if (!dR || (rows > 0 && (!X || !dXr || !R))) return PMOE_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(dXr) || !aligned16(R) || !aligned16(dX) || !aligned16(dR))
+        return PMOE_ERR_INVALID_ARG;
+    if (dX && rows > 0)
+        launch_adapter_grad_dx(rows, dim, b, (const uint16_t *)dXr, (const uint16_t *)R,
+                               (uint16_t *)dX, stream);
+    launch_block_outer(1, rows, dim, b, (const uint16_t *)X, nullptr, 1, (const uint16_t *)dXr,
+                       nullptr, dR, stream);
+    return launched(stream);
+}
+
+pmoe_status adapter_cayley(int32_t nblk, int32_t b, const float *S, void *R_bf16, float *R_f32,
+                           cudaStream_t stream)
+{
+    if (nblk < 0 || b < 1 || b > 128) return PMOE_ERR_INVALID_ARG;
+    if (nblk == 0) return PMOE_OK;
+    if (!S || (!R_bf16 && !R_f32)) return PMOE_ERR_INVALID_ARG;
+    launch_cayley(nblk, b, S, (uint16_t *)R_bf16, R_f32, stream);
+    return launched(stream);
+}
+
+pmoe_status adapter_cayley_grad(int32_t nblk, int32_t b, const float *S, const float *R_f32,
+                                const float *dR, float *dS, cudaStream_t stream)
+{
+    if (nblk < 0 || b < 1 || b > 128) return PMOE_ERR_INVALID_ARG;
+    if (nblk == 0) return PMOE_OK;
+    if (!S || !R_f32 || !dR || !dS) return PMOE_ERR_INVALID_ARG;
+    launch_cayley_grad(nblk, b, S, R_f32, dR, dS, stream);
+    return launched(stream);
+}
+
+}  // extern "C"

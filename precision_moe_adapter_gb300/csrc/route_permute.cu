@@ -1,0 +1,350 @@
+// route_permute.cu -- router top-k and the grouping of (token, slot) pairs
+// by expert ("Active-expert-chunked dequantization", page 1, 技艺细节: the
+// router's selected experts are gathered into fixed-size batches).
+#include "common.cuh"
+#include "launch.h"
+
+namespace pmoe {
+
+// ------------------------------------------------------------------ top-k
+// One warp per token.  Selection j picks the best element strictly after
+// selection j-1 in the total order (logit descending, id ascending), so no
+// "taken" marks are needed and ties go to the lower id.
+__global__ void k_route_topk(int T, int E, int k, const float *__restrict__ logits,
+                             const float *__restrict__ bias, int32_t *__restrict__ idx,
+                             float *__restrict__ w, float *__restrict__ logits_out)
+{
+    int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (warp >= T) return;
+    const float *l = logits + (int64_t)warp * E;
+    if (bias || logits_out) {
+        for (int e = lane; e < E; e += 32) {
+            float v = l[e] + (bias ? bias[e] : 0.f);
+            if (logits_out) logits_out[(int64_t)warp * E + e] = v;
+        }
+    }
+    float pv = __int_as_float(0x7f800000);  // previous selection (+inf, id -1)
+    int pe = -1;
+    float sel_v[32];
+    int sel_e[32];
+#pragma unroll 1
+    for (int j = 0; j < k; ++j) {
+        float bv = -__int_as_float(0x7f800000);
+        int be = 0x7fffffff;
+        for (int e = lane; e < E; e += 32) {
+            float v = l[e] + (bias ? bias[e] : 0.f);
+            bool after = (v < pv) || (v == pv && e > pe);
+            bool better = (v > bv) || (v == bv && e < be);
+            if (after && better) { bv = v; be = e; }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+        }
+        pv = bv;
+        pe = be;
+        if (j < 32) { sel_v[j] = bv; sel_e[j] = be; }
+    }
+    if (lane == 0) {
+        float den = 0.f;
+        for (int j = 0; j < k; ++j) den += expf(sel_v[j] - sel_v[0]);
+        for (int j = 0; j < k; ++j) {
+            idx[(int64_t)warp * k + j] = sel_e[j];
+            w[(int64_t)warp * k + j] = expf(sel_v[j] - sel_v[0]) / den;
+        }
+    }
+}
+
+void launch_route_topk(int T, int E, int k, const float *logits, const float *bias, int32_t *idx,
+                       float *w, float *logits_out, cudaStream_t st)
+{
+    if (T <= 0) return;
+    int threads = 256, blocks = (int)cdiv((int64_t)T * 32, threads);
+    k_route_topk<<<blocks, threads, 0, st>>>(T, E, k, logits, bias, idx, w, logits_out);
+    note_launch();
+}
+
+// ------------------------------------------------------------------ grouping
+// Pairs are processed in blocks of kPB.  Pass 1: per-block histogram.
+// Pass 2 (one CTA): counts, exclusive-scan offsets, per-(block, expert)
+// base positions, active list.  Pass 3: stable scatter; within a block the
+// rank of a pair among same-expert pairs comes from a warp match plus a
+// warp-ordered running counter in shared memory.
+constexpr int kPB = 1024;
+
+__global__ void k_hist(int P, int E, const int32_t *__restrict__ idx, int32_t *__restrict__ hist,
+                       DevErr *err)
+{
+    extern __shared__ int32_t sh[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
+    __syncthreads();
+    int p = blockIdx.x * kPB + threadIdx.x;
+    if (p < P) {
+        int e = idx[p];
+        if (e >= 0 && e < E) atomicAdd(&sh[e], 1);
+        else record_error(err, PMOE_ERR_BAD_INDEX, p, e);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(int64_t)blockIdx.x * E + e] = sh[e];
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim = 1024).
+__device__ int block_excl_scan(int v, int *total)
+{
+    __shared__ int warp_sums[32];
+    int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int s = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        warp_sums[lane] = s;
+    }
+    __syncthreads();
+    int base = wid ? warp_sums[wid - 1] : 0;
+    if (total) *total = warp_sums[31];
+    __syncthreads();
+    return base + x - v;
+}
+
+__global__ void __launch_bounds__(1024) k_scan(int nb, int E, int32_t *__restrict__ hist,
+                                               int32_t *__restrict__ counts,
+                                               int32_t *__restrict__ offsets,
+                                               int32_t *__restrict__ active,
+                                               int32_t *__restrict__ num_active)
+{
+    // each thread owns experts [t*per, t*per + per)
+    int per = (E + 1023) / 1024;
+    int e0 = threadIdx.x * per;
+    int my_cnt = 0, my_act = 0;
+    for (int i = 0; i < per; ++i) {
+        int e = e0 + i;
+        if (e >= E) break;
+        int c = 0;
+        for (int b = 0; b < nb; ++b) c += hist[(int64_t)b * E + e];
+        counts[e] = c;
+        my_cnt += c;
+        my_act += c > 0;
+    }
+    int tot_cnt, tot_act;
+    int off = block_excl_scan(my_cnt, &tot_cnt);
+    int apos = block_excl_scan(my_act, &tot_act);
+    for (int i = 0; i < per; ++i) {
+        int e = e0 + i;
+        if (e >= E) break;
+        int c = counts[e];
+        offsets[e] = off;
+        int run = off;
+        for (int b = 0; b < nb; ++b) {
+            int h = hist[(int64_t)b * E + e];
+            hist[(int64_t)b * E + e] = run;   // base position of (block b, expert e)
+            run += h;
+        }
+        off += c;
+        if (c > 0) active[apos++] = e;
+    }
+    if (threadIdx.x == 0) {
+        offsets[E] = tot_cnt;
+        *num_active = tot_act;
+    }
+    for (int e = tot_act + threadIdx.x; e < E; e += blockDim.x) active[e] = -1;
+}
+
+__global__ void __launch_bounds__(kPB) k_scatter(int P, int E, const int32_t *__restrict__ idx,
+                                                 const int32_t *__restrict__ base,
+                                                 int32_t *__restrict__ perm,
+                                                 int32_t *__restrict__ inv_perm)
+{
+    extern __shared__ int32_t cnt[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = base[(int64_t)blockIdx.x * E + e];
+    int p = blockIdx.x * kPB + threadIdx.x;
+    int e = p < P ? idx[p] : -1;
+    bool valid = e >= 0 && e < E;
+    int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    unsigned mask = __match_any_sync(0xffffffffu, valid ? e : -1);
+    int rank = __popc(mask & ((1u << lane) - 1u));
+    int leader = __ffs(mask) - 1;
+    int pos = 0;
+    for (int w = 0; w < kPB / 32; ++w) {
+        __syncthreads();
+        if (wid == w) {
+            int old = 0;
+            if (lane == leader && valid) {
+                old = cnt[e];
+                cnt[e] = old + __popc(mask);
+            }
+            old = __shfl_sync(0xffffffffu, old, leader);
+            pos = old + rank;
+        }
+    }
+    if (valid) {
+        perm[pos] = p;
+        inv_perm[p] = pos;
+    } else if (p < P) {
+        inv_perm[p] = -1;
+    }
+}
+
+size_t permute_ws_bytes(int P, int E)
+{
+    int nb = (int)cdiv(P > 0 ? P : 1, kPB);
+    return (size_t)nb * E * sizeof(int32_t);
+}
+
+void launch_permute(int P, int E, const int32_t *idx, int32_t *counts, int32_t *offsets,
+                    int32_t *perm, int32_t *inv_perm, int32_t *active, int32_t *num_active,
+                    int32_t *hist, DevErr *err, cudaStream_t st)
+{
+    int nb = (int)cdiv(P, kPB);
+    size_t sm = (size_t)E * sizeof(int32_t);
+    if (nb > 0) {
+        k_hist<<<nb, kPB, sm, st>>>(P, E, idx, hist, err);
+        note_launch();
+    }
+    k_scan<<<1, 1024, 0, st>>>(nb, E, hist, counts, offsets, active, num_active);
+    note_launch();
+    if (nb > 0) {
+        k_scatter<<<nb, kPB, sm, st>>>(P, E, idx, hist, perm, inv_perm);
+        note_launch();
+    }
+}
+
+// ------------------------------------------------------------------ tiles
+// Work list: for the active experts in ascending order, chunk c = active
+// positions [c*C, c*C + C), each expert's rows cut into ceil(n / max_rows)
+// tiles of near-equal size (multiples of `align` rows, last one ragged).
+// Also writes chunk_tiles[c] (first tile of chunk c, nchunks + 1 entries)
+// and chunk_rows[c] = first expert-sorted row of chunk c (nchunks + 1).
+__global__ void __launch_bounds__(1024) k_build_tiles(int E, int C, int max_rows, int align,
+                                                      const int32_t *__restrict__ counts,
+                                                      const int32_t *__restrict__ offsets,
+                                                      const int32_t *__restrict__ active,
+                                                      const int32_t *__restrict__ num_active,
+                                                      Tile *__restrict__ tiles,
+                                                      int32_t *__restrict__ chunk_tiles,
+                                                      int32_t *__restrict__ chunk_rows)
+{
+    int na = *num_active;
+    int nchunks_max = (E + C - 1) / C;
+    int per = (E + 1023) / 1024;
+    int a0 = threadIdx.x * per;
+    int my = 0;
+    for (int i = 0; i < per; ++i) {
+        int a = a0 + i;
+        if (a >= na) break;
+        int n = counts[active[a]];
+        my += (n + max_rows - 1) / max_rows;
+    }
+    int total;
+    int t = block_excl_scan(my, &total);
+    for (int i = 0; i < per; ++i) {
+        int a = a0 + i;
+        if (a >= na) break;
+        int e = active[a];
+        int n = counts[e];
+        int nt = (n + max_rows - 1) / max_rows;
+        int sz = (n + nt - 1) / nt;
+        sz = (sz + align - 1) / align * align;
+        int chunk = a / C, slot = a % C;
+        if (slot == 0) {
+            chunk_tiles[chunk] = t;
+            chunk_rows[chunk] = offsets[e];
+        }
+        for (int j = 0; j < nt; ++j) {
+            int r0 = j * sz;
+            Tile tl;
+            tl.expert = e;
+            tl.row0 = offsets[e] + r0;
+            tl.nrows = min(sz, n - r0);
+            tl.chunk = (chunk << 16) | slot;
+            tiles[t++] = tl;
+        }
+    }
+    __syncthreads();
+    // chunks past the active experts are empty
+    int nch = (na + C - 1) / C;
+    for (int c = nch + threadIdx.x; c <= nchunks_max; c += blockDim.x) {
+        chunk_tiles[c] = total;
+        chunk_rows[c] = offsets[E];
+    }
+}
+
+void launch_build_tiles(int E, int C, int max_rows, int align, const int32_t *counts,
+                        const int32_t *offsets, const int32_t *active, const int32_t *num_active,
+                        Tile *tiles, int32_t *chunk_tiles, int32_t *chunk_rows, cudaStream_t st)
+{
+    k_build_tiles<<<1, 1024, 0, st>>>(E, C, max_rows, align, counts, offsets, active, num_active,
+                                      tiles, chunk_tiles, chunk_rows);
+    note_launch();
+}
+
+// ------------------------------------------------------------------ router logits
+// FP32 logits = X Wr on CUDA cores: 64 x 64 output tile per CTA, 4 x 4 per
+// thread, K step 32.  (X bf16 [T, d], Wr f32 [d, E].)
+__global__ void __launch_bounds__(256) k_logits_f32(int T, int d, int E,
+                                                    const uint16_t *__restrict__ X,
+                                                    const float *__restrict__ Wr,
+                                                    float *__restrict__ out)
+{
+    __shared__ float As[32][64 + 4];
+    __shared__ float Bs[32][64 + 4];
+    int t0 = blockIdx.y * 64, e0 = blockIdx.x * 64;
+    int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < d; k0 += 32) {
+        for (int i = threadIdx.x; i < 64 * 32; i += 256) {
+            int r = i / 32, c = i % 32;
+            int t = t0 + r;
+            As[c][r] = t < T ? bf2f(X[(int64_t)t * d + k0 + c]) : 0.f;
+            int kk = i / 64, e = e0 + i % 64;
+            Bs[kk][i % 64] = e < E ? Wr[(int64_t)(k0 + kk) * E + e] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int kk = 0; kk < 32; ++kk) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int t = t0 + ty * 4 + i;
+        if (t >= T) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            int e = e0 + tx * 4 + j;
+            if (e < E) out[(int64_t)t * E + e] = acc[i][j];
+        }
+    }
+}
+
+void launch_logits_f32(int T, int d, int E, const uint16_t *X, const float *Wr, float *out,
+                       cudaStream_t st)
+{
+    if (T <= 0) return;
+    dim3 grid((unsigned)cdiv(E, 64), (unsigned)cdiv(T, 64));
+    k_logits_f32<<<grid, 256, 0, st>>>(T, d, E, X, Wr, out);
+    note_launch();
+}
+
+}  // namespace pmoe
