@@ -162,7 +162,8 @@ def host_inputs(cfg, with_rbits):
 
 
 def sample_tokens(cfg, threads):
-    return max(1, min(cfg.T, (2 * threads) // cfg.k))
+    """Tokens of the CPU-baseline sample: about 10-30 s of oracle work."""
+    return max(1, min(cfg.T, (8 * threads) // cfg.k))
 
 
 def run_reference(args, cfg, rank):

@@ -210,6 +210,25 @@ pmoe_status moe_dequant(pmoe_wfmt fmt, const void *q, const void *s, int64_t N, 
                         void *out, cudaStream_t stream);
 
 /*
+ * moe_grouped_gemm -- the grouped GEMM step alone (page 1, 技艺细节:
+ * "grouped GEMM" over the dequantized experts), on the tensor cores with
+ * the weights dequantized tile by tile in shared memory.  Rows
+ * offsets[e] .. offsets[e+1]-1 of A belong to expert e.
+ *   trans == 0: out[r] = bf16(A[r] W_e^T), A bf16 [rows, K], out [rows, N]
+ *   trans == 1: out[r] = bf16(A[r] W_e),   A bf16 [rows, N], out [rows, K]
+ * with W_e the [N, K] matrix of expert e in `fmt` (q, s laid out as in
+ * pmoe_wfmt, experts consecutive).  offsets: device int32 [E+1],
+ * nondecreasing, offsets[0] = 0, offsets[E] = rows.  N % 64 == 0,
+ * K % 64 == 0 (FP8: both % 128), rows >= 0, E <= 4096.
+ *   ws  >= moe_grouped_gemm_ws_bytes(E, rows) bytes.
+ */
+pmoe_status moe_grouped_gemm(pmoe_wfmt fmt, const void *q, const void *s, int32_t E, int32_t N,
+                             int32_t K, int trans, const void *A, const int32_t *offsets,
+                             int32_t rows, void *out, void *ws, size_t ws_bytes,
+                             cudaStream_t stream);
+size_t moe_grouped_gemm_ws_bytes(int32_t E, int32_t rows);
+
+/*
  * adapter_apply -- Xr = bf16(X blockdiag(R)) (page 2, 机制拆解: the OFT
  * adapter as a local orthogonal transform).  X bf16 [rows, dim], R bf16
  * [dim/b, b, b], Xr bf16 [rows, dim] (must not alias X).  dim % b == 0,

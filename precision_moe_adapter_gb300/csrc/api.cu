@@ -1,6 +1,7 @@
 // api.cu -- the extern "C" entry points of libpmoe (declared in pmoe.h):
 // host-side validation, workspace layout and the order of launches.
 #include <atomic>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -107,8 +108,30 @@ static bool fmt_ok(const pmoe_dims &d, int fmt)
 static int nchunks_of(const pmoe_dims &d, int C) { return (int)cdiv(d.E, C); }
 static int max_tiles_of(const pmoe_dims &d) { return (int)(cdiv((int64_t)d.T * d.k, 16) + d.E); }
 
-// Tile rows of the CUDA-core grouped GEMM.
-constexpr int kSimpleRows = 64;
+// Grouped GEMM engine: the tcgen05 kernel (token tiles of up to 256 rows,
+// multiples of 16); PMOE_GEMM=simple selects the CUDA-core kernel (64-row
+// tiles) for comparison runs.
+static bool use_simple()
+{
+    static int v = -1;
+    if (v < 0) {
+        const char *e = getenv("PMOE_GEMM");
+        v = (e && !strcmp(e, "simple")) ? 1 : 0;
+    }
+    return v == 1;
+}
+static int tile_rows() { return use_simple() ? 64 : 256; }
+static int tile_align() { return use_simple() ? 1 : 16; }
+static int dtw_parts(int I) { return use_simple() ? I / 64 : I / 32; }
+
+static pmoe_status run_gemm(const GemmArgs &g, int maxt, int64_t P, DevErr *err, cudaStream_t st)
+{
+    if (use_simple()) {
+        launch_gemm_simple(g, maxt, st);
+        return PMOE_OK;
+    }
+    return launch_gemm_tc(g, P, err, st) ? PMOE_OK : PMOE_ERR_CUDA;
+}
 
 struct FwdWs {
     DevErr *err;
@@ -157,7 +180,7 @@ static BwdWs carve_bwd(void *ws, const pmoe_dims &d, int C, size_t *bytes)
     w.dht = c.take<uint16_t>(P * d.inter);
     w.dgu = c.take<uint16_t>(P * 2 * d.inter);
     w.dxt = c.take<uint16_t>(P * d.d);
-    w.dtw_part = c.take<float>(P * (d.inter / 64));
+    w.dtw_part = c.take<float>(P * (d.inter / 32));
     if (bytes) *bytes = c.off;
     return w;
 }
@@ -353,8 +376,9 @@ pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const p
     const int nch = nchunks_of(dims, C);
     const int maxt = max_tiles_of(dims);
 
-    launch_build_tiles(E, C, kSimpleRows, 1, rt->counts, rt->offsets, rt->active, rt->num_active,
-                       w.tiles, w.chunk_tiles, w.chunk_rows, stream);
+    launch_build_tiles(E, C, tile_rows(), tile_align(), rt->counts, rt->offsets, rt->active,
+                       rt->num_active, w.tiles, w.chunk_tiles, w.chunk_rows, stream);
+    pmoe_status gs = PMOE_OK;
     // x~ for every pair, in expert-sorted order (gather + up rotation)
     launch_rotate_rows(P, d, b, (const uint16_t *)X, true, rt->perm, k, rt->idx, R_up, su, w.xt,
                        nullptr, stream);
@@ -397,13 +421,13 @@ pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const p
         gu.c1 = dn.c1 = nch;
         {
             ScopedTimer tm(PMOE_KT_GEMM_GATE_UP, stream);
-            launch_gemm_simple(gu, maxt, stream);
+            if ((gs = run_gemm(gu, maxt, P, w.err, stream)) != PMOE_OK) return gs;
         }
         launch_rotate_rows(P, I, b, w.h, false, rt->perm, k, rt->idx, R_dn, sd, w.ht, nullptr,
                            stream);
         {
             ScopedTimer tm(PMOE_KT_GEMM_DOWN, stream);
-            launch_gemm_simple(dn, maxt, stream);
+            if ((gs = run_gemm(dn, maxt, P, w.err, stream)) != PMOE_OK) return gs;
         }
     } else {
         const int64_t slot_bytes = 3 * (int64_t)I * d * 2;
@@ -421,13 +445,13 @@ pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const p
             gu.c1 = dn.c1 = c + 1;
             {
                 ScopedTimer tm(PMOE_KT_GEMM_GATE_UP, stream);
-                launch_gemm_simple(gu, maxt, stream);
+                if ((gs = run_gemm(gu, maxt, P, w.err, stream)) != PMOE_OK) return gs;
             }
             launch_rotate_rows(P, I, b, w.h, false, rt->perm, k, rt->idx, R_dn, sd, w.ht,
                                w.chunk_rows + c, stream);
             {
                 ScopedTimer tm(PMOE_KT_GEMM_DOWN, stream);
-                launch_gemm_simple(dn, maxt, stream);
+                if ((gs = run_gemm(dn, maxt, P, w.err, stream)) != PMOE_OK) return gs;
             }
         }
     }
@@ -473,8 +497,9 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
         return PMOE_OK;
     }
 
-    launch_build_tiles(E, C, kSimpleRows, 1, rt->counts, rt->offsets, rt->active, rt->num_active,
-                       w.tiles, w.chunk_tiles, w.chunk_rows, stream);
+    launch_build_tiles(E, C, tile_rows(), tile_align(), rt->counts, rt->offsets, rt->active,
+                       rt->num_active, w.tiles, w.chunk_tiles, w.chunk_rows, stream);
+    pmoe_status gs = PMOE_OK;
     launch_gather_rows(P, d, k, (const uint16_t *)dY, rt->perm, w.dyp, stream);
     launch_bwd_prep(P, I, b, (const uint16_t *)ctx, rt->perm, rt->idx, R_dn, sd, w.h, w.ht, stream);
 
@@ -502,9 +527,9 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
     g.dtw_part = w.dtw_part;
     {
         ScopedTimer tm(PMOE_KT_GEMM_BWD_G, stream);
-        launch_gemm_simple(g, maxt, stream);
+        if ((gs = run_gemm(g, maxt, P, w.err, stream)) != PMOE_OK) return gs;
     }
-    if (d_topk_w) launch_dtw_reduce(P, I / 64, w.dtw_part, rt->perm, d_topk_w, stream);
+    if (d_topk_w) launch_dtw_reduce(P, dtw_parts(I), w.dtw_part, rt->perm, d_topk_w, stream);
     launch_bwd_mid(P, I, b, (const uint16_t *)ctx, w.dht, rt->perm, rt->idx, R_dn, sd, w.dgu,
                    stream);
     if (R_dn)
@@ -531,7 +556,7 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
     x.I = I;
     {
         ScopedTimer tm(PMOE_KT_GEMM_BWD_DX, stream);
-        launch_gemm_simple(x, maxt, stream);
+        if ((gs = run_gemm(x, maxt, P, w.err, stream)) != PMOE_OK) return gs;
     }
     if (R_up)
         launch_block_outer(nsets_up, P, d, b, (const uint16_t *)X, rt->perm, k, w.dxt,
@@ -556,6 +581,78 @@ pmoe_status moe_dequant(pmoe_wfmt fmt, const void *q, const void *s, int64_t N, 
     if (!q || !s || !out || !aligned16(q) || !aligned16(s) || !aligned16(out))
         return PMOE_ERR_INVALID_ARG;
     launch_dequant(fmt, q, s, N, K, (uint16_t *)out, stream);
+    return launched(stream);
+}
+
+struct GgWs {
+    DevErr *err;
+    Tile *tiles;
+    int32_t *chunk_tiles, *chunk_rows, *counts, *active, *num_active;
+};
+static GgWs carve_gg(void *ws, int E, int rows, size_t *bytes)
+{
+    Carver c(ws);
+    GgWs w;
+    w.err = c.take<DevErr>(kHdrBytes / sizeof(DevErr));
+    w.tiles = c.take<Tile>(cdiv(rows, 16) + E);
+    w.chunk_tiles = c.take<int32_t>(4);
+    w.chunk_rows = c.take<int32_t>(4);
+    w.counts = c.take<int32_t>(E);
+    w.active = c.take<int32_t>(E);
+    w.num_active = c.take<int32_t>(1);
+    if (bytes) *bytes = c.off;
+    return w;
+}
+
+size_t moe_grouped_gemm_ws_bytes(int32_t E, int32_t rows)
+{
+    if (E <= 0 || rows < 0) return 0;
+    size_t b;
+    carve_gg(nullptr, E, rows, &b);
+    return b;
+}
+
+pmoe_status moe_grouped_gemm(pmoe_wfmt fmt, const void *q, const void *s, int32_t E, int32_t N,
+                             int32_t K, int trans, const void *A, const int32_t *offsets,
+                             int32_t rows, void *out, void *ws, size_t ws_bytes,
+                             cudaStream_t stream)
+{
+    if (E <= 0 || E > 4096 || N <= 0 || K <= 0 || N % 64 || K % 64 || rows < 0)
+        return PMOE_ERR_INVALID_ARG;
+    if (fmt != PMOE_W_INT4_G32_BF16 && fmt != PMOE_W_MXFP4_G32_E8M0 && fmt != PMOE_W_FP8_B128_F32)
+        return PMOE_ERR_INVALID_ARG;
+    if (fmt == PMOE_W_FP8_B128_F32 && (N % 128 || K % 128)) return PMOE_ERR_INVALID_ARG;
+    if (trans != 0 && trans != 1) return PMOE_ERR_INVALID_ARG;
+    if (!q || !s || !offsets || (rows > 0 && (!A || !out))) return PMOE_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(s) || !aligned16(A) || !aligned16(out))
+        return PMOE_ERR_INVALID_ARG;
+    size_t need;
+    GgWs w = carve_gg(ws, E, rows, &need);
+    if (!ws || ws_bytes < need || !aligned16(ws)) return PMOE_ERR_WORKSPACE;
+    if (rows == 0) return PMOE_OK;
+    launch_offsets_to_active(E, rows, offsets, w.counts, w.active, w.num_active, w.err, stream);
+    launch_build_tiles(E, E, tile_rows(), tile_align(), w.counts, offsets, w.active, w.num_active,
+                       w.tiles, w.chunk_tiles, w.chunk_rows, stream);
+    GemmArgs g{};
+    g.kind = trans ? GK_BWD_DX : GK_FWD_DOWN;
+    g.fmt = fmt;
+    g.wq = (const uint8_t *)q;
+    g.ws = (const uint8_t *)s;
+    g.wq_stride = wq_bytes(fmt, N, K);
+    g.ws_stride = ws_bytes_of(fmt, N, K);
+    g.Nst = N;
+    g.Kst = K;
+    g.A = (const uint16_t *)A;
+    g.K = trans ? N : K;
+    g.Nout = trans ? K : N;
+    g.tiles = w.tiles;
+    g.chunk_tiles = w.chunk_tiles;
+    g.c0 = 0;
+    g.c1 = 1;
+    g.out = (uint16_t *)out;
+    g.I = N;
+    pmoe_status gs = run_gemm(g, (int)(cdiv(rows, 16) + E), rows, w.err, stream);
+    if (gs != PMOE_OK) return gs;
     return launched(stream);
 }
 

@@ -1,0 +1,78 @@
+// gemm_tc.cu -- shared host helpers of the tcgen05 grouped GEMM: TMA
+// descriptors (cuTensorMapEncodeTiled reached through the runtime's driver
+// entry point, so the library does not link libcuda) and the dispatch by
+// weight format.
+#include <mutex>
+
+#include "gemm_tc_host.cuh"
+
+namespace pmoe {
+
+bool launch_gemm_tc_int4(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st);
+bool launch_gemm_tc_mxfp4(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st);
+bool launch_gemm_tc_fp8(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st);
+bool launch_gemm_tc_bf16(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st);
+
+namespace tc {
+
+typedef CUresult (*EncodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiled encoder()
+{
+    static EncodeTiled fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiled)p;
+    });
+    return fn;
+}
+
+// 2-D BF16 row-major [rows, cols] tensor, box of 32 rows x 64 columns
+// (128 bytes: one swizzle row), 128-byte swizzle, zero fill out of bounds.
+bool make_rows_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t cols)
+{
+    EncodeTiled enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBoxRows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms()
+{
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 1;
+    }
+    return n;
+}
+
+}  // namespace tc
+
+bool launch_gemm_tc(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st)
+{
+    switch (g.fmt) {
+    case PMOE_W_INT4_G32_BF16: return launch_gemm_tc_int4(g, P, err, st);
+    case PMOE_W_MXFP4_G32_E8M0: return launch_gemm_tc_mxfp4(g, P, err, st);
+    case PMOE_W_FP8_B128_F32: return launch_gemm_tc_fp8(g, P, err, st);
+    case kFmtBF16: return launch_gemm_tc_bf16(g, P, err, st);
+    }
+    return false;
+}
+
+}  // namespace pmoe

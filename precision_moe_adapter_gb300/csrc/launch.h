@@ -80,6 +80,13 @@ struct GemmArgs {
 };
 void launch_gemm_simple(const GemmArgs &a, int max_tiles, cudaStream_t st);
 
+// gemm_tc.cu: tcgen05 grouped GEMM (returns false if the request cannot be
+// launched, e.g. the TMA descriptor could not be encoded)
+bool launch_gemm_tc(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st);
+// counts / active / num_active of experts from row offsets [E+1]
+void launch_offsets_to_active(int E, int rows, const int32_t *offsets, int32_t *counts,
+                              int32_t *active, int32_t *num_active, DevErr *err, cudaStream_t st);
+
 // layer.cu
 void launch_combine(int T, int d, int k, const uint16_t *o, const int32_t *inv_perm,
                     const float *w, uint16_t *Y, cudaStream_t st);

@@ -290,6 +290,51 @@ void launch_build_tiles(int E, int C, int max_rows, int align, const int32_t *co
     note_launch();
 }
 
+// counts[e] = offsets[e+1] - offsets[e]; active = experts with rows, ascending.
+// Offsets that are not a nondecreasing 0..rows sequence record
+// PMOE_ERR_BAD_INDEX and leave every expert empty (nothing is read).
+__global__ void __launch_bounds__(1024) k_offsets_to_active(int E, int rows,
+                                                            const int32_t *__restrict__ offsets,
+                                                            int32_t *__restrict__ counts,
+                                                            int32_t *__restrict__ active,
+                                                            int32_t *__restrict__ num_active,
+                                                            DevErr *err)
+{
+    __shared__ int bad;
+    if (threadIdx.x == 0) bad = (offsets[0] != 0 || offsets[E] != rows);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        if (offsets[e + 1] < offsets[e]) bad = 1;
+    __syncthreads();
+    if (bad && threadIdx.x == 0) record_error(err, PMOE_ERR_BAD_INDEX, -1, -1);
+    int per = (E + 1023) / 1024;
+    int e0 = threadIdx.x * per;
+    int my = 0;
+    for (int i = 0; i < per; ++i) {
+        int e = e0 + i;
+        if (e >= E) break;
+        int c = bad ? 0 : offsets[e + 1] - offsets[e];
+        counts[e] = c;
+        my += c > 0;
+    }
+    int tot;
+    int pos = block_excl_scan(my, &tot);
+    for (int i = 0; i < per; ++i) {
+        int e = e0 + i;
+        if (e >= E) break;
+        if (counts[e] > 0) active[pos++] = e;
+    }
+    if (threadIdx.x == 0) *num_active = tot;
+    for (int e = tot + threadIdx.x; e < E; e += blockDim.x) active[e] = -1;
+}
+
+void launch_offsets_to_active(int E, int rows, const int32_t *offsets, int32_t *counts,
+                              int32_t *active, int32_t *num_active, DevErr *err, cudaStream_t st)
+{
+    k_offsets_to_active<<<1, 1024, 0, st>>>(E, rows, offsets, counts, active, num_active, err);
+    note_launch();
+}
+
 // ------------------------------------------------------------------ router logits
 // FP32 logits = X Wr on CUDA cores: 64 x 64 output tile per CTA, 4 x 4 per
 // thread, K step 32.  (X bf16 [T, d], Wr f32 [d, E].)

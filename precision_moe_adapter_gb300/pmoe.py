@@ -25,7 +25,8 @@ OP_PERMUTE, OP_FORWARD, OP_BACKWARD = 0, 1, 2
 EXPORTS = ("moe_route", "moe_permute", "moe_chunked_forward", "moe_backward_data", "moe_dequant",
            "adapter_apply", "adapter_grad", "adapter_cayley", "adapter_cayley_grad",
            "moe_workspace_bytes", "moe_scratch_bytes", "moe_clear_status", "moe_query_status",
-           "pmoe_status_string", "pmoe_launch_count", "pmoe_kernel_timing", "pmoe_kernel_time")
+           "pmoe_status_string", "pmoe_launch_count", "pmoe_kernel_timing", "pmoe_kernel_time",
+           "moe_grouped_gemm", "moe_grouped_gemm_ws_bytes")
 KT_GEMM_GATE_UP, KT_GEMM_DOWN, KT_GEMM_BWD_G, KT_GEMM_BWD_DX, KT_ROUTER = 0, 1, 2, 3, 4
 
 
@@ -83,6 +84,7 @@ def _declare(L):
         "moe_chunked_forward": [D, PW, PA, PR, p, i32, ctypes.c_int, p, p, p, sz, p],
         "moe_backward_data": [D, PW, PA, PR, p, p, p, i32, p, p, p, p, p, sz, p],
         "moe_dequant": [ctypes.c_int, p, p, i64, i64, p, p],
+        "moe_grouped_gemm": [ctypes.c_int, p, p, i32, i32, i32, ctypes.c_int, p, p, i32, p, p, sz, p],
         "adapter_apply": [i32, i32, i32, p, p, p, p],
         "adapter_grad": [i32, i32, i32, p, p, p, p, p, p],
         "adapter_cayley": [i32, i32, p, p, p, p],
@@ -96,6 +98,8 @@ def _declare(L):
         f.restype = st
     L.moe_workspace_bytes.argtypes = [D, ctypes.c_int, i32, ctypes.c_int]
     L.moe_workspace_bytes.restype = sz
+    L.moe_grouped_gemm_ws_bytes.argtypes = [i32, i32]
+    L.moe_grouped_gemm_ws_bytes.restype = sz
     L.moe_scratch_bytes.argtypes = [D, i32, ctypes.c_int]
     L.moe_scratch_bytes.restype = sz
     L.pmoe_status_string.argtypes = [st]
@@ -194,6 +198,16 @@ def moe_backward_data(dm, wts: Weights, adp, rt: Routing, X, dY, ctx, chunk_C, d
 def moe_dequant(fmt, q, s, N, K, out, stream=None):
     _check(lib().moe_dequant(fmt, _ptr(q), _ptr(s), N, K, _ptr(out), _stream(stream)),
            "moe_dequant")
+
+
+def moe_grouped_gemm_ws_bytes(E: int, rows: int) -> int:
+    return lib().moe_grouped_gemm_ws_bytes(E, rows)
+
+
+def moe_grouped_gemm(fmt, q, s, E, N, K, trans, A, offsets, rows, out, ws, stream=None):
+    _check(lib().moe_grouped_gemm(fmt, _ptr(q), _ptr(s), E, N, K, trans, _ptr(A), _ptr(offsets),
+                                  rows, _ptr(out), _ptr(ws), _nbytes(ws), _stream(stream)),
+           "moe_grouped_gemm")
 
 
 def adapter_apply(rows, dim, b, X, R, Xr, stream=None):

@@ -240,10 +240,13 @@ def test_cayley_and_grad(b, std):
     assert np.max(np.abs(rf - R64)) < 2e-6
     for blk in range(nblk):
         assert np.max(np.abs(rf[blk].T.astype(np.float64) @ rf[blk] - np.eye(b))) < 1e-5
+    # R_bf16 = bf16(R_f32) with |R_f32 - R| <= eps: within half a BF16 step
+    # of (|R| + eps) plus eps of the exact R
+    eps = 2e-6
     rb = bits_to_f64(t2np_bits(Rb))
+    half_ulp = np.ldexp(1.0, np.frexp(np.abs(R64) + eps)[1] - 9)
+    assert np.all(np.abs(rb - R64) <= half_ulp + eps)
     ref = bits_to_f64(oracle.bf16_round(R64.ravel())).reshape(R64.shape)
-    ulp = np.ldexp(1.0, np.frexp(np.maximum(np.abs(R64), 2.0 ** -126))[1] - 8)
-    assert np.all(np.abs(rb - ref) <= ulp)          # one BF16 step at most, at rounding edges
     assert np.mean(rb == ref) > 0.99
     want = oracle.cayley_grad(S, G)
     assert_close(dS.cpu().numpy(), want, "dS", rel_fro=1e-5, max_abs=1e-4)
