@@ -76,7 +76,7 @@ def bytes_of(cfg, counts):
         wq = 3 * d * I // 2 + 3 * d * (I // 32) * (2 if cfg.fmt == gi.INT4 else 1)
     adp = (d + I) * b * 2 if cfg.adapter == "per_expert" else 0
     act_f = cfg.T * d * 2 * 2 + d * cfg.E * 4          # X, Y, Wr
-    act_b = cfg.T * d * 2 * 3 + cfg.P * 2 * I * 2      # X, dY, dX, ctx
+    act_b = cfg.T * d * 2 * 3 + cfg.P * 3 * I * 2      # X, dY, dX, ctx
     return na * (wq + adp) * 2 + act_f + act_b
 
 
@@ -249,7 +249,7 @@ def main():
     rt = L.new_routing()
     Y = torch.empty_like(X)
     dX = torch.empty_like(X)
-    ctx = torch.empty((cfg.P, 2 * cfg.I), dtype=torch.int16, device=dev)
+    ctx = torch.empty((cfg.P, 3 * cfg.I), dtype=torch.int16, device=dev)
     dtw = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
     dRu, dRd = L.grads()
     dSu = None if L.S_up is None else torch.empty_like(L.S_up)

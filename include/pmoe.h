@@ -164,7 +164,7 @@ pmoe_status moe_permute(pmoe_dims dims, const int32_t *idx, const pmoe_routing *
  *   o  = h~ W_down[e]^T
  * and finally Y_t = bf16(sum_j w[t,j] o_(t,j)), slots summed in order.
  *   X   bf16 [T, d] (in)         Y bf16 [T, d] (out)
- *   ctx bf16 [P, 2I] or NULL: when given, receives [g | u] per pair in
+ *   ctx bf16 [P, 3I] or NULL: when given, receives [g | u | h] per pair in
  *       expert-sorted order (row i = pair perm[i]) for moe_backward_data
  *   chunk_C >= 1 experts per chunk (>= E means one chunk)
  *   ws  >= moe_workspace_bytes(dims, PMOE_OP_FORWARD, chunk_C, mode)
@@ -185,7 +185,7 @@ pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const p
  *   dh = dh~ R_down^T;  dg = dh u s(g)(1 + g(1 - s(g)));  du = dh silu(g)
  *   dx~ = dg W_gate + du W_up   dR_up[e] += x_blk^T dx~_blk
  *   dx_pair = dx~ R_up^T        dX_t = bf16(sum_j dx_pair), slots in order
- *   X, dY   bf16 [T, d] (in)    ctx bf16 [P, 2I] from the forward (in)
+ *   X, dY   bf16 [T, d] (in)    ctx bf16 [P, 3I] from the forward (in)
  *   dX      bf16 [T, d] (out)
  *   d_topk_w f32 [T, k] or NULL (out)
  *   dR_up   f32 shaped like R_up, dR_down f32 shaped like R_down (out,

@@ -106,37 +106,48 @@ static bool fmt_ok(const pmoe_dims &d, int fmt)
 }
 
 static int nchunks_of(const pmoe_dims &d, int C) { return (int)cdiv(d.E, C); }
+// Work-list sizes: GEMM token tiles (<= 256 rows, multiples of 16) and
+// rotation tiles (<= 64 rows), each at most rows/16 (rows/64) + E.
 static int max_tiles_of(const pmoe_dims &d) { return (int)(cdiv((int64_t)d.T * d.k, 16) + d.E); }
-
-// Grouped GEMM engine: the tcgen05 kernel (token tiles of up to 256 rows,
-// multiples of 16); PMOE_GEMM=simple selects the CUDA-core kernel (64-row
-// tiles) for comparison runs.
-static bool use_simple()
+static int max_rot_tiles_of(const pmoe_dims &d)
 {
-    static int v = -1;
-    if (v < 0) {
-        const char *e = getenv("PMOE_GEMM");
-        v = (e && !strcmp(e, "simple")) ? 1 : 0;
-    }
-    return v == 1;
+    return (int)(cdiv((int64_t)d.T * d.k, kRotTileRows) + d.E);
 }
-static int tile_rows() { return use_simple() ? 64 : 256; }
-static int tile_align() { return use_simple() ? 1 : 16; }
-static int dtw_parts(int I) { return use_simple() ? I / 64 : I / 32; }
+constexpr int kGemmRows = 256, kGemmAlign = 16;
 
-static pmoe_status run_gemm(const GemmArgs &g, int maxt, int64_t P, DevErr *err, cudaStream_t st)
+static pmoe_status run_gemm(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st)
 {
-    if (use_simple()) {
-        launch_gemm_simple(g, maxt, st);
-        return PMOE_OK;
-    }
     return launch_gemm_tc(g, P, err, st) ? PMOE_OK : PMOE_ERR_CUDA;
+}
+
+// Work lists of one call: GEMM tiles per chunk and rotation tiles per chunk.
+struct Lists {
+    Tile *tiles, *rtiles;
+    int32_t *chunk_tiles, *chunk_rows, *chunk_rtiles, *chunk_rrows;
+};
+static Lists carve_lists(Carver &c, const pmoe_dims &d, int C)
+{
+    Lists l;
+    l.tiles = c.take<Tile>(max_tiles_of(d));
+    l.rtiles = c.take<Tile>(max_rot_tiles_of(d));
+    l.chunk_tiles = c.take<int32_t>(nchunks_of(d, C) + 2);
+    l.chunk_rows = c.take<int32_t>(nchunks_of(d, C) + 2);
+    l.chunk_rtiles = c.take<int32_t>(nchunks_of(d, C) + 2);
+    l.chunk_rrows = c.take<int32_t>(nchunks_of(d, C) + 2);
+    return l;
+}
+static void build_lists(const Lists &l, const pmoe_dims &d, int C, const pmoe_routing *rt,
+                        cudaStream_t st)
+{
+    launch_build_tiles(d.E, C, kGemmRows, kGemmAlign, rt->counts, rt->offsets, rt->active,
+                       rt->num_active, l.tiles, l.chunk_tiles, l.chunk_rows, st);
+    launch_build_tiles(d.E, C, kRotTileRows, 1, rt->counts, rt->offsets, rt->active,
+                       rt->num_active, l.rtiles, l.chunk_rtiles, l.chunk_rrows, st);
 }
 
 struct FwdWs {
     DevErr *err;
-    Tile *tiles;
-    int32_t *chunk_tiles, *chunk_rows;
+    Lists l;
     uint16_t *xt, *h, *ht, *o, *scratch;
 };
 static FwdWs carve_fwd(void *ws, const pmoe_dims &d, int C, int mode, size_t *bytes)
@@ -145,9 +156,7 @@ static FwdWs carve_fwd(void *ws, const pmoe_dims &d, int C, int mode, size_t *by
     FwdWs w;
     int64_t P = (int64_t)d.T * d.k;
     w.err = c.take<DevErr>(kHdrBytes / sizeof(DevErr));
-    w.tiles = c.take<Tile>(max_tiles_of(d));
-    w.chunk_tiles = c.take<int32_t>(nchunks_of(d, C) + 2);
-    w.chunk_rows = c.take<int32_t>(nchunks_of(d, C) + 2);
+    w.l = carve_lists(c, d, C);
     w.xt = c.take<uint16_t>(P * d.d);
     w.h = c.take<uint16_t>(P * d.inter);
     w.ht = c.take<uint16_t>(P * d.inter);
@@ -160,9 +169,8 @@ static FwdWs carve_fwd(void *ws, const pmoe_dims &d, int C, int mode, size_t *by
 
 struct BwdWs {
     DevErr *err;
-    Tile *tiles;
-    int32_t *chunk_tiles, *chunk_rows;
-    uint16_t *dyp, *h, *ht, *dht, *dgu, *dxt;
+    Lists l;
+    uint16_t *dyp, *ht, *dht, *dgu, *dxt;
     float *dtw_part;
 };
 static BwdWs carve_bwd(void *ws, const pmoe_dims &d, int C, size_t *bytes)
@@ -171,11 +179,8 @@ static BwdWs carve_bwd(void *ws, const pmoe_dims &d, int C, size_t *bytes)
     BwdWs w;
     int64_t P = (int64_t)d.T * d.k;
     w.err = c.take<DevErr>(kHdrBytes / sizeof(DevErr));
-    w.tiles = c.take<Tile>(max_tiles_of(d));
-    w.chunk_tiles = c.take<int32_t>(nchunks_of(d, C) + 2);
-    w.chunk_rows = c.take<int32_t>(nchunks_of(d, C) + 2);
-    w.dyp = c.take<uint16_t>(P * d.d);
-    w.h = c.take<uint16_t>(P * d.inter);
+    w.l = carve_lists(c, d, C);
+    w.dyp = c.take<uint16_t>(P * d.d);      // gathered dY rows; later the rotated dx rows
     w.ht = c.take<uint16_t>(P * d.inter);
     w.dht = c.take<uint16_t>(P * d.inter);
     w.dgu = c.take<uint16_t>(P * 2 * d.inter);
@@ -367,21 +372,20 @@ pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const p
     if (!ws || ws_bytes < need || !aligned16(ws)) return PMOE_ERR_WORKSPACE;
     if (dims.T == 0) return PMOE_OK;
 
-    const int d = dims.d, I = dims.inter, b = dims.block, k = dims.k, E = dims.E;
+    const int d = dims.d, I = dims.inter, b = dims.block, k = dims.k;
     const int P = dims.T * k;
     const int fmt = wts->fmt;
     const uint16_t *R_up = adp ? (const uint16_t *)adp->R_up : nullptr;
     const uint16_t *R_dn = adp && R_up ? (const uint16_t *)adp->R_down : nullptr;
     const int64_t su = adp ? adp->stride_up : 0, sd = adp ? adp->stride_down : 0;
     const int nch = nchunks_of(dims, C);
-    const int maxt = max_tiles_of(dims);
-
-    launch_build_tiles(E, C, tile_rows(), tile_align(), rt->counts, rt->offsets, rt->active,
-                       rt->num_active, w.tiles, w.chunk_tiles, w.chunk_rows, stream);
-    pmoe_status gs = PMOE_OK;
-    // x~ for every pair, in expert-sorted order (gather + up rotation)
-    launch_rotate_rows(P, d, b, (const uint16_t *)X, true, rt->perm, k, rt->idx, R_up, su, w.xt,
-                       nullptr, stream);
+    const int maxrt = max_rot_tiles_of(dims);
+    const Lists &L = w.l;
+    build_lists(L, dims, C, rt, stream);
+    // x~ = bf16(x R_up[e]) for every pair, gathered into expert-sorted order
+    launch_rotate_tc(b, false, false, (const uint16_t *)X, d, true, rt->perm, k, rt->idx, R_up, su,
+                     d, w.xt, d, L.rtiles, L.chunk_rtiles, L.chunk_rtiles + nch, maxrt, 0, nullptr,
+                     stream);
 
     GemmArgs gu{};
     gu.kind = GK_FWD_GU;
@@ -390,22 +394,23 @@ pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const p
     gu.Nout = I;
     gu.Nst = 2 * (int64_t)I;
     gu.Kst = d;
-    gu.tiles = w.tiles;
-    gu.chunk_tiles = w.chunk_tiles;
+    gu.tiles = L.tiles;
+    gu.chunk_tiles = L.chunk_tiles;
     gu.out = w.h;
     gu.ctx = (uint16_t *)ctx;
     gu.I = I;
     GemmArgs dn{};
     dn.kind = GK_FWD_DOWN;
-    dn.A = w.ht;
+    dn.A = R_dn ? w.ht : w.h;
     dn.K = I;
     dn.Nout = d;
     dn.Nst = d;
     dn.Kst = I;
-    dn.tiles = w.tiles;
-    dn.chunk_tiles = w.chunk_tiles;
+    dn.tiles = L.tiles;
+    dn.chunk_tiles = L.chunk_tiles;
     dn.out = w.o;
     dn.I = I;
+    pmoe_status gs;
 
     if (mode == PMOE_MODE_FUSED) {
         gu.fmt = dn.fmt = fmt;
@@ -421,15 +426,19 @@ pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const p
         gu.c1 = dn.c1 = nch;
         {
             ScopedTimer tm(PMOE_KT_GEMM_GATE_UP, stream);
-            if ((gs = run_gemm(gu, maxt, P, w.err, stream)) != PMOE_OK) return gs;
+            if ((gs = run_gemm(gu, P, w.err, stream)) != PMOE_OK) return gs;
         }
-        launch_rotate_rows(P, I, b, w.h, false, rt->perm, k, rt->idx, R_dn, sd, w.ht, nullptr,
-                           stream);
+        if (R_dn)
+            launch_rotate_tc(b, false, false, w.h, I, false, rt->perm, k, rt->idx, R_dn, sd, I, w.ht,
+                             I, L.rtiles, L.chunk_rtiles, L.chunk_rtiles + nch, maxrt, 0, nullptr,
+                             stream);
         {
             ScopedTimer tm(PMOE_KT_GEMM_DOWN, stream);
-            if ((gs = run_gemm(dn, maxt, P, w.err, stream)) != PMOE_OK) return gs;
+            if ((gs = run_gemm(dn, P, w.err, stream)) != PMOE_OK) return gs;
         }
     } else {
+        // the pages' literal scheme: dequantize the chunk's experts into the
+        // bounded BF16 scratch, run the chunk's GEMMs, reuse the scratch
         const int64_t slot_bytes = 3 * (int64_t)I * d * 2;
         gu.fmt = dn.fmt = kFmtBF16;
         gu.wq = dn.wq = (const uint8_t *)w.scratch;
@@ -445,13 +454,15 @@ pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const p
             gu.c1 = dn.c1 = c + 1;
             {
                 ScopedTimer tm(PMOE_KT_GEMM_GATE_UP, stream);
-                if ((gs = run_gemm(gu, maxt, P, w.err, stream)) != PMOE_OK) return gs;
+                if ((gs = run_gemm(gu, P, w.err, stream)) != PMOE_OK) return gs;
             }
-            launch_rotate_rows(P, I, b, w.h, false, rt->perm, k, rt->idx, R_dn, sd, w.ht,
-                               w.chunk_rows + c, stream);
+            if (R_dn)
+                launch_rotate_tc(b, false, false, w.h, I, false, rt->perm, k, rt->idx, R_dn, sd, I,
+                                 w.ht, I, L.rtiles, L.chunk_rtiles + c, L.chunk_rtiles + c + 1,
+                                 maxrt, 0, nullptr, stream);
             {
                 ScopedTimer tm(PMOE_KT_GEMM_DOWN, stream);
-                if ((gs = run_gemm(dn, maxt, P, w.err, stream)) != PMOE_OK) return gs;
+                if ((gs = run_gemm(dn, P, w.err, stream)) != PMOE_OK) return gs;
             }
         }
     }
@@ -485,7 +496,7 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
     const int fmt = wts->fmt;
     const int64_t su = adp ? adp->stride_up : 0, sd = adp ? adp->stride_down : 0;
     const int nch = nchunks_of(dims, C);
-    const int maxt = max_tiles_of(dims);
+    const int maxrt = max_rot_tiles_of(dims);
     const int nsets_up = su ? E : 1, nsets_dn = sd ? E : 1;
 
     if (dims.T == 0) {
@@ -496,13 +507,18 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
             return PMOE_ERR_CUDA;
         return PMOE_OK;
     }
-
-    launch_build_tiles(E, C, tile_rows(), tile_align(), rt->counts, rt->offsets, rt->active,
-                       rt->num_active, w.tiles, w.chunk_tiles, w.chunk_rows, stream);
-    pmoe_status gs = PMOE_OK;
-    launch_gather_rows(P, d, k, (const uint16_t *)dY, rt->perm, w.dyp, stream);
-    launch_bwd_prep(P, I, b, (const uint16_t *)ctx, rt->perm, rt->idx, R_dn, sd, w.h, w.ht, stream);
-
+    const Lists &L = w.l;
+    const uint16_t *cx = (const uint16_t *)ctx;
+    const uint16_t *h = cx + 2 * I;   // saved h rows (stride 3I)
+    build_lists(L, dims, C, rt, stream);
+    // dY rows per pair (expert-sorted) and h~ = bf16(h R_down) from the saved h
+    launch_rotate_tc(b, false, false, (const uint16_t *)dY, d, true, rt->perm, k, rt->idx, nullptr,
+                     0, d, w.dyp, d, L.rtiles, L.chunk_rtiles, L.chunk_rtiles + nch, maxrt, 0,
+                     nullptr, stream);
+    launch_rotate_tc(b, false, false, h, 3 * (int64_t)I, false, rt->perm, k, rt->idx, R_dn, sd, I,
+                     w.ht, I, L.rtiles, L.chunk_rtiles, L.chunk_rtiles + nch, maxrt, 0, nullptr,
+                     stream);
+    pmoe_status gs;
     GemmArgs g{};
     g.kind = GK_BWD_G;
     g.fmt = fmt;
@@ -515,8 +531,8 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
     g.A = w.dyp;
     g.K = d;
     g.Nout = I;
-    g.tiles = w.tiles;
-    g.chunk_tiles = w.chunk_tiles;
+    g.tiles = L.tiles;
+    g.chunk_tiles = L.chunk_tiles;
     g.c0 = 0;
     g.c1 = nch;
     g.out = w.dht;
@@ -527,14 +543,16 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
     g.dtw_part = w.dtw_part;
     {
         ScopedTimer tm(PMOE_KT_GEMM_BWD_G, stream);
-        if ((gs = run_gemm(g, maxt, P, w.err, stream)) != PMOE_OK) return gs;
+        if ((gs = run_gemm(g, P, w.err, stream)) != PMOE_OK) return gs;
     }
-    if (d_topk_w) launch_dtw_reduce(P, dtw_parts(I), w.dtw_part, rt->perm, d_topk_w, stream);
-    launch_bwd_mid(P, I, b, (const uint16_t *)ctx, w.dht, rt->perm, rt->idx, R_dn, sd, w.dgu,
-                   stream);
+    if (d_topk_w) launch_dtw_reduce(P, I / 32, w.dtw_part, rt->perm, d_topk_w, stream);
+    // dh = dh~ R_down^T, then the SwiGLU backward into [dg | du]
+    launch_rotate_tc(b, true, true, w.dht, I, false, rt->perm, k, rt->idx, R_dn, sd, I, w.dgu,
+                     2 * (int64_t)I, L.rtiles, L.chunk_rtiles, L.chunk_rtiles + nch, maxrt, 0, cx,
+                     stream);
     if (R_dn)
-        launch_block_outer(nsets_dn, P, I, b, w.h, nullptr, k, w.dht, sd ? rt->offsets : nullptr,
-                           dR_down, stream);
+        launch_outer_tc(nsets_dn, P, I, b, h, 3 * (int64_t)I, false, rt->perm, k, w.dht, I,
+                        sd ? rt->offsets : nullptr, dR_down, stream);
 
     GemmArgs x{};
     x.kind = GK_BWD_DX;
@@ -548,21 +566,28 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
     x.A = w.dgu;
     x.K = 2 * I;
     x.Nout = d;
-    x.tiles = w.tiles;
-    x.chunk_tiles = w.chunk_tiles;
+    x.tiles = L.tiles;
+    x.chunk_tiles = L.chunk_tiles;
     x.c0 = 0;
     x.c1 = nch;
     x.out = w.dxt;
     x.I = I;
     {
         ScopedTimer tm(PMOE_KT_GEMM_BWD_DX, stream);
-        if ((gs = run_gemm(x, maxt, P, w.err, stream)) != PMOE_OK) return gs;
+        if ((gs = run_gemm(x, P, w.err, stream)) != PMOE_OK) return gs;
     }
     if (R_up)
-        launch_block_outer(nsets_up, P, d, b, (const uint16_t *)X, rt->perm, k, w.dxt,
-                           su ? rt->offsets : nullptr, dR_up, stream);
-    launch_combine_bwd(dims.T, d, k, b, w.dxt, rt->inv_perm, rt->idx, R_up, su, (uint16_t *)dX,
-                       stream);
+        launch_outer_tc(nsets_up, P, d, b, (const uint16_t *)X, d, true, rt->perm, k, w.dxt, d,
+                        su ? rt->offsets : nullptr, dR_up, stream);
+    // dx_pair = dx~ R_up^T (into the dY buffer), then the slot sum per token
+    const uint16_t *dxp = w.dxt;
+    if (R_up) {
+        launch_rotate_tc(b, true, false, w.dxt, d, false, rt->perm, k, rt->idx, R_up, su, d, w.dyp,
+                         d, L.rtiles, L.chunk_rtiles, L.chunk_rtiles + nch, maxrt, 0, nullptr,
+                         stream);
+        dxp = w.dyp;
+    }
+    launch_combine(dims.T, d, k, dxp, rt->inv_perm, nullptr, (uint16_t *)dX, stream);
     return launched(stream);
 }
 
@@ -631,7 +656,7 @@ pmoe_status moe_grouped_gemm(pmoe_wfmt fmt, const void *q, const void *s, int32_
     if (!ws || ws_bytes < need || !aligned16(ws)) return PMOE_ERR_WORKSPACE;
     if (rows == 0) return PMOE_OK;
     launch_offsets_to_active(E, rows, offsets, w.counts, w.active, w.num_active, w.err, stream);
-    launch_build_tiles(E, E, tile_rows(), tile_align(), w.counts, offsets, w.active, w.num_active,
+    launch_build_tiles(E, E, kGemmRows, kGemmAlign, w.counts, offsets, w.active, w.num_active,
                        w.tiles, w.chunk_tiles, w.chunk_rows, stream);
     GemmArgs g{};
     g.kind = trans ? GK_BWD_DX : GK_FWD_DOWN;
@@ -651,7 +676,7 @@ pmoe_status moe_grouped_gemm(pmoe_wfmt fmt, const void *q, const void *s, int32_
     g.c1 = 1;
     g.out = (uint16_t *)out;
     g.I = N;
-    pmoe_status gs = run_gemm(g, (int)(cdiv(rows, 16) + E), rows, w.err, stream);
+    pmoe_status gs = run_gemm(g, rows, w.err, stream);
     if (gs != PMOE_OK) return gs;
     return launched(stream);
 }
@@ -665,8 +690,9 @@ pmoe_status adapter_apply(int32_t rows, int32_t dim, int32_t b, const void *X, c
     if (rows == 0) return PMOE_OK;
     if (!X || !R || !Xr || X == Xr || !aligned16(X) || !aligned16(R) || !aligned16(Xr))
         return PMOE_ERR_INVALID_ARG;
-    launch_rotate_rows(rows, dim, b, (const uint16_t *)X, false, nullptr, 1, nullptr,
-                       (const uint16_t *)R, 0, (uint16_t *)Xr, nullptr, stream);
+    launch_rotate_tc(b, false, false, (const uint16_t *)X, dim, false, nullptr, 1, nullptr,
+                     (const uint16_t *)R, 0, dim, (uint16_t *)Xr, dim, nullptr, nullptr, nullptr,
+                     0, rows, nullptr, stream);
     return launched(stream);
 }
 
@@ -675,13 +701,15 @@ pmoe_status adapter_grad(int32_t rows, int32_t dim, int32_t b, const void *X, co
 {
     if (rows < 0 || dim <= 0 || !block_ok(b) || dim % b || dim % 8) return PMOE_ERR_INVALID_ARG;
     if (!dR || (rows > 0 && (!X || !dXr || !R))) return PMOE_ERR_INVALID_ARG;
+    if (dX && dX == dXr) return PMOE_ERR_INVALID_ARG;
     if (!aligned16(X) || !aligned16(dXr) || !aligned16(R) || !aligned16(dX) || !aligned16(dR))
         return PMOE_ERR_INVALID_ARG;
     if (dX && rows > 0)
-        launch_adapter_grad_dx(rows, dim, b, (const uint16_t *)dXr, (const uint16_t *)R,
-                               (uint16_t *)dX, stream);
-    launch_block_outer(1, rows, dim, b, (const uint16_t *)X, nullptr, 1, (const uint16_t *)dXr,
-                       nullptr, dR, stream);
+        launch_rotate_tc(b, true, false, (const uint16_t *)dXr, dim, false, nullptr, 1, nullptr,
+                         (const uint16_t *)R, 0, dim, (uint16_t *)dX, dim, nullptr, nullptr, nullptr,
+                         0, rows, nullptr, stream);
+    launch_outer_tc(1, rows, dim, b, (const uint16_t *)X, dim, false, nullptr, 1,
+                    (const uint16_t *)dXr, dim, nullptr, dR, stream);
     return launched(stream);
 }
 

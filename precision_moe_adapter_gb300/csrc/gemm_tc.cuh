@@ -560,10 +560,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                         const int col = c0 + j + (up ? 1 : 0);
                         if (col < tl.nrows) {
                             const int64_t r = tl.row0 + col;
-                            a.out[r * a.I + f] = f2bf(silu_f(g) * u);
-                            if (a.ctx) {
-                                a.ctx[r * 2 * a.I + f] = f2bf(g);
-                                a.ctx[r * 2 * a.I + a.I + f] = f2bf(u);
+                            const uint16_t h = f2bf(silu_f(g) * u);
+                            a.out[r * a.I + f] = h;
+                            if (a.ctx) {   // saved for the backward: [g | u | h]
+                                uint16_t *c = a.ctx + r * 3 * a.I + f;
+                                c[0] = f2bf(g);
+                                c[a.I] = f2bf(u);
+                                c[2 * a.I] = h;
                             }
                         }
                     }

@@ -32,27 +32,11 @@ void launch_dequant_chunk(int fmt, int d, int I, int C, int chunk, const int32_t
                           const void *w2, const void *s2, uint16_t *scratch, cudaStream_t st);
 
 // adapter.cu
-// out[r] = bf16(src[row(r)] blockdiag(R[e(r)])) for r in [r0, r1) where the
-// row range may come from device memory (rows_dev[0..1]) when non-NULL.
-// row(r) = perm[r] / k when `gather` else r; e(r) = idx_flat[perm[r]] when
-// R is per expert (stride != 0).  R == NULL copies (gathers) the rows.
-void launch_rotate_rows(int nrows_max, int dim, int b, const uint16_t *src, bool gather,
-                        const int32_t *perm, int k, const int32_t *idx_flat, const uint16_t *R,
-                        int64_t stride, uint16_t *out, const int32_t *rows_dev, cudaStream_t st);
-void launch_adapter_grad_dx(int rows, int dim, int b, const uint16_t *dXr, const uint16_t *R,
-                            uint16_t *dX, cudaStream_t st);
-// dR[s][beta] = sum over rows of set s of a_blk^T g_blk (fixed order).
-// a rows: a[arow(i)] with arow(i) = perm[i]/k if perm (gather) else i.
-// Sets: per expert (offsets given: rows offsets[s]..offsets[s+1]) or one
-// set over rows [0, nrows) when offsets == NULL.
-void launch_block_outer(int nsets, int nrows, int dim, int b, const uint16_t *a,
-                        const int32_t *perm, int k, const uint16_t *g, const int32_t *offsets,
-                        float *dR, cudaStream_t st);
 void launch_cayley(int nblk, int b, const float *S, uint16_t *Rb, float *Rf, cudaStream_t st);
 void launch_cayley_grad(int nblk, int b, const float *S, const float *Rf, const float *dR,
                         float *dS, cudaStream_t st);
 
-// gemm_simple.cu
+// grouped GEMM (gemm_tc*.cu)
 enum GemmKind { GK_FWD_GU = 0, GK_FWD_DOWN = 1, GK_BWD_G = 2, GK_BWD_DX = 3 };
 constexpr int kFmtBF16 = 3;  // weights already dequantized (scratch mode)
 struct GemmArgs {
@@ -71,37 +55,40 @@ struct GemmArgs {
     int c0, c1;
     bool slot_index;         // weights indexed by chunk slot (scratch) instead of expert
     uint16_t *out;           // [P, Nout] bf16
-    uint16_t *ctx;           // FWD_GU: [P, 2I] g|u or NULL
+    uint16_t *ctx;           // FWD_GU: [P, 3I] g|u|h or NULL
     int I;
     const float *w;          // BWD_G: routing weights by pair id
     const int32_t *perm;
     const uint16_t *ht;      // BWD_G: h~ [P, I]
-    float *dtw_part;         // BWD_G: [P, I/64]
+    float *dtw_part;         // BWD_G: [P, I/32]
 };
-void launch_gemm_simple(const GemmArgs &a, int max_tiles, cudaStream_t st);
-
-// gemm_tc.cu: tcgen05 grouped GEMM (returns false if the request cannot be
+// tcgen05 grouped GEMM (returns false if the request cannot be
 // launched, e.g. the TMA descriptor could not be encoded)
 bool launch_gemm_tc(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st);
 // counts / active / num_active of experts from row offsets [E+1]
 void launch_offsets_to_active(int E, int rows, const int32_t *offsets, int32_t *counts,
                               int32_t *active, int32_t *num_active, DevErr *err, cudaStream_t st);
 
+// rotate_tc.cu: block-diagonal rotation on mma.sync.  Tiles: 64-row tiles
+// of one expert (indices *tbeg .. *tend-1), or NULL for rows 0..nrows-1 of
+// one shared rotation.  trans: R^T.  swiglu_bwd: the output is [dg | du]
+// (out_ld = 2*dim) from the saved [g | u | h] rows of ctx.
+void launch_rotate_tc(int b, bool trans, bool swiglu_bwd, const uint16_t *src, int64_t src_ld,
+                      bool gather, const int32_t *perm, int k, const int32_t *idx_flat,
+                      const uint16_t *R, int64_t stride, int dim, uint16_t *out, int64_t out_ld,
+                      const Tile *tiles, const int32_t *tbeg, const int32_t *tend, int max_tiles,
+                      int nrows, const uint16_t *ctx, cudaStream_t st);
+// dR[s][beta] = sum over rows of set s of a_blk^T g_blk on mma.sync
+void launch_outer_tc(int nsets, int nrows, int dim, int b, const uint16_t *a, int64_t a_ld,
+                     bool gather, const int32_t *perm, int k, const uint16_t *g, int64_t g_ld,
+                     const int32_t *offsets, float *dR, cudaStream_t st);
+constexpr int kRotTileRows = 64;
+
 // layer.cu
 void launch_combine(int T, int d, int k, const uint16_t *o, const int32_t *inv_perm,
                     const float *w, uint16_t *Y, cudaStream_t st);
 void launch_gather_rows(int P, int d, int k, const uint16_t *src, const int32_t *perm,
                         uint16_t *out, cudaStream_t st);
-void launch_bwd_prep(int P, int I, int b, const uint16_t *ctx, const int32_t *perm,
-                     const int32_t *idx_flat, const uint16_t *R_down, int64_t stride,
-                     uint16_t *h, uint16_t *ht, cudaStream_t st);
-void launch_bwd_mid(int P, int I, int b, const uint16_t *ctx, const uint16_t *dht,
-                    const int32_t *perm, const int32_t *idx_flat, const uint16_t *R_down,
-                    int64_t stride, uint16_t *dgu, cudaStream_t st);
 void launch_dtw_reduce(int P, int nparts, const float *part, const int32_t *perm, float *dtw,
                        cudaStream_t st);
-void launch_combine_bwd(int T, int d, int k, int b, const uint16_t *dxt, const int32_t *inv_perm,
-                        const int32_t *idx_flat, const uint16_t *R_up, int64_t stride,
-                        uint16_t *dX, cudaStream_t st);
-
 }  // namespace pmoe

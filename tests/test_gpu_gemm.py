@@ -46,7 +46,8 @@ def _scales_exhaustive(fmt, E, N, K):
     if fmt == gi.INT4:
         bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
         f = (bits.astype(np.uint32) << 16).view(np.float32)
-        fin = bits[np.isfinite(f) & (np.abs(f) * 8 < 3.38e38)]
+        with np.errstate(over="ignore", invalid="ignore"):
+            fin = bits[np.isfinite(f) & (np.abs(f.astype(np.float64)) * 8 < 3.38e38)]
         return np.resize(fin, ng).reshape(E, N, K // 32)
     return np.resize(np.arange(253, dtype=np.uint8), ng).reshape(E, N, K // 32)
 
@@ -70,10 +71,13 @@ def test_dequant_through_the_mma_is_bit_exact(fmt, trans):
     got, st = run(fmt, q, s, E, N, K, trans, A, [rows_per] * E)
     assert st == pmoe.PMOE_OK
     n_sub = n_sub_exact = 0
+    # -0 weights come out of the contraction as +0 (adding +0 terms): the
+    # comparison identifies the two zeros
+    z = lambda x: np.where((x & 0x7FFF) == 0, 0, x).astype(np.uint16)
     for e in range(E):
         W = oracle.dequant(fmt, q[e], s[e], N, K)          # [N, K] BF16 bits
-        want = W if trans else W.T
-        blk = got[e * rows_per:(e + 1) * rows_per]
+        want = z(W if trans else W.T)
+        blk = z(got[e * rows_per:(e + 1) * rows_per])
         sub = ((want & 0x7F80) == 0) & ((want & 0x7F) != 0)   # BF16 subnormal weights
         assert np.array_equal(blk[~sub], want[~sub]), e
         # the MMA may flush subnormal inputs to zero; otherwise exact

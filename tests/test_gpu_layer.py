@@ -57,7 +57,7 @@ def run_gpu(c, C=None, mode=pmoe.MODE_FUSED, backward=True, R_up="case", R_down=
     L.permute(rt)
     X = dev(c["X"])
     Y = torch.empty((cfg.T, cfg.d), dtype=torch.int16, device="cuda")
-    ctx = torch.empty((max(cfg.P, 1), 2 * cfg.I), dtype=torch.int16, device="cuda")
+    ctx = torch.empty((max(cfg.P, 1), 3 * cfg.I), dtype=torch.int16, device="cuda")
     L.forward(X, rt, Y, C=C, mode=mode, ctx=ctx)
     out = dict(Y=t2np_bits(Y))
     if backward:
@@ -162,7 +162,7 @@ def test_runs_are_deterministic_and_base_is_untouched():
     rt.w.copy_(torch.from_numpy(c["w"]))
     L.permute(rt)
     Y = torch.empty((c["cfg"].T, c["cfg"].d), dtype=torch.int16, device="cuda")
-    ctx = torch.empty((c["cfg"].P, 2 * c["cfg"].I), dtype=torch.int16, device="cuda")
+    ctx = torch.empty((c["cfg"].P, 3 * c["cfg"].I), dtype=torch.int16, device="cuda")
     L.forward(X, rt, Y, ctx=ctx)
     dX = torch.empty_like(Y)
     L.backward(X, dev(c["dY"]), ctx, rt, dX, None, *L.grads())
@@ -186,7 +186,7 @@ def test_tiny_end_to_end_from_the_router():
     L.route(Xd, rt, logits)
     L.permute(rt)
     Y = torch.empty((cfg.T, cfg.d), dtype=torch.int16, device="cuda")
-    ctx = torch.empty((cfg.P, 2 * cfg.I), dtype=torch.int16, device="cuda")
+    ctx = torch.empty((cfg.P, 3 * cfg.I), dtype=torch.int16, device="cuda")
     L.forward(Xd, rt, Y, ctx=ctx)
     dX = torch.empty_like(Y)
     L.backward(Xd, dev(dY), ctx, rt, dX, None, *L.grads())
