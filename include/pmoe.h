@@ -247,16 +247,19 @@ pmoe_status adapter_grad(int32_t rows, int32_t dim, int32_t b, const void *X, co
 
 /*
  * adapter_cayley -- R = (I + S)(I - S)^{-1} for nblk skew-symmetric b x b
- * blocks S (f32 [nblk, b, b]); R written as bf16 (R_bf16, nullable) and
- * f32 (R_f32, nullable).  b <= 128.
+ * blocks S (f32 [nblk, b, b]; only skew input is meaningful: the symmetric
+ * part of I - S must be I); R written as bf16 (R_bf16, nullable) and f32
+ * (R_f32, nullable).  b in {2, 4, 8, 16, 32, 64, 128}.
  */
 pmoe_status adapter_cayley(int32_t nblk, int32_t b, const float *S, void *R_bf16, float *R_f32,
                            cudaStream_t stream);
 
 /*
  * adapter_cayley_grad -- dS = M - M^T with M = (I + R)^T dR (I - S)^{-T},
- * the gradient with respect to the skew parameter of each block.
- * S, R_f32 (from adapter_cayley), dR: f32 [nblk, b, b]; dS f32 out.
+ * the gradient with respect to the skew parameter of each block.  Since
+ * (I - S)^{-1} = (I + R)/2, it is computed from R_f32 (the output of
+ * adapter_cayley for the same S) alone; S is accepted for reference and
+ * may be NULL.  R_f32, dR: f32 [nblk, b, b]; dS f32 out.
  */
 pmoe_status adapter_cayley_grad(int32_t nblk, int32_t b, const float *S, const float *R_f32,
                                 const float *dR, float *dS, cudaStream_t stream);

@@ -716,7 +716,7 @@ pmoe_status adapter_grad(int32_t rows, int32_t dim, int32_t b, const void *X, co
 pmoe_status adapter_cayley(int32_t nblk, int32_t b, const float *S, void *R_bf16, float *R_f32,
                            cudaStream_t stream)
 {
-    if (nblk < 0 || b < 1 || b > 128) return PMOE_ERR_INVALID_ARG;
+    if (nblk < 0 || !cayley_block_ok(b)) return PMOE_ERR_INVALID_ARG;
     if (nblk == 0) return PMOE_OK;
     if (!S || (!R_bf16 && !R_f32)) return PMOE_ERR_INVALID_ARG;
     launch_cayley(nblk, b, S, (uint16_t *)R_bf16, R_f32, stream);
@@ -726,9 +726,9 @@ pmoe_status adapter_cayley(int32_t nblk, int32_t b, const float *S, void *R_bf16
 pmoe_status adapter_cayley_grad(int32_t nblk, int32_t b, const float *S, const float *R_f32,
                                 const float *dR, float *dS, cudaStream_t stream)
 {
-    if (nblk < 0 || b < 1 || b > 128) return PMOE_ERR_INVALID_ARG;
+    if (nblk < 0 || !cayley_block_ok(b)) return PMOE_ERR_INVALID_ARG;
     if (nblk == 0) return PMOE_OK;
-    if (!S || !R_f32 || !dR || !dS) return PMOE_ERR_INVALID_ARG;
+    if (!R_f32 || !dR || !dS) return PMOE_ERR_INVALID_ARG;
     launch_cayley_grad(nblk, b, S, R_f32, dR, dS, stream);
     return launched(stream);
 }

@@ -32,6 +32,7 @@ void launch_dequant_chunk(int fmt, int d, int I, int C, int chunk, const int32_t
                           const void *w2, const void *s2, uint16_t *scratch, cudaStream_t st);
 
 // adapter.cu
+bool cayley_block_ok(int b);
 void launch_cayley(int nblk, int b, const float *S, uint16_t *Rb, float *Rf, cudaStream_t st);
 void launch_cayley_grad(int nblk, int b, const float *S, const float *Rf, const float *dR,
                         float *dS, cudaStream_t st);
