@@ -30,7 +30,6 @@
 namespace pmoe {
 namespace tc {
 
-constexpr int kStages = 4;
 constexpr int kBK = 64;                      // K per stage: one 128-byte swizzle row of BF16
 constexpr int kM = 128;                      // MMA M (weight rows per tile)
 constexpr int kNmax = 256;                   // tokens per tile (MMA N)
@@ -45,8 +44,6 @@ constexpr int kDqWarp0 = 6;
 constexpr int kDqWarps = 8;
 constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;
 constexpr int kTmemCols = 512;
-constexpr int kBarBytes = 8 * (3 * kStages + 4) + 16;
-constexpr size_t kSmemBytes = (size_t)kStages * (kABytes + kBBytes) + kBarBytes + 1024;
 constexpr unsigned long long kWaitNs = 2000000000ull;   // bounded waits: 2 s
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -254,20 +251,54 @@ struct KindTraits {
     static constexpr bool kTrans = (KIND == GK_BWD_G || KIND == GK_BWD_DX);
 };
 
-// Per-thread packed data for one stage.
-template <int KIND, int FMT>
-struct Raw;
-// non-transposed: 32 consecutive K elements of one weight row
-template <int KIND>
-struct Raw4N {
-    uint4 q;
-    uint32_t s;
+// ------------------------------------------------------------------ pipeline sizes
+// Per weight format: A/B shared-memory stages and the ring of packed-weight
+// prefetches (kRawStages steps in flight, kSlot bytes per thread and step).
+template <int FMT>
+struct Pipe {
+    static constexpr bool k4bit = FMT == PMOE_W_INT4_G32_BF16 || FMT == PMOE_W_MXFP4_G32_E8M0;
+    static constexpr int kStagesAB = k4bit ? 4 : 3;
+    static constexpr int kRawStages = 4;
+    static constexpr int kSlot = FMT == PMOE_W_FP8_B128_F32 ? 48 : (FMT == kFmtBF16 ? 64 : 32);
+    static constexpr int kRawBytes = kRawStages * 256 * kSlot;
+    static constexpr int kBarOff = kStagesAB * (kABytes + kBBytes);
+    static constexpr int kBarBytes = 8 * (3 * kStagesAB + 4) + 16;
+    static constexpr int kRawOff = (kBarOff + kBarBytes + 127) & ~127;
+    static constexpr size_t kSmem = (size_t)kRawOff + kRawBytes + 1024;
+    static_assert(kSmem <= 232448, "shared memory budget");
 };
+
+__device__ __forceinline__ void cpa16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cpa8(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cpa4(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cpa_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // ------------------------------------------------------------------ dequant producers
 // Thread task per stage (256 threads):
 //   non-transposed: smem row m = td >> 1, K half = td & 1 (32 elements)
 //   transposed:     rows m = 8*(td & 15) .. +7, K = 4*(td >> 4) .. +3
+// issue() copies the thread's packed bytes (and the aligned 4-byte word
+// holding its scale) into its ring slot; convert() turns the slot into BF16
+// in the A stage.  Slot layouts:
+//   4-bit, non-transposed: q 16 B @0, scale word @16
+//   FP8,   non-transposed: q 32 B @0, scale @32
+//   BF16 (scratch):        64 B @0
+//   4-bit, transposed:     4 q words @0, 4 scale words @16
+//   FP8,   transposed:     4 x 8 B q @0, 4 scales @32
 template <int KIND, int FMT>
 struct Dequant {
     static constexpr bool T = KindTraits<KIND>::kTrans;
@@ -280,26 +311,78 @@ struct Dequant {
         }
         return f0 + m;
     }
-
-    // Convert and store one stage.  `live` false writes zeros (rows past
-    // the end of a ragged feature tile).
-    __device__ static void stage(const TcArgs &a, const uint8_t *wq, const uint8_t *ws, int f0,
-                                 int ks, int td, uint32_t sA)
+    __device__ static bool live(const TcArgs &a, int f0, int td)
     {
+        if (T) return f0 + 8 * (td & 15) < a.Mtot;
+        return KIND == GK_FWD_GU || f0 + (td >> 1) < a.Mtot;
+    }
+    // byte offset of the aligned 4-byte word holding scale index gi
+    __device__ static int64_t sword(int64_t gi)
+    {
+        return FMT == PMOE_W_INT4_G32_BF16 ? 2 * (gi & ~(int64_t)1) : (gi & ~(int64_t)3);
+    }
+    __device__ static uint32_t spick(uint32_t word, int64_t gi)
+    {
+        if (FMT == PMOE_W_INT4_G32_BF16) return (gi & 1) ? word >> 16 : word & 0xFFFFu;
+        return (word >> (8 * (gi & 3))) & 0xFFu;
+    }
+
+    __device__ static void issue(const TcArgs &a, const uint8_t *wq, const uint8_t *ws, int f0,
+                                 int ks, int td, uint32_t slot)
+    {
+        if (!live(a, f0, td)) return;
         if (!T) {
             const int m = td >> 1, half = td & 1;
             const int64_t row = row_of(a, f0, m);
-            const bool live = KIND == GK_FWD_GU ? true : (f0 + m < a.Mtot);
+            const int64_t k0 = (int64_t)ks * kBK + 32 * half;
+            if (FMT == PMOE_W_INT4_G32_BF16 || FMT == PMOE_W_MXFP4_G32_E8M0) {
+                cpa16(slot, wq + row * (a.Kst >> 1) + (k0 >> 1));
+                cpa4(slot + 16, ws + sword(row * (a.Kst >> 5) + (k0 >> 5)));
+            } else if (FMT == PMOE_W_FP8_B128_F32) {
+                const uint8_t *src = wq + row * a.Kst + k0;
+                cpa16(slot, src);
+                cpa16(slot + 16, src + 16);
+                cpa4(slot + 32, ws + 4 * ((row >> 7) * (a.Kst >> 7) + (k0 >> 7)));
+            } else {
+                const uint8_t *src = wq + 2 * (row * a.Kst + k0);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) cpa16(slot + 16 * j, src + 16 * j);
+            }
+        } else {
+            const int mg0 = f0 + 8 * (td & 15);
+            const int64_t n0 = (int64_t)ks * kBK + 4 * (td >> 4);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t n = n0 + j;
+                if (FMT == PMOE_W_FP8_B128_F32) {
+                    cpa8(slot + 8 * j, wq + n * a.Kst + mg0);
+                    cpa4(slot + 32 + 4 * j, ws + 4 * ((n >> 7) * (a.Kst >> 7) + (mg0 >> 7)));
+                } else {
+                    cpa4(slot + 4 * j, wq + n * (a.Kst >> 1) + (mg0 >> 1));
+                    cpa4(slot + 16 + 4 * j, ws + sword(n * (a.Kst >> 5) + (mg0 >> 5)));
+                }
+            }
+        }
+    }
+
+    // Convert the slot into the A stage (zeros for rows past a ragged tile).
+    __device__ static void convert(const TcArgs &a, int f0, int ks, int td, const uint8_t *slot,
+                                   uint32_t sA)
+    {
+        const bool lv = live(a, f0, td);
+        if (!T) {
+            const int m = td >> 1, half = td & 1;
+            const int64_t row = row_of(a, f0, m);
             const int64_t k0 = (int64_t)ks * kBK + 32 * half;
             uint4 out[4];
-            if (!live) {
+            if (!lv) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) out[j] = make_uint4(0, 0, 0, 0);
             } else if (FMT == PMOE_W_INT4_G32_BF16) {
-                uint4 q = ldg_nc_v4(wq + row * (a.Kst >> 1) + (k0 >> 1));
-                uint32_t sb = ((const uint16_t *)ws)[row * (a.Kst >> 5) + (k0 >> 5)];
-                uint32_t s2 = sb | (sb << 16);
-                uint32_t words[4] = {q.x, q.y, q.z, q.w};
+                const uint4 q = *(const uint4 *)slot;
+                const uint32_t sb = spick(*(const uint32_t *)(slot + 16), row * (a.Kst >> 5) + (k0 >> 5));
+                const uint32_t s2 = sb | (sb << 16);
+                const uint32_t words[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     uint32_t p[4];
@@ -310,9 +393,9 @@ struct Dequant {
                     out[j].w = prmt(p[2], p[3], 0x7632);
                 }
             } else if (FMT == PMOE_W_MXFP4_G32_E8M0) {
-                uint4 q = ldg_nc_v4(wq + row * (a.Kst >> 1) + (k0 >> 1));
-                float sc = e8m0_value(ws[row * (a.Kst >> 5) + (k0 >> 5)]);
-                uint32_t words[4] = {q.x, q.y, q.z, q.w};
+                const uint4 q = *(const uint4 *)slot;
+                const float sc = e8m0_value(spick(*(const uint32_t *)(slot + 16), row * (a.Kst >> 5) + (k0 >> 5)));
+                const uint32_t words[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     uint32_t w = words[j], o[4];
@@ -323,29 +406,27 @@ struct Dequant {
                     out[j] = make_uint4(o[0], o[1], o[2], o[3]);
                 }
             } else if (FMT == PMOE_W_FP8_B128_F32) {
-                const uint8_t *src = wq + row * a.Kst + k0;
-                float sc = ((const float *)ws)[(row >> 7) * (a.Kst >> 7) + (k0 >> 7)];
-                uint4 q0 = ldg_nc_v4(src), q1 = ldg_nc_v4(src + 16);
-                uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                const uint4 q0 = *(const uint4 *)slot, q1 = *(const uint4 *)(slot + 16);
+                const float sc = *(const float *)(slot + 32);
+                const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     uint32_t o[4];
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        uint32_t w = words[2 * j + h];
+                        const uint32_t w = words[2 * j + h];
                         __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3);
                         __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
-                        float2 fl = __half22float2(*(const __half2 *)&lo);
-                        float2 fh = __half22float2(*(const __half2 *)&hi);
+                        const float2 fl = __half22float2(*(const __half2 *)&lo);
+                        const float2 fh = __half22float2(*(const __half2 *)&hi);
                         o[2 * h] = pack_bf2(__fmul_rn(fl.x, sc), __fmul_rn(fl.y, sc));
                         o[2 * h + 1] = pack_bf2(__fmul_rn(fh.x, sc), __fmul_rn(fh.y, sc));
                     }
                     out[j] = make_uint4(o[0], o[1], o[2], o[3]);
                 }
-            } else {   // BF16 scratch
-                const uint8_t *src = wq + 2 * (row * a.Kst + k0);
+            } else {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) out[j] = ldg_nc_v4(src + 16 * j);
+                for (int j = 0; j < 4; ++j) out[j] = *(const uint4 *)(slot + 16 * j);
             }
             const uint32_t rowaddr = sA + m * 128;
 #pragma unroll
@@ -357,19 +438,18 @@ struct Dequant {
             // transposed: A[m][k] = W[k0 + k][f0 + m] (contraction over stored rows)
             const int mb = td & 15, kb = td >> 4;
             const int mg0 = f0 + 8 * mb;
-            const bool live = mg0 < a.Mtot;
             const int64_t n0 = (int64_t)ks * kBK + 4 * kb;
             uint32_t v[8][2];   // for each m: (k0,k1), (k2,k3)
-            if (!live) {
+            if (!lv) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) v[i][0] = v[i][1] = 0;
             } else if (FMT == PMOE_W_INT4_G32_BF16) {
                 uint32_t p[4][4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const int64_t n = n0 + j;
-                    uint32_t w = *(const uint32_t *)(wq + n * (a.Kst >> 1) + (mg0 >> 1));
-                    uint32_t sb = ((const uint16_t *)ws)[n * (a.Kst >> 5) + (mg0 >> 5)];
+                    const uint32_t w = *(const uint32_t *)(slot + 4 * j);
+                    const uint32_t sb = spick(*(const uint32_t *)(slot + 16 + 4 * j),
+                                              (n0 + j) * (a.Kst >> 5) + (mg0 >> 5));
                     int4x8_pairs(w, sb | (sb << 16), p[j]);
                 }
                 // p[j][i & 3] holds (m = i, m = i + 4) of row j
@@ -383,15 +463,15 @@ struct Dequant {
                 float f[4][8];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const int64_t n = n0 + j;
                     if (FMT == PMOE_W_MXFP4_G32_E8M0) {
-                        uint32_t w = *(const uint32_t *)(wq + n * (a.Kst >> 1) + (mg0 >> 1));
-                        float sc = e8m0_value(ws[n * (a.Kst >> 5) + (mg0 >> 5)]);
+                        const uint32_t w = *(const uint32_t *)(slot + 4 * j);
+                        const float sc = e8m0_value(spick(*(const uint32_t *)(slot + 16 + 4 * j),
+                                                          (n0 + j) * (a.Kst >> 5) + (mg0 >> 5)));
 #pragma unroll
                         for (int i = 0; i < 8; ++i) f[j][i] = __fmul_rn(e2m1_value((w >> (4 * i)) & 15u), sc);
                     } else {
-                        uint2 w = *(const uint2 *)(wq + n * a.Kst + mg0);
-                        float sc = ((const float *)ws)[(n >> 7) * (a.Kst >> 7) + (mg0 >> 7)];
+                        const uint2 w = *(const uint2 *)(slot + 8 * j);
+                        const float sc = *(const float *)(slot + 32 + 4 * j);
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
                             f[j][i] = __fmul_rn(e4m3_value(((i < 4 ? w.x : w.y) >> (8 * (i & 3))) & 255u), sc);
@@ -420,12 +500,14 @@ template <int KIND, int FMT>
 __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__ CUtensorMap tmB,
                                                          const TcArgs a)
 {
+    using PP = Pipe<FMT>;
+    constexpr int kStages = PP::kStagesAB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sA0 = smem_u32(smem);
     const uint32_t sB0 = sA0 + kStages * kABytes;
     const uint32_t bar0 = sB0 + kStages * kBBytes;
-    uint32_t *tmem_slot = (uint32_t *)(smem + kStages * (kABytes + kBBytes) + 8 * (3 * kStages + 4));
+    uint32_t *tmem_slot = (uint32_t *)(smem + PP::kBarOff + 8 * (3 * kStages + 4));
     auto full_a = [&](int s) { return bar0 + 8 * s; };
     auto full_b = [&](int s) { return bar0 + 8 * (kStages + s); };
     auto empty = [&](int s) { return bar0 + 8 * (2 * kStages + s); };
@@ -511,27 +593,49 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             }
         }
     } else if (warp >= kDqWarp0) {
-        // ---------------- dequant producers
+        // ---------------- dequant producers: packed weights prefetched
+        // kRawStages - 1 steps ahead with cp.async, converted into the A stage
         const int td = threadIdx.x - kDqWarp0 * 32;
-        uint32_t g = 0;
-        bool ok = true;
-        for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        uint8_t *raw = smem + PP::kRawOff + td * PP::kSlot;
+        const uint32_t raw_a = smem_u32(raw);
+        const int my_items = n_items > (int)blockIdx.x ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+        const uint32_t total = (uint32_t)my_items * nk;
+        constexpr uint32_t kRing = PP::kRawStages, kRingStride = 256 * PP::kSlot;
+        auto step_ctx = [&](uint32_t j, int &f0, int &ks, const uint8_t *&wq, const uint8_t *&ws) {
+            const int item = (int)blockIdx.x + (int)(j / nk) * (int)gridDim.x;
+            ks = (int)(j % nk);
             const Tile tl = a.tiles[tbeg + item / nft];
-            const int f0 = (item % nft) * a.m_tile;
+            f0 = (item % nft) * a.m_tile;
             const int64_t widx = a.slot_index ? (tl.chunk & 0xffff) : tl.expert;
-            const uint8_t *wq = a.wq + widx * a.wq_stride;
-            const uint8_t *ws = a.ws ? a.ws + widx * a.ws_stride : nullptr;
-            if (FMT == kFmtBF16) wq += 2 * a.w_off_elems;
-            for (int ks = 0; ks < nk; ++ks, ++g) {
-                const int s = g % kStages;
-                const uint32_t ph = (g / kStages) & 1;
-                if (!(ok = mbar_wait(empty(s), ph ^ 1, a.err, 5))) break;
-                Dequant<KIND, FMT>::stage(a, wq, ws, f0, ks, td, sA0 + s * kABytes);
-                fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(full_a(s));
+            wq = a.wq + widx * a.wq_stride + (FMT == kFmtBF16 ? 2 * a.w_off_elems : 0);
+            ws = a.ws ? a.ws + widx * a.ws_stride : nullptr;
+        };
+        auto issue_step = [&](uint32_t j) {
+            if (j < total) {
+                int f0, ks;
+                const uint8_t *wq, *ws;
+                step_ctx(j, f0, ks, wq, ws);
+                Dequant<KIND, FMT>::issue(a, wq, ws, f0, ks, td, raw_a + (j % kRing) * kRingStride);
             }
+            cpa_commit();
+        };
+        for (uint32_t j = 0; j + 1 < kRing; ++j) issue_step(j);
+        for (uint32_t g = 0; g < total; ++g) {
+            issue_step(g + kRing - 1);
+            cpa_wait<kRing - 1>();
+            int f0, ks;
+            const uint8_t *wq, *ws;
+            step_ctx(g, f0, ks, wq, ws);
+            const int s = g % kStages;
+            const uint32_t ph = (g / kStages) & 1;
+            if (!mbar_wait(empty(s), ph ^ 1, a.err, 5)) break;
+            Dequant<KIND, FMT>::convert(a, f0, ks, td, raw + (g % kRing) * kRingStride,
+                                        sA0 + s * kABytes);
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full_a(s));
         }
+        cpa_wait<0>();
     } else {
         // ---------------- epilogue (warps 0-3: TMEM lanes 32*warp .. +31)
         uint32_t li = 0;

@@ -16,10 +16,10 @@ void launch_kind(const CUtensorMap &tm, const TcArgs &a, cudaStream_t st)
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(k_gemm_tc<KIND, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes);
+                             (int)Pipe<FMT>::kSmem);
         attr = true;
     }
-    k_gemm_tc<KIND, FMT><<<num_sms(), kThreads, kSmemBytes, st>>>(tm, a);
+    k_gemm_tc<KIND, FMT><<<num_sms(), kThreads, Pipe<FMT>::kSmem, st>>>(tm, a);
     note_launch();
 }
 
