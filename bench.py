@@ -42,6 +42,7 @@ def parse():
     ap.add_argument("--mode", default="fused", choices=["fused", "scratch"])
     ap.add_argument("--chunk", type=int, default=0, help="experts per chunk (0: the config's C)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (0: the config's T)")
+    ap.add_argument("--experts", type=int, default=0, help="override E (0: the config's E)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -214,6 +215,8 @@ def main():
     cfg = gi.CONFIGS[args.config]
     if args.tokens:
         cfg = cfg.with_(T=args.tokens)
+    if args.experts:
+        cfg = cfg.with_(E=args.experts)
     if args.chunk:
         cfg = cfg.with_(C=args.chunk)
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -256,17 +259,34 @@ def main():
     dSd = None if L.S_down is None else torch.empty_like(L.S_down)
     b = cfg.b
 
-    def step(Xs, dYs):
+    PHASES = ("cayley", "route", "permute", "forward", "backward", "cayley_grad")
+    phase_ms = {p_: 0.0 for p_ in PHASES}
+    phase_ev = []
+
+    def mark(name, timed):
+        if timed:
+            e = torch.cuda.Event(enable_timing=True)
+            e.record()
+            phase_ev.append((name, e))
+
+    def step(Xs, dYs, timed=False):
+        mark("cayley", timed)
         if L.S_up is not None:   # R = Cayley(S) for the adapter of this step
             pmoe.adapter_cayley(L.S_up.numel() // (b * b), b, L.S_up, L.R_up, L.Rf_up)
             pmoe.adapter_cayley(L.S_down.numel() // (b * b), b, L.S_down, L.R_down, L.Rf_down)
+        mark("route", timed)
         L.route(Xs, rt)
+        mark("permute", timed)
         L.permute(rt)
+        mark("forward", timed)
         L.forward(Xs, rt, Y, C=cfg.C, mode=mode, ctx=ctx)
+        mark("backward", timed)
         L.backward(Xs, dYs, ctx, rt, dX, dtw, dRu, dRd, C=cfg.C)
+        mark("cayley_grad", timed)
         if L.S_up is not None:
             pmoe.adapter_cayley_grad(L.S_up.numel() // (b * b), b, L.S_up, L.Rf_up, dRu, dSu)
             pmoe.adapter_cayley_grad(L.S_down.numel() // (b * b), b, L.S_down, L.Rf_down, dRd, dSd)
+        mark("end", timed)
 
     for _ in range(args.warmup):
         step(X, dY)
@@ -292,6 +312,12 @@ def main():
         torch.cuda.synchronize()
     launches = pmoe.pmoe_launch_count() - n0
     ms = ev0.elapsed_time(ev1)
+    # one extra step with events between the calls: where the step's time goes
+    phase_ev.clear()
+    step(X, dY, timed=True)
+    torch.cuda.synchronize()
+    for (n_, e_), (_, f_) in zip(phase_ev[:-1], phase_ev[1:]):
+        phase_ms[n_] += e_.elapsed_time(f_)
     kt = {name: pmoe.pmoe_kernel_time(i) for i, name in enumerate(
         ("gemm_gate_up", "gemm_down", "gemm_bwd_g", "gemm_bwd_dx", "router"))}
     pmoe.pmoe_kernel_timing(False)
@@ -378,6 +404,7 @@ def main():
                     "flops": f_fwd + f_bwd, "bytes": B,
                     "peaks": f"{pk['src']}: bf16 {pk['bf16_sus']} TF/s sustained, HBM {pk['hbm']} GB/s"},
                 "roofline": roofline, "kernel_ms_per_step": {k_: v[0] / args.steps for k_, v in kt.items()},
+                "phase_ms": {k_: round(v, 3) for k_, v in phase_ms.items()},
                 "clocks": clk.summary(), "e2e": e2e, "gpu_launches": launches,
                 "cpu_baseline": cpu,
                 "scratch_bytes_per_chunk": pmoe.moe_scratch_bytes(L.dims, cfg.C, mode)}

@@ -9,71 +9,125 @@ namespace pmoe {
 
 // ------------------------------------------------------------------ Cayley
 // R = (I + S)(I - S)^{-1} = 2 (I - S)^{-1} - I.  The inverse comes from
-// Gauss-Jordan elimination on [I - S | I] without row exchanges: the
+// in-place Gauss-Jordan elimination of I - S without row exchanges: the
 // symmetric part of I - S is I (S is skew), so every leading minor is
 // nonzero and elimination without pivoting is stable (its growth is bounded
 // by 1 + |S|^2).  4*B threads per block matrix; thread (row r, quarter q)
-// keeps the 2B/4 entries of row r's quarter q in registers; the pivot row
-// goes through shared memory (double-buffered: one barrier per column).
+// keeps columns q*B/4 .. q*B/4 + B/4 - 1 of row r in registers.  Columns
+// are visited quarter by quarter with the inner loop unrolled, so every
+// register index is static; the pivot row goes through shared memory
+// (double-buffered: one barrier per column).
 template <int B>
 __global__ void __launch_bounds__(4 * B) k_cayley(const float *__restrict__ S,
                                                   uint16_t *__restrict__ Rb, float *__restrict__ Rf)
 {
-    constexpr int W = 2 * B, Q = W / 4;   // row width, entries per thread
-    __shared__ float prow[2][W];
+    constexpr int Q = B / 4;
+    constexpr unsigned kMask = 4 * B >= 32 ? 0xffffffffu : (1u << (4 * B)) - 1u;
+    __shared__ __align__(16) float prow[2][B];
     const int r = threadIdx.x >> 2, q = threadIdx.x & 3;
+    const int lane0 = threadIdx.x & 31 & ~3;   // lane of quarter 0 of this row
     const int64_t off = (int64_t)blockIdx.x * B * B;
     float v[Q];
 #pragma unroll
     for (int i = 0; i < Q; ++i) {
         const int c = q * Q + i;
-        v[i] = c < B ? (r == c ? 1.f : 0.f) - S[off + r * B + c] : (r == c - B ? 1.f : 0.f);
+        v[i] = (r == c ? 1.f : 0.f) - S[off + r * B + c];
     }
-    for (int col = 0; col < B; ++col) {
-        const int oq = col / Q, oi = col % Q;   // owner quarter and slot of column col
-        // value of column col in this row (lane of quarter oq of the same row)
-        float mine = 0.f;
+    for (int oq = 0; oq < 4; ++oq) {
 #pragma unroll
-        for (int i = 0; i < Q; ++i)
-            if (i == oi) mine = v[i];
-        constexpr unsigned kMask = 4 * B >= 32 ? 0xffffffffu : (1u << (4 * B)) - 1u;
-        const float colv = __shfl_sync(kMask, mine, (threadIdx.x & 31 & ~3) | oq);
-        float *pr = prow[col & 1];
-        if (r == col) {
-            const float inv = 1.f / colv;
+        for (int i = 0; i < Q; ++i) {
+            const int col = oq * Q + i;
+            const float colv = __shfl_sync(kMask, v[i], lane0 | oq);
+            float *pr = prow[col & 1];
+            const bool mine_col = q == oq;
+            if (r == col) {
+                // pivot row: a[col][:] /= a[col][col], with a[col][col] <- 1 / a[col][col]
+                const float p = 1.f / colv;
+                if (mine_col) v[i] = 1.f;
 #pragma unroll
-            for (int i = 0; i < Q; ++i) {
-                v[i] *= inv;
-                pr[q * Q + i] = v[i];
+                for (int j = 0; j < Q; ++j) v[j] *= p;
+#pragma unroll
+                for (int j = 0; j < Q; j += 4)
+                    *(float4 *)(pr + q * Q + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            }
+            __syncthreads();
+            if (r != col) {
+                // a[r][:] -= a[r][col] * a[col][:], with a[r][col] <- -a[r][col] / pivot
+                if (mine_col) v[i] = 0.f;
+#pragma unroll
+                for (int j = 0; j < Q; j += 4) {
+                    const float4 pv = *(const float4 *)(pr + q * Q + j);
+                    v[j] = fmaf(-colv, pv.x, v[j]);
+                    v[j + 1] = fmaf(-colv, pv.y, v[j + 1]);
+                    v[j + 2] = fmaf(-colv, pv.z, v[j + 2]);
+                    v[j + 3] = fmaf(-colv, pv.w, v[j + 3]);
+                }
             }
         }
-        __syncthreads();
-        if (r != col) {
-#pragma unroll
-            for (int i = 0; i < Q; ++i) v[i] = fmaf(-colv, pr[q * Q + i], v[i]);
-        }
     }
-    // right half holds A = (I - S)^{-1}; R = 2A - I
+    // v holds row r of A = (I - S)^{-1}; R = 2A - I
 #pragma unroll
     for (int i = 0; i < Q; ++i) {
-        const int c = q * Q + i - B;
-        if (c < 0) continue;
+        const int c = q * Q + i;
         const float rv = 2.f * v[i] - (r == c ? 1.f : 0.f);
         if (Rf) Rf[off + r * B + c] = rv;
         if (Rb) Rb[off + r * B + c] = f2bf(rv);
     }
 }
 
+// Small blocks (b <= 8): one thread per block matrix, the same in-place
+// elimination in registers.
+template <int B>
+__global__ void k_cayley_small(int nblk, const float *__restrict__ S, uint16_t *__restrict__ Rb,
+                               float *__restrict__ Rf)
+{
+    const int blk = blockIdx.x * blockDim.x + threadIdx.x;
+    if (blk >= nblk) return;
+    const int64_t off = (int64_t)blk * B * B;
+    float a[B][B];
+#pragma unroll
+    for (int r = 0; r < B; ++r)
+#pragma unroll
+        for (int c = 0; c < B; ++c) a[r][c] = (r == c ? 1.f : 0.f) - S[off + r * B + c];
+#pragma unroll
+    for (int k = 0; k < B; ++k) {
+        const float p = 1.f / a[k][k];
+        a[k][k] = 1.f;
+#pragma unroll
+        for (int j = 0; j < B; ++j) a[k][j] *= p;
+#pragma unroll
+        for (int r = 0; r < B; ++r) {
+            if (r == k) continue;
+            const float f = a[r][k];
+            a[r][k] = 0.f;
+#pragma unroll
+            for (int j = 0; j < B; ++j) a[r][j] = fmaf(-f, a[k][j], a[r][j]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < B; ++r)
+#pragma unroll
+        for (int c = 0; c < B; ++c) {
+            const float rv = 2.f * a[r][c] - (r == c ? 1.f : 0.f);
+            if (Rf) Rf[off + r * B + c] = rv;
+            if (Rb) Rb[off + r * B + c] = f2bf(rv);
+        }
+}
+
 // dL/dS for S skew: with A = (I - S)^{-1} = (I + R)/2, a perturbation dS
 // moves R by (I + R) dS A, so M = (I + R)^T G A^T = (I + R)^T G (I + R)^T / 2
-// and dS = M - M^T.  Two B x B products per block in shared memory.
+// and dS = M - M^T.  Two B x B products per block in shared memory, each
+// thread computing a 4 x 4 tile of the output (B >= 8; smaller blocks use
+// one thread per output).
 template <int B>
 __global__ void __launch_bounds__(256) k_cayley_grad(const float *__restrict__ Rf,
                                                      const float *__restrict__ G,
                                                      float *__restrict__ dS)
 {
     extern __shared__ float sm[];
-    constexpr int P = B + 1;   // padded pitch
+    constexpr int P = B + 4;   // padded pitch, keeps float4 alignment
+    constexpr int TS = B >= 8 ? 4 : 1;   // output tile side per thread
+    constexpr int NT = (B / TS) * (B / TS);
     float *Ip = sm, *Gs = sm + B * P, *T = sm + 2 * B * P;
     const int64_t off = (int64_t)blockIdx.x * B * B;
     for (int i = threadIdx.x; i < B * B; i += blockDim.x) {
@@ -82,20 +136,48 @@ __global__ void __launch_bounds__(256) k_cayley_grad(const float *__restrict__ R
         Gs[r * P + c] = G[off + i];
     }
     __syncthreads();
-    // T = (I + R)^T G
-    for (int i = threadIdx.x; i < B * B; i += blockDim.x) {
-        const int r = i / B, c = i % B;
-        float acc = 0.f;
-        for (int m = 0; m < B; ++m) acc = fmaf(Ip[m * P + r], Gs[m * P + c], acc);
-        T[r * P + c] = acc;
+    // T[r][c] = sum_m Ip[m][r] Gs[m][c]
+    for (int t = threadIdx.x; t < NT; t += blockDim.x) {
+        const int r0 = (t / (B / TS)) * TS, c0 = (t % (B / TS)) * TS;
+        float acc[TS][TS] = {};
+        for (int m = 0; m < B; ++m) {
+            float x[TS], y[TS];
+#pragma unroll
+            for (int u = 0; u < TS; ++u) {
+                x[u] = Ip[m * P + r0 + u];
+                y[u] = Gs[m * P + c0 + u];
+            }
+#pragma unroll
+            for (int u = 0; u < TS; ++u)
+#pragma unroll
+                for (int w = 0; w < TS; ++w) acc[u][w] = fmaf(x[u], y[w], acc[u][w]);
+        }
+#pragma unroll
+        for (int u = 0; u < TS; ++u)
+#pragma unroll
+            for (int w = 0; w < TS; ++w) T[(r0 + u) * P + c0 + w] = acc[u][w];
     }
     __syncthreads();
-    // M = T (I + R)^T / 2, stored over Gs
-    for (int i = threadIdx.x; i < B * B; i += blockDim.x) {
-        const int r = i / B, c = i % B;
-        float acc = 0.f;
-        for (int m = 0; m < B; ++m) acc = fmaf(T[r * P + m], Ip[c * P + m], acc);
-        Gs[r * P + c] = 0.5f * acc;
+    // M[r][c] = 1/2 sum_m T[r][m] Ip[c][m], written over Gs
+    for (int t = threadIdx.x; t < NT; t += blockDim.x) {
+        const int r0 = (t / (B / TS)) * TS, c0 = (t % (B / TS)) * TS;
+        float acc[TS][TS] = {};
+        for (int m = 0; m < B; ++m) {
+            float x[TS], y[TS];
+#pragma unroll
+            for (int u = 0; u < TS; ++u) {
+                x[u] = T[(r0 + u) * P + m];
+                y[u] = Ip[(c0 + u) * P + m];
+            }
+#pragma unroll
+            for (int u = 0; u < TS; ++u)
+#pragma unroll
+                for (int w = 0; w < TS; ++w) acc[u][w] = fmaf(x[u], y[w], acc[u][w]);
+        }
+#pragma unroll
+        for (int u = 0; u < TS; ++u)
+#pragma unroll
+            for (int w = 0; w < TS; ++w) Gs[(r0 + u) * P + c0 + w] = 0.5f * acc[u][w];
     }
     __syncthreads();
     for (int i = threadIdx.x; i < B * B; i += blockDim.x) {
@@ -107,13 +189,16 @@ __global__ void __launch_bounds__(256) k_cayley_grad(const float *__restrict__ R
 template <int B>
 static void cayley_b(int nblk, const float *S, uint16_t *Rb, float *Rf, cudaStream_t st)
 {
-    k_cayley<B><<<nblk, 4 * B, 0, st>>>(S, Rb, Rf);
+    if constexpr (B < 16)
+        k_cayley_small<B><<<(int)cdiv(nblk, 128), 128, 0, st>>>(nblk, S, Rb, Rf);
+    else
+        k_cayley<B><<<nblk, 4 * B, 0, st>>>(S, Rb, Rf);
 }
 
 template <int B>
 static void cayley_grad_b(int nblk, const float *Rf, const float *dR, float *dS, cudaStream_t st)
 {
-    const size_t sm = 3 * (size_t)B * (B + 1) * sizeof(float);
+    const size_t sm = 3 * (size_t)B * (B + 4) * sizeof(float);
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(k_cayley_grad<B>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);

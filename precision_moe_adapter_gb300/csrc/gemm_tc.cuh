@@ -292,13 +292,15 @@ __device__ __forceinline__ void cpa_wait()
 //   non-transposed: smem row m = td >> 1, K half = td & 1 (32 elements)
 //   transposed:     rows m = 8*(td & 15) .. +7, K = 4*(td >> 4) .. +3
 // issue() copies the thread's packed bytes (and the aligned 4-byte word
-// holding its scale) into its ring slot; convert() turns the slot into BF16
-// in the A stage.  Slot layouts:
-//   4-bit, non-transposed: q 16 B @0, scale word @16
-//   FP8,   non-transposed: q 32 B @0, scale @32
-//   BF16 (scratch):        64 B @0
-//   4-bit, transposed:     4 q words @0, 4 scale words @16
-//   FP8,   transposed:     4 x 8 B q @0, 4 scales @32
+// holding its scale) into the ring stage; convert() turns them into BF16 in
+// the A stage.  A ring stage is laid out by piece, not by thread: piece j of
+// thread td sits at j * 256 * size + td * size, so a warp reading its
+// pieces touches consecutive words (no bank conflicts).  Pieces:
+//   4-bit, non-transposed: q (16 B), scale word (4 B)
+//   FP8,   non-transposed: q0, q1 (16 B each), scale (4 B)
+//   BF16 (scratch):        4 x 16 B
+//   4-bit, transposed:     4 q words, 4 scale words (4 B each)
+//   FP8,   transposed:     4 x q (8 B), 4 scales (4 B)
 template <int KIND, int FMT>
 struct Dequant {
     static constexpr bool T = KindTraits<KIND>::kTrans;
@@ -313,7 +315,7 @@ struct Dequant {
     }
     __device__ static bool live(const TcArgs &a, int f0, int td)
     {
-        if (T) return f0 + 8 * (td & 15) < a.Mtot;
+        if (T) return f0 + 8 * (td >> 4) < a.Mtot;
         return KIND == GK_FWD_GU || f0 + (td >> 1) < a.Mtot;
     }
     // byte offset of the aligned 4-byte word holding scale index gi
@@ -327,6 +329,11 @@ struct Dequant {
         return (word >> (8 * (gi & 3))) & 0xFFu;
     }
 
+    // byte offsets of a thread's pieces inside a ring stage (256 threads)
+    __device__ static uint32_t p16(int j, int td) { return (uint32_t)(j * 256 + td) * 16; }
+    __device__ static uint32_t p8(int j, int td) { return (uint32_t)(j * 256 + td) * 8; }
+    __device__ static uint32_t p4(int j, int td) { return (uint32_t)(j * 256 + td) * 4; }
+
     __device__ static void issue(const TcArgs &a, const uint8_t *wq, const uint8_t *ws, int f0,
                                  int ks, int td, uint32_t slot)
     {
@@ -336,30 +343,30 @@ struct Dequant {
             const int64_t row = row_of(a, f0, m);
             const int64_t k0 = (int64_t)ks * kBK + 32 * half;
             if (FMT == PMOE_W_INT4_G32_BF16 || FMT == PMOE_W_MXFP4_G32_E8M0) {
-                cpa16(slot, wq + row * (a.Kst >> 1) + (k0 >> 1));
-                cpa4(slot + 16, ws + sword(row * (a.Kst >> 5) + (k0 >> 5)));
+                cpa16(slot + p16(0, td), wq + row * (a.Kst >> 1) + (k0 >> 1));
+                cpa4(slot + 256 * 16 + p4(0, td), ws + sword(row * (a.Kst >> 5) + (k0 >> 5)));
             } else if (FMT == PMOE_W_FP8_B128_F32) {
                 const uint8_t *src = wq + row * a.Kst + k0;
-                cpa16(slot, src);
-                cpa16(slot + 16, src + 16);
-                cpa4(slot + 32, ws + 4 * ((row >> 7) * (a.Kst >> 7) + (k0 >> 7)));
+                cpa16(slot + p16(0, td), src);
+                cpa16(slot + p16(1, td), src + 16);
+                cpa4(slot + 2 * 256 * 16 + p4(0, td), ws + 4 * ((row >> 7) * (a.Kst >> 7) + (k0 >> 7)));
             } else {
                 const uint8_t *src = wq + 2 * (row * a.Kst + k0);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) cpa16(slot + 16 * j, src + 16 * j);
+                for (int j = 0; j < 4; ++j) cpa16(slot + p16(j, td), src + 16 * j);
             }
         } else {
-            const int mg0 = f0 + 8 * (td & 15);
-            const int64_t n0 = (int64_t)ks * kBK + 4 * (td >> 4);
+            const int mg0 = f0 + 8 * (td >> 4);
+            const int64_t n0 = (int64_t)ks * kBK + 4 * (td & 15);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int64_t n = n0 + j;
                 if (FMT == PMOE_W_FP8_B128_F32) {
-                    cpa8(slot + 8 * j, wq + n * a.Kst + mg0);
-                    cpa4(slot + 32 + 4 * j, ws + 4 * ((n >> 7) * (a.Kst >> 7) + (mg0 >> 7)));
+                    cpa8(slot + p8(j, td), wq + n * a.Kst + mg0);
+                    cpa4(slot + 4 * 256 * 8 + p4(j, td), ws + 4 * ((n >> 7) * (a.Kst >> 7) + (mg0 >> 7)));
                 } else {
-                    cpa4(slot + 4 * j, wq + n * (a.Kst >> 1) + (mg0 >> 1));
-                    cpa4(slot + 16 + 4 * j, ws + sword(n * (a.Kst >> 5) + (mg0 >> 5)));
+                    cpa4(slot + p4(j, td), wq + n * (a.Kst >> 1) + (mg0 >> 1));
+                    cpa4(slot + 4 * 256 * 4 + p4(j, td), ws + sword(n * (a.Kst >> 5) + (mg0 >> 5)));
                 }
             }
         }
@@ -379,8 +386,9 @@ struct Dequant {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) out[j] = make_uint4(0, 0, 0, 0);
             } else if (FMT == PMOE_W_INT4_G32_BF16) {
-                const uint4 q = *(const uint4 *)slot;
-                const uint32_t sb = spick(*(const uint32_t *)(slot + 16), row * (a.Kst >> 5) + (k0 >> 5));
+                const uint4 q = *(const uint4 *)(slot + p16(0, td));
+                const uint32_t sb = spick(*(const uint32_t *)(slot + 256 * 16 + p4(0, td)),
+                                          row * (a.Kst >> 5) + (k0 >> 5));
                 const uint32_t s2 = sb | (sb << 16);
                 const uint32_t words[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -393,8 +401,9 @@ struct Dequant {
                     out[j].w = prmt(p[2], p[3], 0x7632);
                 }
             } else if (FMT == PMOE_W_MXFP4_G32_E8M0) {
-                const uint4 q = *(const uint4 *)slot;
-                const float sc = e8m0_value(spick(*(const uint32_t *)(slot + 16), row * (a.Kst >> 5) + (k0 >> 5)));
+                const uint4 q = *(const uint4 *)(slot + p16(0, td));
+                const float sc = e8m0_value(spick(*(const uint32_t *)(slot + 256 * 16 + p4(0, td)),
+                                                  row * (a.Kst >> 5) + (k0 >> 5)));
                 const uint32_t words[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -406,8 +415,9 @@ struct Dequant {
                     out[j] = make_uint4(o[0], o[1], o[2], o[3]);
                 }
             } else if (FMT == PMOE_W_FP8_B128_F32) {
-                const uint4 q0 = *(const uint4 *)slot, q1 = *(const uint4 *)(slot + 16);
-                const float sc = *(const float *)(slot + 32);
+                const uint4 q0 = *(const uint4 *)(slot + p16(0, td));
+                const uint4 q1 = *(const uint4 *)(slot + p16(1, td));
+                const float sc = *(const float *)(slot + 2 * 256 * 16 + p4(0, td));
                 const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -426,7 +436,7 @@ struct Dequant {
                 }
             } else {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) out[j] = *(const uint4 *)(slot + 16 * j);
+                for (int j = 0; j < 4; ++j) out[j] = *(const uint4 *)(slot + p16(j, td));
             }
             const uint32_t rowaddr = sA + m * 128;
 #pragma unroll
@@ -436,7 +446,9 @@ struct Dequant {
             }
         } else {
             // transposed: A[m][k] = W[k0 + k][f0 + m] (contraction over stored rows)
-            const int mb = td & 15, kb = td >> 4;
+            // lanes vary kb (K chunks of one row m): the 8-byte stores of a warp
+            // cover whole 128-byte rows, conflict-free
+            const int kb = td & 15, mb = td >> 4;
             const int mg0 = f0 + 8 * mb;
             const int64_t n0 = (int64_t)ks * kBK + 4 * kb;
             uint32_t v[8][2];   // for each m: (k0,k1), (k2,k3)
@@ -447,8 +459,8 @@ struct Dequant {
                 uint32_t p[4][4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint32_t w = *(const uint32_t *)(slot + 4 * j);
-                    const uint32_t sb = spick(*(const uint32_t *)(slot + 16 + 4 * j),
+                    const uint32_t w = *(const uint32_t *)(slot + p4(j, td));
+                    const uint32_t sb = spick(*(const uint32_t *)(slot + 4 * 256 * 4 + p4(j, td)),
                                               (n0 + j) * (a.Kst >> 5) + (mg0 >> 5));
                     int4x8_pairs(w, sb | (sb << 16), p[j]);
                 }
@@ -464,14 +476,14 @@ struct Dequant {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     if (FMT == PMOE_W_MXFP4_G32_E8M0) {
-                        const uint32_t w = *(const uint32_t *)(slot + 4 * j);
-                        const float sc = e8m0_value(spick(*(const uint32_t *)(slot + 16 + 4 * j),
+                        const uint32_t w = *(const uint32_t *)(slot + p4(j, td));
+                        const float sc = e8m0_value(spick(*(const uint32_t *)(slot + 4 * 256 * 4 + p4(j, td)),
                                                           (n0 + j) * (a.Kst >> 5) + (mg0 >> 5)));
 #pragma unroll
                         for (int i = 0; i < 8; ++i) f[j][i] = __fmul_rn(e2m1_value((w >> (4 * i)) & 15u), sc);
                     } else {
-                        const uint2 w = *(const uint2 *)(slot + 8 * j);
-                        const float sc = *(const float *)(slot + 32 + 4 * j);
+                        const uint2 w = *(const uint2 *)(slot + p8(j, td));
+                        const float sc = *(const float *)(slot + 4 * 256 * 8 + p4(j, td));
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
                             f[j][i] = __fmul_rn(e4m3_value(((i < 4 ? w.x : w.y) >> (8 * (i & 3))) & 255u), sc);
@@ -596,40 +608,44 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
         // ---------------- dequant producers: packed weights prefetched
         // kRawStages - 1 steps ahead with cp.async, converted into the A stage
         const int td = threadIdx.x - kDqWarp0 * 32;
-        uint8_t *raw = smem + PP::kRawOff + td * PP::kSlot;
+        uint8_t *raw = smem + PP::kRawOff;
         const uint32_t raw_a = smem_u32(raw);
         const int my_items = n_items > (int)blockIdx.x ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
         const uint32_t total = (uint32_t)my_items * nk;
         constexpr uint32_t kRing = PP::kRawStages, kRingStride = 256 * PP::kSlot;
-        auto step_ctx = [&](uint32_t j, int &f0, int &ks, const uint8_t *&wq, const uint8_t *&ws) {
-            const int item = (int)blockIdx.x + (int)(j / nk) * (int)gridDim.x;
-            ks = (int)(j % nk);
-            const Tile tl = a.tiles[tbeg + item / nft];
-            f0 = (item % nft) * a.m_tile;
-            const int64_t widx = a.slot_index ? (tl.chunk & 0xffff) : tl.expert;
-            wq = a.wq + widx * a.wq_stride + (FMT == kFmtBF16 ? 2 * a.w_off_elems : 0);
-            ws = a.ws ? a.ws + widx * a.ws_stride : nullptr;
+        // work-item context, reloaded only when a step starts a new item
+        struct Ctx {
+            int li = -1, f0 = 0;
+            const uint8_t *wq = nullptr, *ws = nullptr;
         };
+        auto load_ctx = [&](Ctx &c, int li) {
+            if (c.li == li) return;
+            const int item = (int)blockIdx.x + li * (int)gridDim.x;
+            const Tile tl = a.tiles[tbeg + item / nft];
+            c.li = li;
+            c.f0 = (item % nft) * a.m_tile;
+            const int64_t widx = a.slot_index ? (tl.chunk & 0xffff) : tl.expert;
+            c.wq = a.wq + widx * a.wq_stride + (FMT == kFmtBF16 ? 2 * a.w_off_elems : 0);
+            c.ws = a.ws ? a.ws + widx * a.ws_stride : nullptr;
+        };
+        Ctx cur, ahead;
         auto issue_step = [&](uint32_t j) {
             if (j < total) {
-                int f0, ks;
-                const uint8_t *wq, *ws;
-                step_ctx(j, f0, ks, wq, ws);
-                Dequant<KIND, FMT>::issue(a, wq, ws, f0, ks, td, raw_a + (j % kRing) * kRingStride);
+                load_ctx(ahead, (int)(j / nk));
+                Dequant<KIND, FMT>::issue(a, ahead.wq, ahead.ws, ahead.f0, (int)(j % nk), td,
+                                          raw_a + (j % kRing) * kRingStride);
             }
             cpa_commit();
         };
         for (uint32_t j = 0; j + 1 < kRing; ++j) issue_step(j);
         for (uint32_t g = 0; g < total; ++g) {
             issue_step(g + kRing - 1);
+            load_ctx(cur, (int)(g / nk));
             cpa_wait<kRing - 1>();
-            int f0, ks;
-            const uint8_t *wq, *ws;
-            step_ctx(g, f0, ks, wq, ws);
             const int s = g % kStages;
             const uint32_t ph = (g / kStages) & 1;
             if (!mbar_wait(empty(s), ph ^ 1, a.err, 5)) break;
-            Dequant<KIND, FMT>::convert(a, f0, ks, td, raw + (g % kRing) * kRingStride,
+            Dequant<KIND, FMT>::convert(a, cur.f0, (int)(g % nk), td, raw + (g % kRing) * kRingStride,
                                         sA0 + s * kABytes);
             fence_proxy_async();
             __syncwarp();
@@ -677,20 +693,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                 } else if (KIND == GK_BWD_G) {
                     const int f = f0 + 32 * q + lane;
                     const bool fl = f < a.Mtot;
+                    const int ncol = min(32, tl.nrows - c0);
+                    // routing weight of column `lane` (one load per lane, then broadcast)
+                    const float w_lane = lane < ncol ? a.w[a.perm[tl.row0 + c0 + lane]] : 0.f;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int col = c0 + j;
-                        if (col >= tl.nrows) break;
-                        const int64_t r = tl.row0 + col;
-                        float part = 0.f;
-                        if (fl) {
-                            const float wr = a.w[a.perm[r]];
-                            a.out[r * a.Mtot + f] = f2bf(wr * v[j]);
-                            part = v[j] * bf2f(a.ht[r * a.Mtot + f]);
+                    for (int hh = 0; hh < 32; hh += 16) {
+                        uint16_t hts[16];   // h~ of the 16 columns, loaded together
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            hts[j] = (fl && hh + j < ncol)
+                                         ? a.ht[(int64_t)(tl.row0 + c0 + hh + j) * a.Mtot + f]
+                                         : 0;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int jj = hh + j;
+                            const float wr = __shfl_sync(0xffffffffu, w_lane, jj);
+                            const int64_t r = tl.row0 + c0 + jj;
+                            float part = fl ? v[jj] * bf2f(hts[j]) : 0.f;
+                            if (fl && jj < ncol) a.out[r * a.Mtot + f] = f2bf(wr * v[jj]);
+#pragma unroll
+                            for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                            if (fl && lane == 0 && jj < ncol)
+                                a.dtw_part[r * (a.Mtot / 32) + (f0 + 32 * q) / 32] = part;
                         }
-#pragma unroll
-                        for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-                        if (fl && lane == 0) a.dtw_part[r * (a.Mtot / 32) + (f0 + 32 * q) / 32] = part;
                     }
                 } else {
                     const int f = f0 + 32 * q + lane;
