@@ -399,6 +399,7 @@ pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const p
     gu.out = w.h;
     gu.ctx = (uint16_t *)ctx;
     gu.I = I;
+    gu.nmat = dims.E;
     GemmArgs dn{};
     dn.kind = GK_FWD_DOWN;
     dn.A = R_dn ? w.ht : w.h;
@@ -410,6 +411,7 @@ pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const p
     dn.chunk_tiles = L.chunk_tiles;
     dn.out = w.o;
     dn.I = I;
+    dn.nmat = dims.E;
     pmoe_status gs;
 
     if (mode == PMOE_MODE_FUSED) {
@@ -447,6 +449,7 @@ pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const p
         gu.w_off_elems = 0;
         dn.w_off_elems = 2 * (int64_t)I * d;
         gu.slot_index = dn.slot_index = true;
+        gu.nmat = dn.nmat = C;
         for (int c = 0; c < nch; ++c) {
             launch_dequant_chunk(fmt, d, I, C, c, rt->active, rt->num_active, wts->w13, wts->s13,
                                  wts->w2, wts->s2, w.scratch, stream);
@@ -541,6 +544,7 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
     g.perm = rt->perm;
     g.ht = w.ht;
     g.dtw_part = w.dtw_part;
+    g.nmat = E;
     {
         ScopedTimer tm(PMOE_KT_GEMM_BWD_G, stream);
         if ((gs = run_gemm(g, P, w.err, stream)) != PMOE_OK) return gs;
@@ -572,6 +576,7 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
     x.c1 = nch;
     x.out = w.dxt;
     x.I = I;
+    x.nmat = E;
     {
         ScopedTimer tm(PMOE_KT_GEMM_BWD_DX, stream);
         if ((gs = run_gemm(x, P, w.err, stream)) != PMOE_OK) return gs;
@@ -676,6 +681,7 @@ pmoe_status moe_grouped_gemm(pmoe_wfmt fmt, const void *q, const void *s, int32_
     g.c1 = 1;
     g.out = (uint16_t *)out;
     g.I = N;
+    g.nmat = E;
     pmoe_status gs = run_gemm(g, rows, w.err, stream);
     if (gs != PMOE_OK) return gs;
     return launched(stream);

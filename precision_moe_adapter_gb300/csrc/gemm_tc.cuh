@@ -227,6 +227,7 @@ struct TcArgs {
     const uint8_t *ws;          // scales of expert 0
     int64_t wq_stride, ws_stride;
     int64_t Kst;                // columns of one expert's stored [N, K] matrix
+    int64_t Nst;                // rows of one expert's stored matrix
     int64_t w_off_elems;        // BF16 scratch: element offset of the matrix in a slot
     int K;                      // contraction length
     int Mtot;                   // output features
@@ -252,18 +253,30 @@ struct KindTraits {
 };
 
 // ------------------------------------------------------------------ pipeline sizes
-// Per weight format: A/B shared-memory stages and the ring of packed-weight
-// prefetches (kRawStages steps in flight, kSlot bytes per thread and step).
-template <int FMT>
+// Per kind and weight format.  Non-transposed kinds get their packed weight
+// tile by TMA (raw ring of kRawTma stages: 128 rows of kRowBytes, then 128
+// scale words fetched by the producer warp's lanes with cp.async).  BF16
+// scratch weights come by TMA straight into the swizzled A stage.  The
+// transposed kinds (contraction over the stored rows) prefetch per thread
+// with cp.async (ring of kRawStages steps, kSlot bytes per thread).
+template <int KIND, int FMT>
 struct Pipe {
-    static constexpr bool k4bit = FMT == PMOE_W_INT4_G32_BF16 || FMT == PMOE_W_MXFP4_G32_E8M0;
-    static constexpr int kStagesAB = k4bit ? 4 : 3;
+    static constexpr bool kTrans = KIND == GK_BWD_G || KIND == GK_BWD_DX;
+    static constexpr bool kBf16 = FMT == kFmtBF16;
+    static constexpr bool kTmaRaw = !kTrans && !kBf16;
+    static constexpr bool kFp8 = FMT == PMOE_W_FP8_B128_F32;
+    static constexpr int kStagesAB = kFp8 ? 3 : 4;
+    static constexpr int kRowBytes = kFp8 ? 64 : 32;
+    static constexpr int kRawTile = 128 * kRowBytes + 128 * 4;
+    static constexpr int kRawTma = 4;
     static constexpr int kRawStages = 4;
-    static constexpr int kSlot = FMT == PMOE_W_FP8_B128_F32 ? 48 : (FMT == kFmtBF16 ? 64 : 32);
-    static constexpr int kRawBytes = kRawStages * 256 * kSlot;
+    static constexpr int kSlot = kFp8 ? 48 : 32;
+    static constexpr int kRawBytes =
+        kTmaRaw ? kRawTma * kRawTile : (kTrans ? kRawStages * 256 * kSlot : 0);
+    static constexpr int kNumBars = 3 * kStagesAB + 4 + 2 * kRawTma;
     static constexpr int kBarOff = kStagesAB * (kABytes + kBBytes);
-    static constexpr int kBarBytes = 8 * (3 * kStagesAB + 4) + 16;
-    static constexpr int kRawOff = (kBarOff + kBarBytes + 127) & ~127;
+    static constexpr int kBarBytes = 8 * kNumBars + 16;
+    static constexpr int kRawOff = (kBarOff + kBarBytes + 1023) & ~1023;
     static constexpr size_t kSmem = (size_t)kRawOff + kRawBytes + 1024;
     static_assert(kSmem <= 232448, "shared memory budget");
 };
@@ -281,6 +294,20 @@ __device__ __forceinline__ void cpa4(uint32_t dst, const void *src)
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// arrive on `bar` once this thread's earlier cp.async copies have landed
+__device__ __forceinline__ void cpa_mbar_arrive(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm, int x, int y, int z,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+            dst),
+        "l"((uint64_t)tm), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
 template <int N>
 __device__ __forceinline__ void cpa_wait()
 {
@@ -327,6 +354,99 @@ struct Dequant {
     {
         if (FMT == PMOE_W_INT4_G32_BF16) return (gi & 1) ? word >> 16 : word & 0xFFFFu;
         return (word >> (8 * (gi & 3))) & 0xFFu;
+    }
+
+    // raw-tile row of A row m: GU tiles hold [gate rows | up rows] (64 each)
+    __device__ static int raw_row(int m)
+    {
+        if (KIND != GK_FWD_GU) return m;
+        const int q = m >> 5, r = m & 31;
+        return r < 16 ? 16 * q + r : 64 + 16 * q + r - 16;
+    }
+    // stored row of raw-tile row rr
+    __device__ static int64_t stored_row(const TcArgs &a, int f0, int rr)
+    {
+        if (KIND == GK_FWD_GU) return rr < 64 ? (int64_t)(f0 + rr) : (int64_t)(a.I + f0 + rr - 64);
+        return f0 + rr;
+    }
+    // byte offset of the aligned scale word of stored row `row` for step ks
+    __device__ static int64_t scale_word(const TcArgs &a, int64_t row, int ks)
+    {
+        if (FMT == PMOE_W_INT4_G32_BF16) return 2 * (row * (a.Kst >> 5) + 2 * ks);
+        if (FMT == PMOE_W_MXFP4_G32_E8M0) return (row * (a.Kst >> 5) + 2 * ks) & ~(int64_t)3;
+        return 4 * ((row >> 7) * (a.Kst >> 7) + ((int64_t)ks * kBK >> 7));
+    }
+
+    // Convert one TMA raw tile (non-transposed kinds) into the A stage.
+    // Thread: A row m = td >> 1, K half = td & 1 (32 elements).
+    __device__ static void convert_tma(const TcArgs &a, int f0, int ks, int td, const uint8_t *rawt,
+                                       uint32_t sA)
+    {
+        using PP = Pipe<KIND, FMT>;
+        const int m = td >> 1, half = td & 1;
+        const int rr = raw_row(m);
+        const bool lv = KIND == GK_FWD_GU || f0 + m < a.Mtot;
+        const uint8_t *row = rawt + rr * PP::kRowBytes;
+        const uint32_t sw = *(const uint32_t *)(rawt + 128 * PP::kRowBytes + 4 * rr);
+        uint4 out[4];
+        if (!lv) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) out[j] = make_uint4(0, 0, 0, 0);
+        } else if (FMT == PMOE_W_INT4_G32_BF16) {
+            const uint4 q = *(const uint4 *)(row + 16 * half);
+            const uint32_t sb = half ? sw >> 16 : sw & 0xFFFFu;
+            const uint32_t s2 = sb | (sb << 16);
+            const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t p[4];
+                int4x8_pairs(words[j], s2, p);
+                out[j].x = prmt(p[0], p[1], 0x5410);
+                out[j].y = prmt(p[2], p[3], 0x5410);
+                out[j].z = prmt(p[0], p[1], 0x7632);
+                out[j].w = prmt(p[2], p[3], 0x7632);
+            }
+        } else if (FMT == PMOE_W_MXFP4_G32_E8M0) {
+            const uint4 q = *(const uint4 *)(row + 16 * half);
+            const int64_t gi = stored_row(a, f0, rr) * (a.Kst >> 5) + 2 * ks + half;
+            const float sc = e8m0_value((sw >> (8 * (gi & 3))) & 0xFFu);
+            const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t w = words[j], o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    o[e] = pack_bf2(__fmul_rn(e2m1_value((w >> (8 * e)) & 15u), sc),
+                                    __fmul_rn(e2m1_value((w >> (8 * e + 4)) & 15u), sc));
+                out[j] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        } else {
+            const uint4 q0 = *(const uint4 *)(row + 32 * half);
+            const uint4 q1 = *(const uint4 *)(row + 32 * half + 16);
+            const float sc = __uint_as_float(sw);
+            const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t o[4];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t w = words[2 * j + h];
+                    __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3);
+                    __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+                    const float2 fl = __half22float2(*(const __half2 *)&lo);
+                    const float2 fh = __half22float2(*(const __half2 *)&hi);
+                    o[2 * h] = pack_bf2(__fmul_rn(fl.x, sc), __fmul_rn(fl.y, sc));
+                    o[2 * h + 1] = pack_bf2(__fmul_rn(fh.x, sc), __fmul_rn(fh.y, sc));
+                }
+                out[j] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+        const uint32_t rowaddr = sA + m * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int c = 4 * half + j;
+            st_shared_v4(rowaddr + ((c ^ (m & 7)) << 4), out[j]);
+        }
     }
 
     // byte offsets of a thread's pieces inside a ring stage (256 threads)
@@ -510,21 +630,25 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.f + expf(-g)); 
 // ------------------------------------------------------------------ kernel
 template <int KIND, int FMT>
 __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__ CUtensorMap tmB,
+                                                         const __grid_constant__ CUtensorMap tmA,
                                                          const TcArgs a)
 {
-    using PP = Pipe<FMT>;
+    using PP = Pipe<KIND, FMT>;
     constexpr int kStages = PP::kStagesAB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sA0 = smem_u32(smem);
     const uint32_t sB0 = sA0 + kStages * kABytes;
     const uint32_t bar0 = sB0 + kStages * kBBytes;
-    uint32_t *tmem_slot = (uint32_t *)(smem + PP::kBarOff + 8 * (3 * kStages + 4));
+    uint32_t *tmem_slot = (uint32_t *)(smem + PP::kBarOff + 8 * PP::kNumBars);
     auto full_a = [&](int s) { return bar0 + 8 * s; };
     auto full_b = [&](int s) { return bar0 + 8 * (kStages + s); };
     auto empty = [&](int s) { return bar0 + 8 * (2 * kStages + s); };
     auto tfull = [&](int c) { return bar0 + 8 * (3 * kStages + c); };
     auto tempty = [&](int c) { return bar0 + 8 * (3 * kStages + 2 + c); };
+    auto raw_full = [&](int r) { return bar0 + 8 * (3 * kStages + 4 + r); };
+    auto raw_empty = [&](int r) { return bar0 + 8 * (3 * kStages + 4 + PP::kRawTma + r); };
+    const uint32_t raw0 = smem_u32(smem + PP::kRawOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tbeg = a.chunk_tiles[a.c0], tend = a.chunk_tiles[a.c1];
@@ -534,13 +658,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(full_a(s), kDqWarps);
+            mbar_init(full_a(s), PP::kBf16 ? 1 : kDqWarps);
             mbar_init(full_b(s), 1);
             mbar_init(empty(s), 1);
         }
         for (int c = 0; c < 2; ++c) {
             mbar_init(tfull(c), 1);
             mbar_init(tempty(c), kEpiWarps);
+        }
+        for (int r = 0; r < PP::kRawTma; ++r) {
+            mbar_init(raw_full(r), 1 + 32);   // TMA transaction + the 32 lanes' scale copies
+            mbar_init(raw_empty(r), kDqWarps);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
@@ -558,21 +686,68 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     const uint32_t tmem = *(volatile uint32_t *)tmem_slot;
 
     if (warp == kProdWarp) {
-        // ---------------- TMA producer of the token tiles
-        if (lane == 0) {
-            uint32_t g = 0;
-            bool ok = true;
-            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-                const Tile tl = a.tiles[tbeg + item / nft];
-                const int nbox = (tl.nrows + kBoxRows - 1) / kBoxRows;
-                for (int ks = 0; ks < nk; ++ks, ++g) {
-                    const int s = g % kStages;
-                    const uint32_t ph = (g / kStages) & 1;
-                    if (!(ok = mbar_wait(empty(s), ph ^ 1, a.err, 1))) break;
+        // ---------------- producer: token tiles (TMA), packed weight tiles
+        // (TMA) with their scale words (cp.async by the 32 lanes), or BF16
+        // weight tiles (TMA into the swizzled A stage)
+        uint32_t g = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+            const Tile tl = a.tiles[tbeg + item / nft];
+            const int nbox = (tl.nrows + kBoxRows - 1) / kBoxRows;
+            const int f0 = (item % nft) * a.m_tile;
+            const int64_t widx = a.slot_index ? (tl.chunk & 0xffff) : tl.expert;
+            for (int ks = 0; ks < nk; ++ks, ++g) {
+                if constexpr (PP::kTmaRaw) {
+                    const int r = g % PP::kRawTma;
+                    if (!(ok = mbar_wait(raw_empty(r), ((g / PP::kRawTma) & 1) ^ 1, a.err, 7))) break;
+                    const uint32_t dst = raw0 + r * PP::kRawTile;
+                    if (lane == 0) {
+                        mbar_expect_tx(raw_full(r), 128 * PP::kRowBytes);
+                        const int x = ks * PP::kRowBytes;
+                        const int y = (int)(widx * a.Nst) + f0;
+                        if (KIND == GK_FWD_GU) {
+                            tma_load_2d(dst, &tmA, x, y, raw_full(r));
+                            tma_load_2d(dst + 64 * PP::kRowBytes, &tmA, x, y + a.I, raw_full(r));
+                        } else {
+                            tma_load_2d(dst, &tmA, x, y, raw_full(r));
+                        }
+                    }
+                    const uint8_t *ws = a.ws + widx * a.ws_stride;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int rr = lane + 32 * i;
+                        const bool lv = KIND == GK_FWD_GU || f0 + rr < a.Mtot;
+                        if (lv)
+                            cpa4(dst + 128 * PP::kRowBytes + 4 * rr,
+                                 ws + Dequant<KIND, FMT>::scale_word(
+                                          a, Dequant<KIND, FMT>::stored_row(a, f0, rr), ks));
+                    }
+                    cpa_mbar_arrive(raw_full(r));
+                }
+                const int s = g % kStages;
+                const uint32_t ph = (g / kStages) & 1;
+                if (!(ok = mbar_wait(empty(s), ph ^ 1, a.err, 1))) break;
+                if (lane == 0) {
                     mbar_expect_tx(full_b(s), nbox * kBoxBytes);
                     for (int bx = 0; bx < nbox; ++bx)
                         tma_load_2d(sB0 + s * kBBytes + bx * kBoxBytes, &tmB, ks * kBK,
                                     tl.row0 + bx * kBoxRows, full_b(s));
+                    if constexpr (PP::kBf16) {
+                        mbar_expect_tx(full_a(s), kABytes);
+                        const int slot = (int)widx;
+                        if (KIND == GK_FWD_GU) {
+                            // A rows 32q .. 32q+15: gate f0+16q ..; 32q+16 .. 32q+31: up
+#pragma unroll
+                            for (int qq = 0; qq < 4; ++qq) {
+                                tma_load_3d(sA0 + s * kABytes + (32 * qq) * 128, &tmA, ks * kBK,
+                                            f0 + 16 * qq, slot, full_a(s));
+                                tma_load_3d(sA0 + s * kABytes + (32 * qq + 16) * 128, &tmA, ks * kBK,
+                                            a.I + f0 + 16 * qq, slot, full_a(s));
+                            }
+                        } else {
+                            tma_load_3d(sA0 + s * kABytes, &tmA, ks * kBK, f0, slot, full_a(s));
+                        }
+                    }
                 }
             }
         }
@@ -605,9 +780,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             }
         }
     } else if (warp >= kDqWarp0) {
+        const int td = threadIdx.x - kDqWarp0 * 32;
+        if constexpr (PP::kTmaRaw) {
+            // ---------------- converters: TMA raw tile -> BF16 A stage
+            uint32_t g = 0;
+            for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+                const int f0 = (item % nft) * a.m_tile;
+                bool ok = true;
+                for (int ks = 0; ks < nk; ++ks, ++g) {
+                    const int s = g % kStages;
+                    const int r = g % PP::kRawTma;
+                    if (!(ok = mbar_wait(empty(s), ((g / kStages) & 1) ^ 1, a.err, 5))) break;
+                    if (!(ok = mbar_wait(raw_full(r), (g / PP::kRawTma) & 1, a.err, 8))) break;
+                    Dequant<KIND, FMT>::convert_tma(a, f0, ks, td, smem + PP::kRawOff + r * PP::kRawTile,
+                                                    sA0 + s * kABytes);
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(raw_empty(r));
+                        mbar_arrive(full_a(s));
+                    }
+                }
+                if (!ok) break;
+            }
+        } else if constexpr (PP::kTrans) {
         // ---------------- dequant producers: packed weights prefetched
         // kRawStages - 1 steps ahead with cp.async, converted into the A stage
-        const int td = threadIdx.x - kDqWarp0 * 32;
         uint8_t *raw = smem + PP::kRawOff;
         const uint32_t raw_a = smem_u32(raw);
         const int my_items = n_items > (int)blockIdx.x ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
@@ -652,6 +850,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             if (lane == 0) mbar_arrive(full_a(s));
         }
         cpa_wait<0>();
+        }
     } else {
         // ---------------- epilogue (warps 0-3: TMEM lanes 32*warp .. +31)
         uint32_t li = 0;

@@ -2,25 +2,48 @@
 // weight format (instantiated once per format in its own translation unit).
 #pragma once
 
+#include <cstring>
+
 #include "gemm_tc.cuh"
 
 namespace pmoe {
 namespace tc {
 
 bool make_rows_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t cols);
+// uint8 [rows, row_bytes] tensor, box of box_rows x box_bytes, no swizzle
+bool make_bytes_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t row_bytes,
+                     int box_bytes, int box_rows);
+// BF16 scratch slots [slots][rows][cols], box 64 cols x box_rows, 128-byte swizzle
+bool make_slots_tmap(CUtensorMap *m, const void *base, int64_t slots, int64_t rows, int64_t cols,
+                     int64_t slot_bytes, int box_rows);
 int num_sms();
 
 template <int KIND, int FMT>
-void launch_kind(const CUtensorMap &tm, const TcArgs &a, cudaStream_t st)
+bool launch_kind(const CUtensorMap &tm, const TcArgs &a, int64_t nmat, cudaStream_t st)
 {
+    using PP = Pipe<KIND, FMT>;
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(k_gemm_tc<KIND, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)Pipe<FMT>::kSmem);
+                             (int)PP::kSmem);
         attr = true;
     }
-    k_gemm_tc<KIND, FMT><<<num_sms(), kThreads, Pipe<FMT>::kSmem, st>>>(tm, a);
+    CUtensorMap tmA;
+    memset(&tmA, 0, sizeof tmA);
+    if constexpr (PP::kTmaRaw) {
+        // packed weights of all experts as one [nmat * Nst, row bytes] byte tensor
+        const int64_t rb = FMT == PMOE_W_FP8_B128_F32 ? a.Kst : a.Kst / 2;
+        if (!make_bytes_tmap(&tmA, a.wq, nmat * a.Nst, rb, PP::kRowBytes,
+                             KIND == GK_FWD_GU ? 64 : 128))
+            return false;
+    } else if constexpr (PP::kBf16) {
+        if (!make_slots_tmap(&tmA, a.wq + 2 * a.w_off_elems, nmat, a.Nst, a.Kst, a.wq_stride,
+                             KIND == GK_FWD_GU ? 16 : 128))
+            return false;
+    }
+    k_gemm_tc<KIND, FMT><<<num_sms(), kThreads, PP::kSmem, st>>>(tm, tmA, a);
     note_launch();
+    return true;
 }
 
 template <int FMT>
@@ -35,6 +58,7 @@ bool launch_fmt(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st)
     a.wq_stride = g.wq_stride;
     a.ws_stride = g.ws_stride;
     a.Kst = g.Kst;
+    a.Nst = g.Nst;
     a.w_off_elems = g.w_off_elems;
     a.K = g.K;
     a.Mtot = g.Nout;
@@ -53,19 +77,16 @@ bool launch_fmt(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st)
     a.dtw_part = g.dtw_part;
     a.err = err;
     switch (g.kind) {
-    case GK_FWD_GU: launch_kind<GK_FWD_GU, FMT>(tm, a, st); break;
-    case GK_FWD_DOWN: launch_kind<GK_FWD_DOWN, FMT>(tm, a, st); break;
+    case GK_FWD_GU: return launch_kind<GK_FWD_GU, FMT>(tm, a, g.nmat, st);
+    case GK_FWD_DOWN: return launch_kind<GK_FWD_DOWN, FMT>(tm, a, g.nmat, st);
     case GK_BWD_G:
-        if constexpr (FMT != kFmtBF16) launch_kind<GK_BWD_G, FMT>(tm, a, st);
-        else return false;
-        break;
+        if constexpr (FMT != kFmtBF16) return launch_kind<GK_BWD_G, FMT>(tm, a, g.nmat, st);
+        return false;
     case GK_BWD_DX:
-        if constexpr (FMT != kFmtBF16) launch_kind<GK_BWD_DX, FMT>(tm, a, st);
-        else return false;
-        break;
-    default: return false;
+        if constexpr (FMT != kFmtBF16) return launch_kind<GK_BWD_DX, FMT>(tm, a, g.nmat, st);
+        return false;
     }
-    return true;
+    return false;
 }
 
 }  // namespace tc

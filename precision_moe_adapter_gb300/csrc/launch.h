@@ -47,6 +47,7 @@ struct GemmArgs {
     const uint8_t *ws;       // scales of expert 0
     int64_t wq_stride, ws_stride;  // bytes between experts (or slots)
     int64_t Nst, Kst;        // storage shape [Nst, Kst] of one expert's matrix
+    int64_t nmat;            // number of stored matrices (experts, or scratch slots)
     int64_t w_off_elems;     // element offset of the matrix inside a scratch slot
     const uint16_t *A;       // activations [P, K] bf16, expert-sorted rows
     int K;                   // contraction length
