@@ -35,15 +35,15 @@ static EncodeTiled encoder()
     return fn;
 }
 
-// 2-D BF16 row-major [rows, cols] tensor, box of 32 rows x 64 columns
+// 2-D BF16 row-major [rows, cols] tensor, box of box_rows rows x 64 columns
 // (128 bytes: one swizzle row), 128-byte swizzle, zero fill out of bounds.
-bool make_rows_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t cols)
+bool make_rows_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int box_rows)
 {
     EncodeTiled enc = encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBoxRows};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

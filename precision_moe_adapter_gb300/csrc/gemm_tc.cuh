@@ -35,13 +35,12 @@ constexpr int kM = 128;                      // MMA M (weight rows per tile)
 constexpr int kNmax = 256;                   // tokens per tile (MMA N)
 constexpr int kABytes = kM * kBK * 2;        // 16 KB
 constexpr int kBBytes = kNmax * kBK * 2;     // 32 KB
-constexpr int kBoxRows = 32;                 // TMA box: 32 token rows x 64 K
-constexpr int kBoxBytes = kBoxRows * kBK * 2;
+constexpr int kBoxRows = 32;                 // smallest TMA box: 32 token rows x 64 K
 constexpr int kEpiWarps = 4;
 constexpr int kProdWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kDqWarp0 = 6;
-constexpr int kDqWarps = 8;
+constexpr int kDqWarps = 16;
 constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;
 constexpr int kTmemCols = 512;
 constexpr unsigned long long kWaitNs = 2000000000ull;   // bounded waits: 2 s
@@ -162,6 +161,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v)
 {
@@ -378,27 +390,28 @@ struct Dequant {
     }
 
     // Convert one TMA raw tile (non-transposed kinds) into the A stage.
-    // Thread: A row m = td >> 1, K half = td & 1 (32 elements).
+    // Thread (512 of them): A row m = td >> 2, K quarter qk = td & 3
+    // (16 elements: two 16-byte chunks of the swizzled row).
     __device__ static void convert_tma(const TcArgs &a, int f0, int ks, int td, const uint8_t *rawt,
                                        uint32_t sA)
     {
         using PP = Pipe<KIND, FMT>;
-        const int m = td >> 1, half = td & 1;
+        const int m = td >> 2, qk = td & 3;
         const int rr = raw_row(m);
         const bool lv = KIND == GK_FWD_GU || f0 + m < a.Mtot;
         const uint8_t *row = rawt + rr * PP::kRowBytes;
         const uint32_t sw = *(const uint32_t *)(rawt + 128 * PP::kRowBytes + 4 * rr);
-        uint4 out[4];
+        const int grp = qk >> 1;   // scale group (32 elements) of this quarter
+        uint4 out[2];
         if (!lv) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) out[j] = make_uint4(0, 0, 0, 0);
+            out[0] = out[1] = make_uint4(0, 0, 0, 0);
         } else if (FMT == PMOE_W_INT4_G32_BF16) {
-            const uint4 q = *(const uint4 *)(row + 16 * half);
-            const uint32_t sb = half ? sw >> 16 : sw & 0xFFFFu;
+            const uint2 q = *(const uint2 *)(row + 8 * qk);
+            const uint32_t sb = grp ? sw >> 16 : sw & 0xFFFFu;
             const uint32_t s2 = sb | (sb << 16);
-            const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+            const uint32_t words[2] = {q.x, q.y};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 2; ++j) {
                 uint32_t p[4];
                 int4x8_pairs(words[j], s2, p);
                 out[j].x = prmt(p[0], p[1], 0x5410);
@@ -407,12 +420,12 @@ struct Dequant {
                 out[j].w = prmt(p[2], p[3], 0x7632);
             }
         } else if (FMT == PMOE_W_MXFP4_G32_E8M0) {
-            const uint4 q = *(const uint4 *)(row + 16 * half);
-            const int64_t gi = stored_row(a, f0, rr) * (a.Kst >> 5) + 2 * ks + half;
+            const uint2 q = *(const uint2 *)(row + 8 * qk);
+            const int64_t gi = stored_row(a, f0, rr) * (a.Kst >> 5) + 2 * ks + grp;
             const float sc = e8m0_value((sw >> (8 * (gi & 3))) & 0xFFu);
-            const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+            const uint32_t words[2] = {q.x, q.y};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 2; ++j) {
                 uint32_t w = words[j], o[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
@@ -421,12 +434,11 @@ struct Dequant {
                 out[j] = make_uint4(o[0], o[1], o[2], o[3]);
             }
         } else {
-            const uint4 q0 = *(const uint4 *)(row + 32 * half);
-            const uint4 q1 = *(const uint4 *)(row + 32 * half + 16);
+            const uint4 q = *(const uint4 *)(row + 16 * qk);
             const float sc = __uint_as_float(sw);
-            const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+            const uint32_t words[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 2; ++j) {
                 uint32_t o[4];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -443,8 +455,8 @@ struct Dequant {
         }
         const uint32_t rowaddr = sA + m * 128;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int c = 4 * half + j;
+        for (int j = 0; j < 2; ++j) {
+            const int c = 2 * qk + j;
             st_shared_v4(rowaddr + ((c ^ (m & 7)) << 4), out[j]);
         }
     }
@@ -629,7 +641,10 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.f + expf(-g)); 
 
 // ------------------------------------------------------------------ kernel
 template <int KIND, int FMT>
-__global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__ CUtensorMap tmB,
+__global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__ CUtensorMap tmB256,
+                                                         const __grid_constant__ CUtensorMap tmB128,
+                                                         const __grid_constant__ CUtensorMap tmB64,
+                                                         const __grid_constant__ CUtensorMap tmB32,
                                                          const __grid_constant__ CUtensorMap tmA,
                                                          const TcArgs a)
 {
@@ -693,7 +708,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
         bool ok = true;
         for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
             const Tile tl = a.tiles[tbeg + item / nft];
-            const int nbox = (tl.nrows + kBoxRows - 1) / kBoxRows;
+            // token rows covered: round up to 32, in boxes of 256/128/64/32 rows
+            const int brows = (tl.nrows + kBoxRows - 1) & ~(kBoxRows - 1);
             const int f0 = (item % nft) * a.m_tile;
             const int64_t widx = a.slot_index ? (tl.chunk & 0xffff) : tl.expert;
             for (int ks = 0; ks < nk; ++ks, ++g) {
@@ -728,10 +744,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                 const uint32_t ph = (g / kStages) & 1;
                 if (!(ok = mbar_wait(empty(s), ph ^ 1, a.err, 1))) break;
                 if (lane == 0) {
-                    mbar_expect_tx(full_b(s), nbox * kBoxBytes);
-                    for (int bx = 0; bx < nbox; ++bx)
-                        tma_load_2d(sB0 + s * kBBytes + bx * kBoxBytes, &tmB, ks * kBK,
-                                    tl.row0 + bx * kBoxRows, full_b(s));
+                    mbar_expect_tx(full_b(s), brows * kBK * 2);
+                    for (int r0 = 0; r0 < brows;) {
+                        const int left = brows - r0;
+                        const CUtensorMap *tm = left >= 256 ? &tmB256 : left >= 128 ? &tmB128
+                                              : left >= 64 ? &tmB64 : &tmB32;
+                        const int rows = left >= 256 ? 256 : left >= 128 ? 128 : left >= 64 ? 64 : 32;
+                        tma_load_2d(sB0 + s * kBBytes + r0 * kBK * 2, tm, ks * kBK, tl.row0 + r0, full_b(s));
+                        r0 += rows;
+                    }
                     if constexpr (PP::kBf16) {
                         mbar_expect_tx(full_a(s), kABytes);
                         const int slot = (int)widx;
@@ -804,6 +825,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                 if (!ok) break;
             }
         } else if constexpr (PP::kTrans) {
+            // transposed kinds: the first 256 converter threads convert, the
+            // other warps only take part in the stage handshake
+            const bool worker = td < 256;
         // ---------------- dequant producers: packed weights prefetched
         // kRawStages - 1 steps ahead with cp.async, converted into the A stage
         uint8_t *raw = smem + PP::kRawOff;
@@ -828,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
         };
         Ctx cur, ahead;
         auto issue_step = [&](uint32_t j) {
-            if (j < total) {
+            if (worker && j < total) {
                 load_ctx(ahead, (int)(j / nk));
                 Dequant<KIND, FMT>::issue(a, ahead.wq, ahead.ws, ahead.f0, (int)(j % nk), td,
                                           raw_a + (j % kRing) * kRingStride);
@@ -843,8 +867,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             const int s = g % kStages;
             const uint32_t ph = (g / kStages) & 1;
             if (!mbar_wait(empty(s), ph ^ 1, a.err, 5)) break;
-            Dequant<KIND, FMT>::convert(a, cur.f0, (int)(g % nk), td, raw + (g % kRing) * kRingStride,
-                                        sA0 + s * kABytes);
+            if (worker)
+                Dequant<KIND, FMT>::convert(a, cur.f0, (int)(g % nk), td,
+                                            raw + (g % kRing) * kRingStride, sA0 + s * kABytes);
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) mbar_arrive(full_a(s));
@@ -862,16 +887,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             if (!mbar_wait(tfull(acc), (li >> 1) & 1, a.err, 6)) break;
             tc_fence_after();
             const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + acc * (kTmemCols / 2);
-            const int ncols = (tl.nrows + 31) & ~31;
-            for (int c0 = 0; c0 < ncols; c0 += 32) {
-                float v[32];
-                tmem_ld32(taddr + c0, v);
+            const int ncols = (tl.nrows + 15) & ~15;
+            for (int c0 = 0; c0 < ncols; c0 += 16) {
+                float v[16];
+                tmem_ld16(taddr + c0, v);
                 if (KIND == GK_FWD_GU) {
                     // lanes 0-15 gate, 16-31 up of features f0 + 16q + (lane & 15)
                     const int f = f0 + 16 * q + (lane & 15);
                     const bool up = lane >= 16;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
+                    for (int j = 0; j < 16; j += 2) {
                         const float send = up ? v[j] : v[j + 1];
                         const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
                         const float g = up ? recv : v[j];
@@ -892,20 +917,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                 } else if (KIND == GK_BWD_G) {
                     const int f = f0 + 32 * q + lane;
                     const bool fl = f < a.Mtot;
-                    const int ncol = min(32, tl.nrows - c0);
+                    const int ncol = min(16, tl.nrows - c0);
                     // routing weight of column `lane` (one load per lane, then broadcast)
                     const float w_lane = lane < ncol ? a.w[a.perm[tl.row0 + c0 + lane]] : 0.f;
 #pragma unroll
-                    for (int hh = 0; hh < 32; hh += 16) {
-                        uint16_t hts[16];   // h~ of the 16 columns, loaded together
+                    for (int j8 = 0; j8 < 16; j8 += 8) {
+                        uint16_t hts[8];   // h~ of 8 columns, loaded together
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            hts[j] = (fl && hh + j < ncol)
-                                         ? a.ht[(int64_t)(tl.row0 + c0 + hh + j) * a.Mtot + f]
+                        for (int j = 0; j < 8; ++j)
+                            hts[j] = (fl && j8 + j < ncol)
+                                         ? a.ht[(int64_t)(tl.row0 + c0 + j8 + j) * a.Mtot + f]
                                          : 0;
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int jj = hh + j;
+                        for (int j = 0; j < 8; ++j) {
+                            const int jj = j8 + j;
                             const float wr = __shfl_sync(0xffffffffu, w_lane, jj);
                             const int64_t r = tl.row0 + c0 + jj;
                             float part = fl ? v[jj] * bf2f(hts[j]) : 0.f;
@@ -920,7 +945,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                     const int f = f0 + 32 * q + lane;
                     if (f < a.Mtot) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
+                        for (int j = 0; j < 16; ++j) {
                             const int col = c0 + j;
                             if (col < tl.nrows) a.out[(int64_t)(tl.row0 + col) * a.Mtot + f] = f2bf(v[j]);
                         }

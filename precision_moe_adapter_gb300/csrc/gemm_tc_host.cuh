@@ -9,7 +9,7 @@
 namespace pmoe {
 namespace tc {
 
-bool make_rows_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t cols);
+bool make_rows_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int box_rows);
 // uint8 [rows, row_bytes] tensor, box of box_rows x box_bytes, no swizzle
 bool make_bytes_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t row_bytes,
                      int box_bytes, int box_rows);
@@ -19,7 +19,7 @@ bool make_slots_tmap(CUtensorMap *m, const void *base, int64_t slots, int64_t ro
 int num_sms();
 
 template <int KIND, int FMT>
-bool launch_kind(const CUtensorMap &tm, const TcArgs &a, int64_t nmat, cudaStream_t st)
+bool launch_kind(const CUtensorMap (&tmB)[4], const TcArgs &a, int64_t nmat, cudaStream_t st)
 {
     using PP = Pipe<KIND, FMT>;
     static bool attr = false;
@@ -41,7 +41,7 @@ bool launch_kind(const CUtensorMap &tm, const TcArgs &a, int64_t nmat, cudaStrea
                              KIND == GK_FWD_GU ? 16 : 128))
             return false;
     }
-    k_gemm_tc<KIND, FMT><<<num_sms(), kThreads, PP::kSmem, st>>>(tm, tmA, a);
+    k_gemm_tc<KIND, FMT><<<num_sms(), kThreads, PP::kSmem, st>>>(tmB[0], tmB[1], tmB[2], tmB[3], tmA, a);
     note_launch();
     return true;
 }
@@ -50,8 +50,9 @@ template <int FMT>
 bool launch_fmt(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st)
 {
     if (P <= 0) return true;
-    CUtensorMap tm;
-    if (!make_rows_tmap(&tm, g.A, P, g.K)) return false;
+    CUtensorMap tm[4];   // token tiles in boxes of 256, 128, 64 and 32 rows
+    for (int i = 0; i < 4; ++i)
+        if (!make_rows_tmap(&tm[i], g.A, P, g.K, 256 >> i)) return false;
     TcArgs a{};
     a.wq = g.wq;
     a.ws = g.ws;
