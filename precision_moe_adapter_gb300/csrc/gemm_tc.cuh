@@ -280,8 +280,7 @@ struct Pipe {
     static constexpr int kStagesAB = kFp8 ? 3 : 4;
     static constexpr int kRowBytes = kFp8 ? 64 : 32;
     static constexpr int kRawTile = 128 * kRowBytes + 128 * 4;
-    static constexpr int kRawTma = 6;      // raw ring stages
-    static constexpr int kRawAhead = 3;    // raw tiles issued this many steps before the token tile
+    static constexpr int kRawTma = 4;
     static constexpr int kRawStages = 4;
     static constexpr int kSlot = kFp8 ? 48 : 32;
     static constexpr int kRawBytes =
@@ -391,28 +390,28 @@ struct Dequant {
     }
 
     // Convert one TMA raw tile (non-transposed kinds) into the A stage.
-    // Thread (256 of a converter group): A row m = td >> 1, K half = td & 1
-    // (32 elements: four 16-byte chunks of the swizzled row).
+    // Thread (512 of them): A row m = td >> 2, K quarter qk = td & 3
+    // (16 elements: two 16-byte chunks of the swizzled row).
     __device__ static void convert_tma(const TcArgs &a, int f0, int ks, int td, const uint8_t *rawt,
                                        uint32_t sA)
     {
         using PP = Pipe<KIND, FMT>;
-        const int m = td >> 1, half = td & 1;
+        const int m = td >> 2, qk = td & 3;
         const int rr = raw_row(m);
         const bool lv = KIND == GK_FWD_GU || f0 + m < a.Mtot;
         const uint8_t *row = rawt + rr * PP::kRowBytes;
         const uint32_t sw = *(const uint32_t *)(rawt + 128 * PP::kRowBytes + 4 * rr);
-        uint4 out[4];
+        const int grp = qk >> 1;   // scale group (32 elements) of this quarter
+        uint4 out[2];
         if (!lv) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) out[j] = make_uint4(0, 0, 0, 0);
+            out[0] = out[1] = make_uint4(0, 0, 0, 0);
         } else if (FMT == PMOE_W_INT4_G32_BF16) {
-            const uint4 q = *(const uint4 *)(row + 16 * half);
-            const uint32_t sb = half ? sw >> 16 : sw & 0xFFFFu;
+            const uint2 q = *(const uint2 *)(row + 8 * qk);
+            const uint32_t sb = grp ? sw >> 16 : sw & 0xFFFFu;
             const uint32_t s2 = sb | (sb << 16);
-            const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+            const uint32_t words[2] = {q.x, q.y};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 2; ++j) {
                 uint32_t p[4];
                 int4x8_pairs(words[j], s2, p);
                 out[j].x = prmt(p[0], p[1], 0x5410);
@@ -421,12 +420,12 @@ struct Dequant {
                 out[j].w = prmt(p[2], p[3], 0x7632);
             }
         } else if (FMT == PMOE_W_MXFP4_G32_E8M0) {
-            const uint4 q = *(const uint4 *)(row + 16 * half);
-            const int64_t gi = stored_row(a, f0, rr) * (a.Kst >> 5) + 2 * ks + half;
+            const uint2 q = *(const uint2 *)(row + 8 * qk);
+            const int64_t gi = stored_row(a, f0, rr) * (a.Kst >> 5) + 2 * ks + grp;
             const float sc = e8m0_value((sw >> (8 * (gi & 3))) & 0xFFu);
-            const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+            const uint32_t words[2] = {q.x, q.y};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 2; ++j) {
                 uint32_t w = words[j], o[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
@@ -435,12 +434,11 @@ struct Dequant {
                 out[j] = make_uint4(o[0], o[1], o[2], o[3]);
             }
         } else {
-            const uint4 q0 = *(const uint4 *)(row + 32 * half);
-            const uint4 q1 = *(const uint4 *)(row + 32 * half + 16);
+            const uint4 q = *(const uint4 *)(row + 16 * qk);
             const float sc = __uint_as_float(sw);
-            const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+            const uint32_t words[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 2; ++j) {
                 uint32_t o[4];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -457,8 +455,8 @@ struct Dequant {
         }
         const uint32_t rowaddr = sA + m * 128;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int c = 4 * half + j;
+        for (int j = 0; j < 2; ++j) {
+            const int c = 2 * qk + j;
             st_shared_v4(rowaddr + ((c ^ (m & 7)) << 4), out[j]);
         }
     }
@@ -675,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(full_a(s), PP::kBf16 ? 1 : PP::kTmaRaw ? kDqWarps / 2 : kDqWarps);
+            mbar_init(full_a(s), PP::kBf16 ? 1 : kDqWarps);
             mbar_init(full_b(s), 1);
             mbar_init(empty(s), 1);
         }
@@ -685,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
         }
         for (int r = 0; r < PP::kRawTma; ++r) {
             mbar_init(raw_full(r), 1 + 32);   // TMA transaction + the 32 lanes' scale copies
-            mbar_init(raw_empty(r), kDqWarps / 2);
+            mbar_init(raw_empty(r), kDqWarps);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
@@ -703,46 +701,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     const uint32_t tmem = *(volatile uint32_t *)tmem_slot;
 
     if (warp == kProdWarp) {
-        // ---------------- producer: packed weight tiles (TMA) with their scale
-        // words (cp.async by the 32 lanes) run kRawAhead steps ahead of the
-        // token tiles (TMA); BF16 scratch weights go by TMA straight into the
-        // swizzled A stage with the token tile
-        const int my_items = n_items > (int)blockIdx.x ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-        const uint32_t total = (uint32_t)my_items * nk;
-        uint32_t graw = 0;
-        bool ok = true;
-        // issue the raw tile of flat step j
-        auto issue_raw = [&](uint32_t j) -> bool {
-            const int item = (int)blockIdx.x + (int)(j / nk) * (int)gridDim.x;
-            const int ks = (int)(j % nk);
-            const Tile tl = a.tiles[tbeg + item / nft];
-            const int f0 = (item % nft) * a.m_tile;
-            const int64_t widx = a.slot_index ? (tl.chunk & 0xffff) : tl.expert;
-            const int r = j % PP::kRawTma;
-            if (!mbar_wait(raw_empty(r), ((j / PP::kRawTma) & 1) ^ 1, a.err, 7)) return false;
-            const uint32_t dst = raw0 + r * PP::kRawTile;
-            if (lane == 0) {
-                mbar_expect_tx(raw_full(r), 128 * PP::kRowBytes);
-                const int x = ks * PP::kRowBytes;
-                const int y = (int)(widx * a.Nst) + f0;
-                tma_load_2d(dst, &tmA, x, y, raw_full(r));
-                if (KIND == GK_FWD_GU)
-                    tma_load_2d(dst + 64 * PP::kRowBytes, &tmA, x, y + a.I, raw_full(r));
-            }
-            const uint8_t *ws = a.ws + widx * a.ws_stride;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int rr = lane + 32 * i;
-                const bool lv = KIND == GK_FWD_GU || f0 + rr < a.Mtot;
-                if (lv)
-                    cpa4(dst + 128 * PP::kRowBytes + 4 * rr,
-                         ws + Dequant<KIND, FMT>::scale_word(a, Dequant<KIND, FMT>::stored_row(a, f0, rr),
-                                                             ks));
-            }
-            cpa_mbar_arrive(raw_full(r));
-            return true;
-        };
+        // ---------------- producer: token tiles (TMA), packed weight tiles
+        // (TMA) with their scale words (cp.async by the 32 lanes), or BF16
+        // weight tiles (TMA into the swizzled A stage)
         uint32_t g = 0;
+        bool ok = true;
         for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
             const Tile tl = a.tiles[tbeg + item / nft];
             // token rows covered: round up to 32, in boxes of 256/128/64/32 rows
@@ -751,8 +714,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             const int64_t widx = a.slot_index ? (tl.chunk & 0xffff) : tl.expert;
             for (int ks = 0; ks < nk; ++ks, ++g) {
                 if constexpr (PP::kTmaRaw) {
-                    while (ok && graw < total && graw <= g + PP::kRawAhead) ok = issue_raw(graw++);
-                    if (!ok) break;
+                    const int r = g % PP::kRawTma;
+                    if (!(ok = mbar_wait(raw_empty(r), ((g / PP::kRawTma) & 1) ^ 1, a.err, 7))) break;
+                    const uint32_t dst = raw0 + r * PP::kRawTile;
+                    if (lane == 0) {
+                        mbar_expect_tx(raw_full(r), 128 * PP::kRowBytes);
+                        const int x = ks * PP::kRowBytes;
+                        const int y = (int)(widx * a.Nst) + f0;
+                        if (KIND == GK_FWD_GU) {
+                            tma_load_2d(dst, &tmA, x, y, raw_full(r));
+                            tma_load_2d(dst + 64 * PP::kRowBytes, &tmA, x, y + a.I, raw_full(r));
+                        } else {
+                            tma_load_2d(dst, &tmA, x, y, raw_full(r));
+                        }
+                    }
+                    const uint8_t *ws = a.ws + widx * a.ws_stride;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int rr = lane + 32 * i;
+                        const bool lv = KIND == GK_FWD_GU || f0 + rr < a.Mtot;
+                        if (lv)
+                            cpa4(dst + 128 * PP::kRowBytes + 4 * rr,
+                                 ws + Dequant<KIND, FMT>::scale_word(
+                                          a, Dequant<KIND, FMT>::stored_row(a, f0, rr), ks));
+                    }
+                    cpa_mbar_arrive(raw_full(r));
                 }
                 const int s = g % kStages;
                 const uint32_t ph = (g / kStages) & 1;
@@ -817,29 +803,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     } else if (warp >= kDqWarp0) {
         const int td = threadIdx.x - kDqWarp0 * 32;
         if constexpr (PP::kTmaRaw) {
-            // ---------------- converters: TMA raw tile -> BF16 A stage.  Two
-            // groups of kDqWarps/2 warps take alternate steps, so each group has
-            // two MMA steps for the latency of one stage (load, convert,
-            // store, proxy fence).
-            const int grp = td >> 8, tg = td & 255;
-            const int my_items = n_items > (int)blockIdx.x ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-            const uint32_t total = (uint32_t)my_items * nk;
-            for (uint32_t g = grp; g < total; g += 2) {
-                const int item = (int)blockIdx.x + (int)(g / nk) * (int)gridDim.x;
-                const int ks = (int)(g % nk);
+            // ---------------- converters: TMA raw tile -> BF16 A stage
+            uint32_t g = 0;
+            for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
                 const int f0 = (item % nft) * a.m_tile;
-                const int s = g % kStages;
-                const int r = g % PP::kRawTma;
-                if (!mbar_wait(empty(s), ((g / kStages) & 1) ^ 1, a.err, 5)) break;
-                if (!mbar_wait(raw_full(r), (g / PP::kRawTma) & 1, a.err, 8)) break;
-                Dequant<KIND, FMT>::convert_tma(a, f0, ks, tg, smem + PP::kRawOff + r * PP::kRawTile,
-                                                sA0 + s * kABytes);
-                fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(raw_empty(r));
-                    mbar_arrive(full_a(s));
+                bool ok = true;
+                for (int ks = 0; ks < nk; ++ks, ++g) {
+                    const int s = g % kStages;
+                    const int r = g % PP::kRawTma;
+                    if (!(ok = mbar_wait(empty(s), ((g / kStages) & 1) ^ 1, a.err, 5))) break;
+                    if (!(ok = mbar_wait(raw_full(r), (g / PP::kRawTma) & 1, a.err, 8))) break;
+                    Dequant<KIND, FMT>::convert_tma(a, f0, ks, td, smem + PP::kRawOff + r * PP::kRawTile,
+                                                    sA0 + s * kABytes);
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(raw_empty(r));
+                        mbar_arrive(full_a(s));
+                    }
                 }
+                if (!ok) break;
             }
         } else if constexpr (PP::kTrans) {
             // transposed kinds: the first 256 converter threads convert, the
