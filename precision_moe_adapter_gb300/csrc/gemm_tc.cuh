@@ -280,7 +280,8 @@ struct Pipe {
     static constexpr int kStagesAB = kFp8 ? 3 : 4;
     static constexpr int kRowBytes = kFp8 ? 64 : 32;
     static constexpr int kRawTile = 128 * kRowBytes + 128 * 4;
-    static constexpr int kRawTma = 4;
+    static constexpr int kRawTma = 6;      // raw ring stages
+    static constexpr int kRawAhead = 2;    // raw tiles issued this many steps before the token tile
     static constexpr int kRawStages = 4;
     static constexpr int kSlot = kFp8 ? 48 : 32;
     static constexpr int kRawBytes =
@@ -389,11 +390,12 @@ struct Dequant {
         return 4 * ((row >> 7) * (a.Kst >> 7) + ((int64_t)ks * kBK >> 7));
     }
 
-    // Convert one TMA raw tile (non-transposed kinds) into the A stage.
+    // Convert one TMA raw tile (non-transposed kinds) for the A stage.
     // Thread (512 of them): A row m = td >> 2, K quarter qk = td & 3
-    // (16 elements: two 16-byte chunks of the swizzled row).
-    __device__ static void convert_tma(const TcArgs &a, int f0, int ks, int td, const uint8_t *rawt,
-                                       uint32_t sA)
+    // (16 elements: two 16-byte chunks of the swizzled row).  The converted
+    // chunks stay in registers; store_tma() writes them.
+    __device__ static void compute_tma(const TcArgs &a, int f0, int ks, int td, const uint8_t *rawt,
+                                       uint4 (&out)[2])
     {
         using PP = Pipe<KIND, FMT>;
         const int m = td >> 2, qk = td & 3;
@@ -402,7 +404,6 @@ struct Dequant {
         const uint8_t *row = rawt + rr * PP::kRowBytes;
         const uint32_t sw = *(const uint32_t *)(rawt + 128 * PP::kRowBytes + 4 * rr);
         const int grp = qk >> 1;   // scale group (32 elements) of this quarter
-        uint4 out[2];
         if (!lv) {
             out[0] = out[1] = make_uint4(0, 0, 0, 0);
         } else if (FMT == PMOE_W_INT4_G32_BF16) {
@@ -453,6 +454,10 @@ struct Dequant {
                 out[j] = make_uint4(o[0], o[1], o[2], o[3]);
             }
         }
+    }
+    __device__ static void store_tma(int td, const uint4 (&out)[2], uint32_t sA)
+    {
+        const int m = td >> 2, qk = td & 3;
         const uint32_t rowaddr = sA + m * 128;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -701,11 +706,46 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     const uint32_t tmem = *(volatile uint32_t *)tmem_slot;
 
     if (warp == kProdWarp) {
-        // ---------------- producer: token tiles (TMA), packed weight tiles
-        // (TMA) with their scale words (cp.async by the 32 lanes), or BF16
-        // weight tiles (TMA into the swizzled A stage)
-        uint32_t g = 0;
+        // ---------------- producer: packed weight tiles (TMA) with their scale
+        // words (cp.async by the 32 lanes) run kRawAhead steps ahead of the
+        // token tiles (TMA); BF16 scratch weights go by TMA straight into the
+        // swizzled A stage with the token tile
+        const int my_items = n_items > (int)blockIdx.x ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+        const uint32_t total = (uint32_t)my_items * nk;
+        uint32_t graw = 0;
         bool ok = true;
+        // issue the raw tile of flat step j
+        auto issue_raw = [&](uint32_t j) -> bool {
+            const int item = (int)blockIdx.x + (int)(j / nk) * (int)gridDim.x;
+            const int ks = (int)(j % nk);
+            const Tile tl = a.tiles[tbeg + item / nft];
+            const int f0 = (item % nft) * a.m_tile;
+            const int64_t widx = a.slot_index ? (tl.chunk & 0xffff) : tl.expert;
+            const int r = j % PP::kRawTma;
+            if (!mbar_wait(raw_empty(r), ((j / PP::kRawTma) & 1) ^ 1, a.err, 7)) return false;
+            const uint32_t dst = raw0 + r * PP::kRawTile;
+            if (lane == 0) {
+                mbar_expect_tx(raw_full(r), 128 * PP::kRowBytes);
+                const int x = ks * PP::kRowBytes;
+                const int y = (int)(widx * a.Nst) + f0;
+                tma_load_2d(dst, &tmA, x, y, raw_full(r));
+                if (KIND == GK_FWD_GU)
+                    tma_load_2d(dst + 64 * PP::kRowBytes, &tmA, x, y + a.I, raw_full(r));
+            }
+            const uint8_t *ws = a.ws + widx * a.ws_stride;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int rr = lane + 32 * i;
+                const bool lv = KIND == GK_FWD_GU || f0 + rr < a.Mtot;
+                if (lv)
+                    cpa4(dst + 128 * PP::kRowBytes + 4 * rr,
+                         ws + Dequant<KIND, FMT>::scale_word(a, Dequant<KIND, FMT>::stored_row(a, f0, rr),
+                                                             ks));
+            }
+            cpa_mbar_arrive(raw_full(r));
+            return true;
+        };
+        uint32_t g = 0;
         for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
             const Tile tl = a.tiles[tbeg + item / nft];
             // token rows covered: round up to 32, in boxes of 256/128/64/32 rows
@@ -714,31 +754,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             const int64_t widx = a.slot_index ? (tl.chunk & 0xffff) : tl.expert;
             for (int ks = 0; ks < nk; ++ks, ++g) {
                 if constexpr (PP::kTmaRaw) {
-                    const int r = g % PP::kRawTma;
-                    if (!(ok = mbar_wait(raw_empty(r), ((g / PP::kRawTma) & 1) ^ 1, a.err, 7))) break;
-                    const uint32_t dst = raw0 + r * PP::kRawTile;
-                    if (lane == 0) {
-                        mbar_expect_tx(raw_full(r), 128 * PP::kRowBytes);
-                        const int x = ks * PP::kRowBytes;
-                        const int y = (int)(widx * a.Nst) + f0;
-                        if (KIND == GK_FWD_GU) {
-                            tma_load_2d(dst, &tmA, x, y, raw_full(r));
-                            tma_load_2d(dst + 64 * PP::kRowBytes, &tmA, x, y + a.I, raw_full(r));
-                        } else {
-                            tma_load_2d(dst, &tmA, x, y, raw_full(r));
-                        }
-                    }
-                    const uint8_t *ws = a.ws + widx * a.ws_stride;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int rr = lane + 32 * i;
-                        const bool lv = KIND == GK_FWD_GU || f0 + rr < a.Mtot;
-                        if (lv)
-                            cpa4(dst + 128 * PP::kRowBytes + 4 * rr,
-                                 ws + Dequant<KIND, FMT>::scale_word(
-                                          a, Dequant<KIND, FMT>::stored_row(a, f0, rr), ks));
-                    }
-                    cpa_mbar_arrive(raw_full(r));
+                    while (ok && graw < total && graw <= g + PP::kRawAhead) ok = issue_raw(graw++);
+                    if (!ok) break;
                 }
                 const int s = g % kStages;
                 const uint32_t ph = (g / kStages) & 1;
@@ -803,26 +820,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     } else if (warp >= kDqWarp0) {
         const int td = threadIdx.x - kDqWarp0 * 32;
         if constexpr (PP::kTmaRaw) {
-            // ---------------- converters: TMA raw tile -> BF16 A stage
-            uint32_t g = 0;
-            for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-                const int f0 = (item % nft) * a.m_tile;
-                bool ok = true;
-                for (int ks = 0; ks < nk; ++ks, ++g) {
-                    const int s = g % kStages;
-                    const int r = g % PP::kRawTma;
-                    if (!(ok = mbar_wait(empty(s), ((g / kStages) & 1) ^ 1, a.err, 5))) break;
-                    if (!(ok = mbar_wait(raw_full(r), (g / PP::kRawTma) & 1, a.err, 8))) break;
-                    Dequant<KIND, FMT>::convert_tma(a, f0, ks, td, smem + PP::kRawOff + r * PP::kRawTile,
-                                                    sA0 + s * kABytes);
-                    fence_proxy_async();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(raw_empty(r));
-                        mbar_arrive(full_a(s));
-                    }
-                }
-                if (!ok) break;
+            // ---------------- converters: TMA raw tile -> BF16 A stage,
+            // software-pipelined: step g+1 is converted in registers while the
+            // shared-memory stores of step g drain, then g is fenced and signalled
+            const int my_items = n_items > (int)blockIdx.x ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+            const uint32_t total = (uint32_t)my_items * nk;
+            auto compute = [&](uint32_t j, uint4 (&o)[2]) -> bool {
+                const int item = (int)blockIdx.x + (int)(j / nk) * (int)gridDim.x;
+                const int r = j % PP::kRawTma;
+                if (!mbar_wait(raw_full(r), (j / PP::kRawTma) & 1, a.err, 8)) return false;
+                Dequant<KIND, FMT>::compute_tma(a, (item % nft) * a.m_tile, (int)(j % nk), td,
+                                                smem + PP::kRawOff + r * PP::kRawTile, o);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(raw_empty(r));
+                return true;
+            };
+            uint4 cur[2], nxt[2];
+            bool ok = total == 0 || compute(0, cur);
+            for (uint32_t g = 0; ok && g < total; ++g) {
+                const int s = g % kStages;
+                if (!mbar_wait(empty(s), ((g / kStages) & 1) ^ 1, a.err, 5)) break;
+                Dequant<KIND, FMT>::store_tma(td, cur, sA0 + s * kABytes);
+                if (g + 1 < total) ok = compute(g + 1, nxt);
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full_a(s));
+                cur[0] = nxt[0];
+                cur[1] = nxt[1];
             }
         } else if constexpr (PP::kTrans) {
             // transposed kinds: the first 256 converter threads convert, the
