@@ -94,17 +94,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, DevErr 
         }
     }
 }
-// Warp-level bounded wait: lane 0 alone polls the barrier (so a warp adds one
-// poller, not 32), the outcome is broadcast and __syncwarp orders the other
-// lanes after lane 0's acquire.  All lanes of the warp must call it.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, DevErr *err, int where)
-{
-    int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, err, where) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
-}
 __device__ __forceinline__ void fence_proxy_async()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -291,7 +280,8 @@ struct Pipe {
     static constexpr int kStagesAB = kFp8 ? 3 : 4;
     static constexpr int kRowBytes = kFp8 ? 64 : 32;
     static constexpr int kRawTile = 128 * kRowBytes + 128 * 4;
-    static constexpr int kRawTma = 4;      // raw ring stages
+    static constexpr int kRawTma = 6;      // raw ring stages
+    static constexpr int kRawAhead = 2;    // raw tiles issued this many steps before the token tile
     static constexpr int kRawStages = 4;
     static constexpr int kSlot = kFp8 ? 48 : 32;
     static constexpr int kRawBytes =
@@ -716,11 +706,46 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     const uint32_t tmem = *(volatile uint32_t *)tmem_slot;
 
     if (warp == kProdWarp) {
-        // ---------------- producer: token tiles (TMA), packed weight tiles
-        // (TMA) with their scale words (cp.async by the 32 lanes), or BF16
-        // weight tiles (TMA into the swizzled A stage)
-        uint32_t g = 0;
+        // ---------------- producer: packed weight tiles (TMA) with their scale
+        // words (cp.async by the 32 lanes) run kRawAhead steps ahead of the
+        // token tiles (TMA); BF16 scratch weights go by TMA straight into the
+        // swizzled A stage with the token tile
+        const int my_items = n_items > (int)blockIdx.x ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+        const uint32_t total = (uint32_t)my_items * nk;
+        uint32_t graw = 0;
         bool ok = true;
+        // issue the raw tile of flat step j
+        auto issue_raw = [&](uint32_t j) -> bool {
+            const int item = (int)blockIdx.x + (int)(j / nk) * (int)gridDim.x;
+            const int ks = (int)(j % nk);
+            const Tile tl = a.tiles[tbeg + item / nft];
+            const int f0 = (item % nft) * a.m_tile;
+            const int64_t widx = a.slot_index ? (tl.chunk & 0xffff) : tl.expert;
+            const int r = j % PP::kRawTma;
+            if (!mbar_wait(raw_empty(r), ((j / PP::kRawTma) & 1) ^ 1, a.err, 7)) return false;
+            const uint32_t dst = raw0 + r * PP::kRawTile;
+            if (lane == 0) {
+                mbar_expect_tx(raw_full(r), 128 * PP::kRowBytes);
+                const int x = ks * PP::kRowBytes;
+                const int y = (int)(widx * a.Nst) + f0;
+                tma_load_2d(dst, &tmA, x, y, raw_full(r));
+                if (KIND == GK_FWD_GU)
+                    tma_load_2d(dst + 64 * PP::kRowBytes, &tmA, x, y + a.I, raw_full(r));
+            }
+            const uint8_t *ws = a.ws + widx * a.ws_stride;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int rr = lane + 32 * i;
+                const bool lv = KIND == GK_FWD_GU || f0 + rr < a.Mtot;
+                if (lv)
+                    cpa4(dst + 128 * PP::kRowBytes + 4 * rr,
+                         ws + Dequant<KIND, FMT>::scale_word(a, Dequant<KIND, FMT>::stored_row(a, f0, rr),
+                                                             ks));
+            }
+            cpa_mbar_arrive(raw_full(r));
+            return true;
+        };
+        uint32_t g = 0;
         for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
             const Tile tl = a.tiles[tbeg + item / nft];
             // token rows covered: round up to 32, in boxes of 256/128/64/32 rows
@@ -729,35 +754,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             const int64_t widx = a.slot_index ? (tl.chunk & 0xffff) : tl.expert;
             for (int ks = 0; ks < nk; ++ks, ++g) {
                 if constexpr (PP::kTmaRaw) {
-                    const int r = g % PP::kRawTma;
-                    if (!(ok = mbar_wait_warp(raw_empty(r), ((g / PP::kRawTma) & 1) ^ 1, a.err, 7))) break;
-                    const uint32_t dst = raw0 + r * PP::kRawTile;
-                    if (lane == 0) {
-                        mbar_expect_tx(raw_full(r), 128 * PP::kRowBytes);
-                        const int x = ks * PP::kRowBytes;
-                        const int y = (int)(widx * a.Nst) + f0;
-                        if (KIND == GK_FWD_GU) {
-                            tma_load_2d(dst, &tmA, x, y, raw_full(r));
-                            tma_load_2d(dst + 64 * PP::kRowBytes, &tmA, x, y + a.I, raw_full(r));
-                        } else {
-                            tma_load_2d(dst, &tmA, x, y, raw_full(r));
-                        }
-                    }
-                    const uint8_t *ws = a.ws + widx * a.ws_stride;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int rr = lane + 32 * i;
-                        const bool lv = KIND == GK_FWD_GU || f0 + rr < a.Mtot;
-                        if (lv)
-                            cpa4(dst + 128 * PP::kRowBytes + 4 * rr,
-                                 ws + Dequant<KIND, FMT>::scale_word(
-                                          a, Dequant<KIND, FMT>::stored_row(a, f0, rr), ks));
-                    }
-                    cpa_mbar_arrive(raw_full(r));
+                    while (ok && graw < total && graw <= g + PP::kRawAhead) ok = issue_raw(graw++);
+                    if (!ok) break;
                 }
                 const int s = g % kStages;
                 const uint32_t ph = (g / kStages) & 1;
-                if (!(ok = mbar_wait_warp(empty(s), ph ^ 1, a.err, 1))) break;
+                if (!(ok = mbar_wait(empty(s), ph ^ 1, a.err, 1))) break;
                 if (lane == 0) {
                     mbar_expect_tx(full_b(s), brows * kBK * 2);
                     for (int r0 = 0; r0 < brows;) {
@@ -826,7 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             auto compute = [&](uint32_t j, uint4 (&o)[2]) -> bool {
                 const int item = (int)blockIdx.x + (int)(j / nk) * (int)gridDim.x;
                 const int r = j % PP::kRawTma;
-                if (!mbar_wait_warp(raw_full(r), (j / PP::kRawTma) & 1, a.err, 8)) return false;
+                if (!mbar_wait(raw_full(r), (j / PP::kRawTma) & 1, a.err, 8)) return false;
                 Dequant<KIND, FMT>::compute_tma(a, (item % nft) * a.m_tile, (int)(j % nk), td,
                                                 smem + PP::kRawOff + r * PP::kRawTile, o);
                 __syncwarp();
@@ -837,7 +839,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             bool ok = total == 0 || compute(0, cur);
             for (uint32_t g = 0; ok && g < total; ++g) {
                 const int s = g % kStages;
-                if (!mbar_wait_warp(empty(s), ((g / kStages) & 1) ^ 1, a.err, 5)) break;
+                if (!mbar_wait(empty(s), ((g / kStages) & 1) ^ 1, a.err, 5)) break;
                 Dequant<KIND, FMT>::store_tma(td, cur, sA0 + s * kABytes);
                 if (g + 1 < total) ok = compute(g + 1, nxt);
                 fence_proxy_async();
@@ -888,7 +890,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             cpa_wait<kRing - 1>();
             const int s = g % kStages;
             const uint32_t ph = (g / kStages) & 1;
-            if (!mbar_wait_warp(empty(s), ph ^ 1, a.err, 5)) break;
+            if (!mbar_wait(empty(s), ph ^ 1, a.err, 5)) break;
             if (worker)
                 Dequant<KIND, FMT>::convert(a, cur.f0, (int)(g % nk), td,
                                             raw + (g % kRing) * kRingStride, sA0 + s * kABytes);
@@ -906,7 +908,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             const Tile tl = a.tiles[tbeg + item / nft];
             const int f0 = (item % nft) * a.m_tile;
             const int acc = li & 1;
-            if (!mbar_wait_warp(tfull(acc), (li >> 1) & 1, a.err, 6)) break;
+            if (!mbar_wait(tfull(acc), (li >> 1) & 1, a.err, 6)) break;
             tc_fence_after();
             const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + acc * (kTmemCols / 2);
             const int ncols = (tl.nrows + 15) & ~15;
