@@ -280,8 +280,7 @@ struct Pipe {
     static constexpr int kStagesAB = kFp8 ? 3 : 4;
     static constexpr int kRowBytes = kFp8 ? 64 : 32;
     static constexpr int kRawTile = 128 * kRowBytes + 128 * 4;
-    static constexpr int kRawTma = 6;      // raw ring stages
-    static constexpr int kRawAhead = 2;    // raw tiles issued this many steps before the token tile
+    static constexpr int kRawTma = 4;      // raw ring stages
     static constexpr int kRawStages = 4;
     static constexpr int kSlot = kFp8 ? 48 : 32;
     static constexpr int kRawBytes =
@@ -706,46 +705,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     const uint32_t tmem = *(volatile uint32_t *)tmem_slot;
 
     if (warp == kProdWarp) {
-        // ---------------- producer: packed weight tiles (TMA) with their scale
-        // words (cp.async by the 32 lanes) run kRawAhead steps ahead of the
-        // token tiles (TMA); BF16 scratch weights go by TMA straight into the
-        // swizzled A stage with the token tile
-        const int my_items = n_items > (int)blockIdx.x ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-        const uint32_t total = (uint32_t)my_items * nk;
-        uint32_t graw = 0;
-        bool ok = true;
-        // issue the raw tile of flat step j
-        auto issue_raw = [&](uint32_t j) -> bool {
-            const int item = (int)blockIdx.x + (int)(j / nk) * (int)gridDim.x;
-            const int ks = (int)(j % nk);
-            const Tile tl = a.tiles[tbeg + item / nft];
-            const int f0 = (item % nft) * a.m_tile;
-            const int64_t widx = a.slot_index ? (tl.chunk & 0xffff) : tl.expert;
-            const int r = j % PP::kRawTma;
-            if (!mbar_wait(raw_empty(r), ((j / PP::kRawTma) & 1) ^ 1, a.err, 7)) return false;
-            const uint32_t dst = raw0 + r * PP::kRawTile;
-            if (lane == 0) {
-                mbar_expect_tx(raw_full(r), 128 * PP::kRowBytes);
-                const int x = ks * PP::kRowBytes;
-                const int y = (int)(widx * a.Nst) + f0;
-                tma_load_2d(dst, &tmA, x, y, raw_full(r));
-                if (KIND == GK_FWD_GU)
-                    tma_load_2d(dst + 64 * PP::kRowBytes, &tmA, x, y + a.I, raw_full(r));
-            }
-            const uint8_t *ws = a.ws + widx * a.ws_stride;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int rr = lane + 32 * i;
-                const bool lv = KIND == GK_FWD_GU || f0 + rr < a.Mtot;
-                if (lv)
-                    cpa4(dst + 128 * PP::kRowBytes + 4 * rr,
-                         ws + Dequant<KIND, FMT>::scale_word(a, Dequant<KIND, FMT>::stored_row(a, f0, rr),
-                                                             ks));
-            }
-            cpa_mbar_arrive(raw_full(r));
-            return true;
-        };
+        // ---------------- producer: token tiles (TMA), packed weight tiles
+        // (TMA) with their scale words (cp.async by the 32 lanes), or BF16
+        // weight tiles (TMA into the swizzled A stage)
         uint32_t g = 0;
+        bool ok = true;
         for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
             const Tile tl = a.tiles[tbeg + item / nft];
             // token rows covered: round up to 32, in boxes of 256/128/64/32 rows
@@ -754,8 +718,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             const int64_t widx = a.slot_index ? (tl.chunk & 0xffff) : tl.expert;
             for (int ks = 0; ks < nk; ++ks, ++g) {
                 if constexpr (PP::kTmaRaw) {
-                    while (ok && graw < total && graw <= g + PP::kRawAhead) ok = issue_raw(graw++);
-                    if (!ok) break;
+                    const int r = g % PP::kRawTma;
+                    if (!(ok = mbar_wait(raw_empty(r), ((g / PP::kRawTma) & 1) ^ 1, a.err, 7))) break;
+                    const uint32_t dst = raw0 + r * PP::kRawTile;
+                    if (lane == 0) {
+                        mbar_expect_tx(raw_full(r), 128 * PP::kRowBytes);
+                        const int x = ks * PP::kRowBytes;
+                        const int y = (int)(widx * a.Nst) + f0;
+                        if (KIND == GK_FWD_GU) {
+                            tma_load_2d(dst, &tmA, x, y, raw_full(r));
+                            tma_load_2d(dst + 64 * PP::kRowBytes, &tmA, x, y + a.I, raw_full(r));
+                        } else {
+                            tma_load_2d(dst, &tmA, x, y, raw_full(r));
+                        }
+                    }
+                    const uint8_t *ws = a.ws + widx * a.ws_stride;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int rr = lane + 32 * i;
+                        const bool lv = KIND == GK_FWD_GU || f0 + rr < a.Mtot;
+                        if (lv)
+                            cpa4(dst + 128 * PP::kRowBytes + 4 * rr,
+                                 ws + Dequant<KIND, FMT>::scale_word(
+                                          a, Dequant<KIND, FMT>::stored_row(a, f0, rr), ks));
+                    }
+                    cpa_mbar_arrive(raw_full(r));
                 }
                 const int s = g % kStages;
                 const uint32_t ph = (g / kStages) & 1;
