@@ -41,6 +41,10 @@ constexpr int kProdWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kDqWarp0 = 6;
 constexpr int kDqWarps = 16;
+#ifndef PMOE_CONV_GROUPS
+#define PMOE_CONV_GROUPS 2
+#endif
+constexpr int kConvGroups = PMOE_CONV_GROUPS;   // converter groups taking alternate stages
 constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;
 constexpr int kTmemCols = 512;
 constexpr unsigned long long kWaitNs = 2000000000ull;   // bounded waits: 2 s
@@ -390,59 +394,52 @@ struct Dequant {
     }
 
     // Convert one TMA raw tile (non-transposed kinds) for the A stage.
-    // Thread (512 of them): A row m = td >> 2, K quarter qk = td & 3
-    // (16 elements: two 16-byte chunks of the swizzled row).  The converted
-    // chunks stay in registers; store_tma() writes them.
-    __device__ static void compute_tma(const TcArgs &a, int f0, int ks, int td, const uint8_t *rawt,
-                                       uint4 (&out)[2])
+    // A converter group of 8192 / EPT threads: thread tg takes A row
+    // m = tg / (64 / EPT) and EPT consecutive K elements of it (EPT / 8
+    // 16-byte chunks of the swizzled row).  The converted chunks stay in
+    // registers; store_tma() writes them.
+    template <int EPT>
+    __device__ static void compute_tma(const TcArgs &a, int f0, int ks, int tg, const uint8_t *rawt,
+                                       uint4 (&out)[EPT / 8])
     {
         using PP = Pipe<KIND, FMT>;
-        const int m = td >> 2, qk = td & 3;
+        constexpr int P = 64 / EPT;
+        const int m = tg / P, e0 = (tg % P) * EPT;
         const int rr = raw_row(m);
         const bool lv = KIND == GK_FWD_GU || f0 + m < a.Mtot;
         const uint8_t *row = rawt + rr * PP::kRowBytes;
         const uint32_t sw = *(const uint32_t *)(rawt + 128 * PP::kRowBytes + 4 * rr);
-        const int grp = qk >> 1;   // scale group (32 elements) of this quarter
-        if (!lv) {
-            out[0] = out[1] = make_uint4(0, 0, 0, 0);
-        } else if (FMT == PMOE_W_INT4_G32_BF16) {
-            const uint2 q = *(const uint2 *)(row + 8 * qk);
-            const uint32_t sb = grp ? sw >> 16 : sw & 0xFFFFu;
-            const uint32_t s2 = sb | (sb << 16);
-            const uint32_t words[2] = {q.x, q.y};
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
+        for (int c = 0; c < EPT / 8; ++c) {
+            const int e = e0 + 8 * c, grp = e >> 5;
+            if (!lv) {
+                out[c] = make_uint4(0, 0, 0, 0);
+            } else if (FMT == PMOE_W_INT4_G32_BF16) {
+                const uint32_t w = *(const uint32_t *)(row + (e >> 1));
+                const uint32_t sb = grp ? sw >> 16 : sw & 0xFFFFu;
                 uint32_t p[4];
-                int4x8_pairs(words[j], s2, p);
-                out[j].x = prmt(p[0], p[1], 0x5410);
-                out[j].y = prmt(p[2], p[3], 0x5410);
-                out[j].z = prmt(p[0], p[1], 0x7632);
-                out[j].w = prmt(p[2], p[3], 0x7632);
-            }
-        } else if (FMT == PMOE_W_MXFP4_G32_E8M0) {
-            const uint2 q = *(const uint2 *)(row + 8 * qk);
-            const int64_t gi = stored_row(a, f0, rr) * (a.Kst >> 5) + 2 * ks + grp;
-            const float sc = e8m0_value((sw >> (8 * (gi & 3))) & 0xFFu);
-            const uint32_t words[2] = {q.x, q.y};
+                int4x8_pairs(w, sb | (sb << 16), p);
+                out[c].x = prmt(p[0], p[1], 0x5410);
+                out[c].y = prmt(p[2], p[3], 0x5410);
+                out[c].z = prmt(p[0], p[1], 0x7632);
+                out[c].w = prmt(p[2], p[3], 0x7632);
+            } else if (FMT == PMOE_W_MXFP4_G32_E8M0) {
+                const uint32_t w = *(const uint32_t *)(row + (e >> 1));
+                const int64_t gi = stored_row(a, f0, rr) * (a.Kst >> 5) + 2 * ks + grp;
+                const float sc = e8m0_value((sw >> (8 * (gi & 3))) & 0xFFu);
+                uint32_t o[4];
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                uint32_t w = words[j], o[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    o[e] = pack_bf2(__fmul_rn(e2m1_value((w >> (8 * e)) & 15u), sc),
-                                    __fmul_rn(e2m1_value((w >> (8 * e + 4)) & 15u), sc));
-                out[j] = make_uint4(o[0], o[1], o[2], o[3]);
-            }
-        } else {
-            const uint4 q = *(const uint4 *)(row + 16 * qk);
-            const float sc = __uint_as_float(sw);
-            const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
+                for (int j = 0; j < 4; ++j)
+                    o[j] = pack_bf2(__fmul_rn(e2m1_value((w >> (8 * j)) & 15u), sc),
+                                    __fmul_rn(e2m1_value((w >> (8 * j + 4)) & 15u), sc));
+                out[c] = make_uint4(o[0], o[1], o[2], o[3]);
+            } else {
+                const uint2 w2 = *(const uint2 *)(row + e);
+                const float sc = __uint_as_float(sw);
                 uint32_t o[4];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const uint32_t w = words[2 * j + h];
+                    const uint32_t w = h ? w2.y : w2.x;
                     __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3);
                     __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
                     const float2 fl = __half22float2(*(const __half2 *)&lo);
@@ -450,19 +447,18 @@ struct Dequant {
                     o[2 * h] = pack_bf2(__fmul_rn(fl.x, sc), __fmul_rn(fl.y, sc));
                     o[2 * h + 1] = pack_bf2(__fmul_rn(fh.x, sc), __fmul_rn(fh.y, sc));
                 }
-                out[j] = make_uint4(o[0], o[1], o[2], o[3]);
+                out[c] = make_uint4(o[0], o[1], o[2], o[3]);
             }
         }
     }
-    __device__ static void store_tma(int td, const uint4 (&out)[2], uint32_t sA)
+    template <int EPT>
+    __device__ static void store_tma(int tg, const uint4 (&out)[EPT / 8], uint32_t sA)
     {
-        const int m = td >> 2, qk = td & 3;
+        constexpr int P = 64 / EPT;
+        const int m = tg / P, c0 = (tg % P) * (EPT / 8);
         const uint32_t rowaddr = sA + m * 128;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int c = 2 * qk + j;
-            st_shared_v4(rowaddr + ((c ^ (m & 7)) << 4), out[j]);
-        }
+        for (int j = 0; j < EPT / 8; ++j) st_shared_v4(rowaddr + (((c0 + j) ^ (m & 7)) << 4), out[j]);
     }
 
     // byte offsets of a thread's pieces inside a ring stage (256 threads)
@@ -677,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(full_a(s), PP::kBf16 ? 1 : kDqWarps);
+            mbar_init(full_a(s), PP::kBf16 ? 1 : PP::kTmaRaw ? kDqWarps / kConvGroups : kDqWarps);
             mbar_init(full_b(s), 1);
             mbar_init(empty(s), 1);
         }
@@ -687,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
         }
         for (int r = 0; r < PP::kRawTma; ++r) {
             mbar_init(raw_full(r), 1 + 32);   // TMA transaction + the 32 lanes' scale copies
-            mbar_init(raw_empty(r), kDqWarps);
+            mbar_init(raw_empty(r), kDqWarps / kConvGroups);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
@@ -807,33 +803,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     } else if (warp >= kDqWarp0) {
         const int td = threadIdx.x - kDqWarp0 * 32;
         if constexpr (PP::kTmaRaw) {
-            // ---------------- converters: TMA raw tile -> BF16 A stage,
-            // software-pipelined: step g+1 is converted in registers while the
-            // shared-memory stores of step g drain, then g is fenced and signalled
+            // ---------------- converters: TMA raw tile -> BF16 A stage.  The
+            // converter warps form kConvGroups groups; group G takes the steps
+            // g = G (mod kConvGroups), so several stages are in conversion at
+            // once.  Within a group the loop is software-pipelined: step g+G
+            // is converted in registers while the stores of step g drain.
+            constexpr int kTPG = kDqWarps * 32 / kConvGroups;   // threads per group
+            constexpr int kEPT = 8192 / kTPG;                   // elements per thread
+            const int grp = td / kTPG, tg = td % kTPG;
             const int my_items = n_items > (int)blockIdx.x ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
             const uint32_t total = (uint32_t)my_items * nk;
-            auto compute = [&](uint32_t j, uint4 (&o)[2]) -> bool {
+            auto compute = [&](uint32_t j, uint4 (&o)[kEPT / 8]) -> bool {
                 const int item = (int)blockIdx.x + (int)(j / nk) * (int)gridDim.x;
                 const int r = j % PP::kRawTma;
                 if (!mbar_wait(raw_full(r), (j / PP::kRawTma) & 1, a.err, 8)) return false;
-                Dequant<KIND, FMT>::compute_tma(a, (item % nft) * a.m_tile, (int)(j % nk), td,
-                                                smem + PP::kRawOff + r * PP::kRawTile, o);
+                Dequant<KIND, FMT>::template compute_tma<kEPT>(a, (item % nft) * a.m_tile, (int)(j % nk),
+                                                               tg, smem + PP::kRawOff + r * PP::kRawTile, o);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(raw_empty(r));
                 return true;
             };
-            uint4 cur[2], nxt[2];
-            bool ok = total == 0 || compute(0, cur);
-            for (uint32_t g = 0; ok && g < total; ++g) {
+            uint4 cur[kEPT / 8], nxt[kEPT / 8];
+            bool ok = (uint32_t)grp >= total || compute(grp, cur);
+            for (uint32_t g = grp; ok && g < total; g += kConvGroups) {
                 const int s = g % kStages;
                 if (!mbar_wait(empty(s), ((g / kStages) & 1) ^ 1, a.err, 5)) break;
-                Dequant<KIND, FMT>::store_tma(td, cur, sA0 + s * kABytes);
-                if (g + 1 < total) ok = compute(g + 1, nxt);
+                Dequant<KIND, FMT>::template store_tma<kEPT>(tg, cur, sA0 + s * kABytes);
+                if (g + kConvGroups < total) ok = compute(g + kConvGroups, nxt);
                 fence_proxy_async();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(full_a(s));
-                cur[0] = nxt[0];
-                cur[1] = nxt[1];
+#pragma unroll
+                for (int c = 0; c < kEPT / 8; ++c) cur[c] = nxt[c];
             }
         } else if constexpr (PP::kTrans) {
             // transposed kinds: the first 256 converter threads convert, the
