@@ -9,12 +9,16 @@
 //
 //   D[f, t] = sum_k W~[f, k] * B[t, k]      (FP32 in TMEM: lanes = f, columns = t)
 //
-// Roles (448 threads, one CTA per SM, persistent over the work list):
-//   warps 0-3  epilogue: TMEM -> registers -> fused epilogue -> global
-//   warp  4    TMA producer of the activation tiles B (128B swizzle)
-//   warp  5    TMEM allocator and MMA issuer (one elected thread)
-//   warps 6-13 dequant producers: packed weights -> BF16 A tiles in the
-//              canonical K-major 128B-swizzled layout
+// Roles (704 threads, one CTA per SM, persistent over the work list):
+//   warps 0-3   epilogue: TMEM -> registers -> fused epilogue -> global
+//   warp  4     TMA producer of the packed weight tiles (with their scale
+//               words) and of the activation tiles B (128B swizzle)
+//   warp  5     TMEM allocator and MMA issuer (one elected thread)
+//   warps 6-21  converters: packed weights -> BF16 A tiles, 128B-swizzled.
+//               Forward kinds contract over the stored matrix's columns and
+//               write A K-major; backward kinds contract over its rows and
+//               write A MN-major (each stored row segment lands as one
+//               swizzle row, and the MMA reads the tile transposed).
 // Pipeline: kStages shared-memory stages (A 16 KB + B 32 KB) with full/empty
 // mbarriers; two TMEM accumulators of 256 columns so the epilogue of one
 // tile overlaps the main loop of the next.  Every wait is bounded.
@@ -130,11 +134,24 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr)
     d |= (uint64_t)2 << 61;             // 128-byte swizzle
     return d;
 }
-// Instruction descriptor, kind::f16: BF16 A and B (K-major), FP32 D, M x N.
-__device__ __forceinline__ uint32_t idesc_bf16(int M, int N)
+// MN-major A tile (128 M x 64 K, 128-byte swizzle): the swizzle atom is 64
+// M-elements x 8 K-rows (1024 B); the two M halves sit 1024 B apart (LBO),
+// consecutive 8-row K groups 2048 B apart (SBO).
+__device__ __forceinline__ uint64_t sdesc_mn(uint32_t saddr)
 {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(1024 >> 4) << 16;   // leading byte offset: next 64 M-elements
+    d |= (uint64_t)(2048 >> 4) << 32;   // stride byte offset: next 8 K-rows
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+// Instruction descriptor, kind::f16: BF16 A and B, FP32 D, M x N; B K-major,
+// A K-major or (a_mn) MN-major.
+__device__ __forceinline__ uint32_t idesc_bf16(int M, int N, bool a_mn = false)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                      uint32_t accum)
@@ -262,33 +279,30 @@ struct TcArgs {
     DevErr *err;
 };
 
-template <int KIND>
-struct KindTraits {
-    // transposed: the contraction runs over the stored matrix's rows
-    static constexpr bool kTrans = (KIND == GK_BWD_G || KIND == GK_BWD_DX);
-};
-
 // ------------------------------------------------------------------ pipeline sizes
-// Per kind and weight format.  Non-transposed kinds get their packed weight
-// tile by TMA (raw ring of kRawTma stages: 128 rows of kRowBytes, then 128
-// scale words fetched by the producer warp's lanes with cp.async).  BF16
-// scratch weights come by TMA straight into the swizzled A stage.  The
-// transposed kinds (contraction over the stored rows) prefetch per thread
-// with cp.async (ring of kRawStages steps, kSlot bytes per thread).
+// Per kind and weight format.  Packed weight tiles come by TMA into a raw
+// ring of kRawTma stages, each followed by the tile's scale words, which the
+// producer warp's lanes fetch with cp.async:
+//   forward kinds:  128 stored rows x 64 columns (kRowBytes each), no
+//                   swizzle; one 4-byte scale word per row
+//   backward kinds: 64 stored rows x 128 columns (kRowBytes each), 64- or
+//                   128-byte TMA swizzle (conflict-free converter reads);
+//                   two 4-byte scale words per row
+// BF16 scratch weights come by TMA straight into the swizzled A stage.
 template <int KIND, int FMT>
 struct Pipe {
+    // backward kinds: the contraction runs over the stored matrix's rows
     static constexpr bool kTrans = KIND == GK_BWD_G || KIND == GK_BWD_DX;
     static constexpr bool kBf16 = FMT == kFmtBF16;
-    static constexpr bool kTmaRaw = !kTrans && !kBf16;
+    static constexpr bool kTmaRaw = !kBf16;
     static constexpr bool kFp8 = FMT == PMOE_W_FP8_B128_F32;
     static constexpr int kStagesAB = kFp8 ? 3 : 4;
-    static constexpr int kRowBytes = kFp8 ? 64 : 32;
-    static constexpr int kRawTile = 128 * kRowBytes + 128 * 4;
+    static constexpr int kRawRows = kTrans ? 64 : 128;
+    static constexpr int kRowBytes = kTrans ? (kFp8 ? 128 : 64) : (kFp8 ? 64 : 32);
+    static constexpr int kScaleOff = kRawRows * kRowBytes;   // scale words after the data
+    static constexpr int kRawTile = kTrans ? (kScaleOff + 64 * 8 + 1023) & ~1023 : kScaleOff + 128 * 4;
     static constexpr int kRawTma = 4;      // raw ring stages
-    static constexpr int kRawStages = 4;
-    static constexpr int kSlot = kFp8 ? 48 : 32;
-    static constexpr int kRawBytes =
-        kTmaRaw ? kRawTma * kRawTile : (kTrans ? kRawStages * 256 * kSlot : 0);
+    static constexpr int kRawBytes = kTmaRaw ? kRawTma * kRawTile : 0;
     static constexpr int kNumBars = 3 * kStagesAB + 4 + 2 * kRawTma;
     static constexpr int kBarOff = kStagesAB * (kABytes + kBBytes);
     static constexpr int kBarBytes = 8 * kNumBars + 16;
@@ -330,48 +344,13 @@ __device__ __forceinline__ void cpa_wait()
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// ------------------------------------------------------------------ dequant producers
-// Thread task per stage (256 threads):
-//   non-transposed: smem row m = td >> 1, K half = td & 1 (32 elements)
-//   transposed:     rows m = 8*(td & 15) .. +7, K = 4*(td >> 4) .. +3
-// issue() copies the thread's packed bytes (and the aligned 4-byte word
-// holding its scale) into the ring stage; convert() turns them into BF16 in
-// the A stage.  A ring stage is laid out by piece, not by thread: piece j of
-// thread td sits at j * 256 * size + td * size, so a warp reading its
-// pieces touches consecutive words (no bank conflicts).  Pieces:
-//   4-bit, non-transposed: q (16 B), scale word (4 B)
-//   FP8,   non-transposed: q0, q1 (16 B each), scale (4 B)
-//   BF16 (scratch):        4 x 16 B
-//   4-bit, transposed:     4 q words, 4 scale words (4 B each)
-//   FP8,   transposed:     4 x q (8 B), 4 scales (4 B)
+// ------------------------------------------------------------------ converters
+// The converters turn one raw tile (TMA-fetched packed weights plus scale
+// words) into one BF16 A stage.  compute_*() leaves the converted 16-byte
+// chunks in registers; store_*() writes them, so a converter group can
+// overlap the stores of one stage with the conversion of the next.
 template <int KIND, int FMT>
 struct Dequant {
-    static constexpr bool T = KindTraits<KIND>::kTrans;
-    // storage row of smem row m (non-transposed kinds)
-    __device__ static int64_t row_of(const TcArgs &a, int f0, int m)
-    {
-        if (KIND == GK_FWD_GU) {
-            int q = m >> 5, r = m & 31;
-            return r < 16 ? (int64_t)(f0 + 16 * q + r) : (int64_t)(a.I + f0 + 16 * q + r - 16);
-        }
-        return f0 + m;
-    }
-    __device__ static bool live(const TcArgs &a, int f0, int td)
-    {
-        if (T) return f0 + 8 * (td >> 4) < a.Mtot;
-        return KIND == GK_FWD_GU || f0 + (td >> 1) < a.Mtot;
-    }
-    // byte offset of the aligned 4-byte word holding scale index gi
-    __device__ static int64_t sword(int64_t gi)
-    {
-        return FMT == PMOE_W_INT4_G32_BF16 ? 2 * (gi & ~(int64_t)1) : (gi & ~(int64_t)3);
-    }
-    __device__ static uint32_t spick(uint32_t word, int64_t gi)
-    {
-        if (FMT == PMOE_W_INT4_G32_BF16) return (gi & 1) ? word >> 16 : word & 0xFFFFu;
-        return (word >> (8 * (gi & 3))) & 0xFFu;
-    }
-
     // raw-tile row of A row m: GU tiles hold [gate rows | up rows] (64 each)
     __device__ static int raw_row(int m)
     {
@@ -386,18 +365,66 @@ struct Dequant {
         return f0 + rr;
     }
     // byte offset of the aligned scale word of stored row `row` for step ks
+    // (forward kinds: the two groups of 32 columns ks*64 .. ks*64+63)
     __device__ static int64_t scale_word(const TcArgs &a, int64_t row, int ks)
     {
         if (FMT == PMOE_W_INT4_G32_BF16) return 2 * (row * (a.Kst >> 5) + 2 * ks);
         if (FMT == PMOE_W_MXFP4_G32_E8M0) return (row * (a.Kst >> 5) + 2 * ks) & ~(int64_t)3;
         return 4 * ((row >> 7) * (a.Kst >> 7) + ((int64_t)ks * kBK >> 7));
     }
+    // backward kinds: byte offset of the first aligned scale word covering
+    // columns f0 .. f0+127 of stored row `row` (two consecutive words hold
+    // the four groups of 32: INT4 4 x BF16; MXFP4 4 bytes starting at byte
+    // (row * Kst/32) & 3 of the first word; FP8 the block's f32 scale)
+    __device__ static int64_t scale_word_t(const TcArgs &a, int64_t row, int f0)
+    {
+        if (FMT == PMOE_W_INT4_G32_BF16) return 2 * (row * (a.Kst >> 5) + (f0 >> 5));
+        if (FMT == PMOE_W_MXFP4_G32_E8M0) return (row * (a.Kst >> 5) + (f0 >> 5)) & ~(int64_t)3;
+        return 4 * ((row >> 7) * (a.Kst >> 7) + (f0 >> 7));
+    }
 
-    // Convert one TMA raw tile (non-transposed kinds) for the A stage.
-    // A converter group of 8192 / EPT threads: thread tg takes A row
-    // m = tg / (64 / EPT) and EPT consecutive K elements of it (EPT / 8
-    // 16-byte chunks of the swizzled row).  The converted chunks stay in
-    // registers; store_tma() writes them.
+    // 8 packed elements (one u32 of 4-bit codes, or a uint2 of FP8 codes)
+    // and their scale -> one 16-byte chunk of 8 BF16 in element order
+    __device__ static uint4 chunk4(uint32_t w, uint32_t sbits)
+    {
+        uint4 o;
+        if (FMT == PMOE_W_INT4_G32_BF16) {
+            uint32_t p[4];
+            int4x8_pairs(w, sbits | (sbits << 16), p);
+            o.x = prmt(p[0], p[1], 0x5410);
+            o.y = prmt(p[2], p[3], 0x5410);
+            o.z = prmt(p[0], p[1], 0x7632);
+            o.w = prmt(p[2], p[3], 0x7632);
+        } else {
+            const float sc = e8m0_value(sbits);
+            uint32_t r[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                r[j] = pack_bf2(__fmul_rn(e2m1_value((w >> (8 * j)) & 15u), sc),
+                                __fmul_rn(e2m1_value((w >> (8 * j + 4)) & 15u), sc));
+            o = make_uint4(r[0], r[1], r[2], r[3]);
+        }
+        return o;
+    }
+    __device__ static uint4 chunk8(uint2 w2, float sc)
+    {
+        uint32_t o[4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t w = h ? w2.y : w2.x;
+            __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3);
+            __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+            const float2 fl = __half22float2(*(const __half2 *)&lo);
+            const float2 fh = __half22float2(*(const __half2 *)&hi);
+            o[2 * h] = pack_bf2(__fmul_rn(fl.x, sc), __fmul_rn(fl.y, sc));
+            o[2 * h + 1] = pack_bf2(__fmul_rn(fh.x, sc), __fmul_rn(fh.y, sc));
+        }
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    }
+
+    // Forward kinds (K-major A).  A converter group of 8192 / EPT threads:
+    // thread tg takes A row m = tg / (64 / EPT) and EPT consecutive K
+    // elements of it (EPT / 8 chunks of the swizzled row).
     template <int EPT>
     __device__ static void compute_tma(const TcArgs &a, int f0, int ks, int tg, const uint8_t *rawt,
                                        uint4 (&out)[EPT / 8])
@@ -408,46 +435,19 @@ struct Dequant {
         const int rr = raw_row(m);
         const bool lv = KIND == GK_FWD_GU || f0 + m < a.Mtot;
         const uint8_t *row = rawt + rr * PP::kRowBytes;
-        const uint32_t sw = *(const uint32_t *)(rawt + 128 * PP::kRowBytes + 4 * rr);
+        const uint32_t sw = *(const uint32_t *)(rawt + PP::kScaleOff + 4 * rr);
 #pragma unroll
         for (int c = 0; c < EPT / 8; ++c) {
             const int e = e0 + 8 * c, grp = e >> 5;
             if (!lv) {
                 out[c] = make_uint4(0, 0, 0, 0);
             } else if (FMT == PMOE_W_INT4_G32_BF16) {
-                const uint32_t w = *(const uint32_t *)(row + (e >> 1));
-                const uint32_t sb = grp ? sw >> 16 : sw & 0xFFFFu;
-                uint32_t p[4];
-                int4x8_pairs(w, sb | (sb << 16), p);
-                out[c].x = prmt(p[0], p[1], 0x5410);
-                out[c].y = prmt(p[2], p[3], 0x5410);
-                out[c].z = prmt(p[0], p[1], 0x7632);
-                out[c].w = prmt(p[2], p[3], 0x7632);
+                out[c] = chunk4(*(const uint32_t *)(row + (e >> 1)), grp ? sw >> 16 : sw & 0xFFFFu);
             } else if (FMT == PMOE_W_MXFP4_G32_E8M0) {
-                const uint32_t w = *(const uint32_t *)(row + (e >> 1));
                 const int64_t gi = stored_row(a, f0, rr) * (a.Kst >> 5) + 2 * ks + grp;
-                const float sc = e8m0_value((sw >> (8 * (gi & 3))) & 0xFFu);
-                uint32_t o[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    o[j] = pack_bf2(__fmul_rn(e2m1_value((w >> (8 * j)) & 15u), sc),
-                                    __fmul_rn(e2m1_value((w >> (8 * j + 4)) & 15u), sc));
-                out[c] = make_uint4(o[0], o[1], o[2], o[3]);
+                out[c] = chunk4(*(const uint32_t *)(row + (e >> 1)), (sw >> (8 * (gi & 3))) & 0xFFu);
             } else {
-                const uint2 w2 = *(const uint2 *)(row + e);
-                const float sc = __uint_as_float(sw);
-                uint32_t o[4];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t w = h ? w2.y : w2.x;
-                    __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3);
-                    __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
-                    const float2 fl = __half22float2(*(const __half2 *)&lo);
-                    const float2 fh = __half22float2(*(const __half2 *)&hi);
-                    o[2 * h] = pack_bf2(__fmul_rn(fl.x, sc), __fmul_rn(fl.y, sc));
-                    o[2 * h + 1] = pack_bf2(__fmul_rn(fh.x, sc), __fmul_rn(fh.y, sc));
-                }
-                out[c] = make_uint4(o[0], o[1], o[2], o[3]);
+                out[c] = chunk8(*(const uint2 *)(row + e), __uint_as_float(sw));
             }
         }
     }
@@ -461,179 +461,55 @@ struct Dequant {
         for (int j = 0; j < EPT / 8; ++j) st_shared_v4(rowaddr + (((c0 + j) ^ (m & 7)) << 4), out[j]);
     }
 
-    // byte offsets of a thread's pieces inside a ring stage (256 threads)
-    __device__ static uint32_t p16(int j, int td) { return (uint32_t)(j * 256 + td) * 16; }
-    __device__ static uint32_t p8(int j, int td) { return (uint32_t)(j * 256 + td) * 8; }
-    __device__ static uint32_t p4(int j, int td) { return (uint32_t)(j * 256 + td) * 4; }
-
-    __device__ static void issue(const TcArgs &a, const uint8_t *wq, const uint8_t *ws, int f0,
-                                 int ks, int td, uint32_t slot)
+    // Backward kinds (MN-major A): A[m][k] = W[ks*64 + k][f0 + m].  A group
+    // of 256 threads; thread tg takes stored row k = 8*(tg >> 5) + (tg & 7)
+    // of the step and the 32 columns 32*mq .. 32*mq+31, mq = (tg >> 3) & 3
+    // (one scale group).  The 8 lanes of a quarter-warp take 8 consecutive
+    // rows, so their raw reads and swizzled stores fall in distinct banks.
+    __device__ static void compute_t(const TcArgs &a, int f0, int ks, int tg, const uint8_t *rawt,
+                                     uint4 (&out)[4])
     {
-        if (!live(a, f0, td)) return;
-        if (!T) {
-            const int m = td >> 1, half = td & 1;
-            const int64_t row = row_of(a, f0, m);
-            const int64_t k0 = (int64_t)ks * kBK + 32 * half;
-            if (FMT == PMOE_W_INT4_G32_BF16 || FMT == PMOE_W_MXFP4_G32_E8M0) {
-                cpa16(slot + p16(0, td), wq + row * (a.Kst >> 1) + (k0 >> 1));
-                cpa4(slot + 256 * 16 + p4(0, td), ws + sword(row * (a.Kst >> 5) + (k0 >> 5)));
-            } else if (FMT == PMOE_W_FP8_B128_F32) {
-                const uint8_t *src = wq + row * a.Kst + k0;
-                cpa16(slot + p16(0, td), src);
-                cpa16(slot + p16(1, td), src + 16);
-                cpa4(slot + 2 * 256 * 16 + p4(0, td), ws + 4 * ((row >> 7) * (a.Kst >> 7) + (k0 >> 7)));
-            } else {
-                const uint8_t *src = wq + 2 * (row * a.Kst + k0);
+        using PP = Pipe<KIND, FMT>;
+        const int k = 8 * (tg >> 5) + (tg & 7), mq = (tg >> 3) & 3;
+        if (f0 + 32 * mq >= a.Mtot) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) cpa16(slot + p16(j, td), src + 16 * j);
-            }
+            for (int j = 0; j < 4; ++j) out[j] = make_uint4(0, 0, 0, 0);
+            return;
+        }
+        const uint8_t *row = rawt + k * PP::kRowBytes;
+        const uint32_t *sw = (const uint32_t *)(rawt + PP::kScaleOff + 8 * k);
+        if (FMT == PMOE_W_FP8_B128_F32) {
+            // 128-byte rows, 128-byte swizzle: chunk c sits at c ^ (k & 7)
+            const uint4 q0 = *(const uint4 *)(row + (((2 * mq) ^ (k & 7)) << 4));
+            const uint4 q1 = *(const uint4 *)(row + (((2 * mq + 1) ^ (k & 7)) << 4));
+            const float sc = __uint_as_float(sw[0]);
+            out[0] = chunk8(make_uint2(q0.x, q0.y), sc);
+            out[1] = chunk8(make_uint2(q0.z, q0.w), sc);
+            out[2] = chunk8(make_uint2(q1.x, q1.y), sc);
+            out[3] = chunk8(make_uint2(q1.z, q1.w), sc);
         } else {
-            const int mg0 = f0 + 8 * (td >> 4);
-            const int64_t n0 = (int64_t)ks * kBK + 4 * (td & 15);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int64_t n = n0 + j;
-                if (FMT == PMOE_W_FP8_B128_F32) {
-                    cpa8(slot + p8(j, td), wq + n * a.Kst + mg0);
-                    cpa4(slot + 4 * 256 * 8 + p4(j, td), ws + 4 * ((n >> 7) * (a.Kst >> 7) + (mg0 >> 7)));
-                } else {
-                    cpa4(slot + p4(j, td), wq + n * (a.Kst >> 1) + (mg0 >> 1));
-                    cpa4(slot + 4 * 256 * 4 + p4(j, td), ws + sword(n * (a.Kst >> 5) + (mg0 >> 5)));
-                }
+            // 64-byte rows, 64-byte swizzle: chunk c sits at c ^ ((k >> 1) & 3)
+            const uint4 q = *(const uint4 *)(row + ((mq ^ ((k >> 1) & 3)) << 4));
+            uint32_t sb;
+            if (FMT == PMOE_W_INT4_G32_BF16) {
+                sb = (sw[mq >> 1] >> (16 * (mq & 1))) & 0xFFFFu;
+            } else {
+                const int64_t srow = (int64_t)ks * kBK + k;
+                const int byte = (int)((srow * (a.Kst >> 5)) & 3) + mq;
+                sb = (sw[byte >> 2] >> (8 * (byte & 3))) & 0xFFu;
             }
+            out[0] = chunk4(q.x, sb);
+            out[1] = chunk4(q.y, sb);
+            out[2] = chunk4(q.z, sb);
+            out[3] = chunk4(q.w, sb);
         }
     }
-
-    // Convert the slot into the A stage (zeros for rows past a ragged tile).
-    __device__ static void convert(const TcArgs &a, int f0, int ks, int td, const uint8_t *slot,
-                                   uint32_t sA)
+    __device__ static void store_t(int tg, const uint4 (&out)[4], uint32_t sA)
     {
-        const bool lv = live(a, f0, td);
-        if (!T) {
-            const int m = td >> 1, half = td & 1;
-            const int64_t row = row_of(a, f0, m);
-            const int64_t k0 = (int64_t)ks * kBK + 32 * half;
-            uint4 out[4];
-            if (!lv) {
+        const int r = tg & 7, mq = (tg >> 3) & 3, kg = tg >> 5;
+        const uint32_t base = sA + kg * 2048 + (mq >> 1) * 1024 + r * 128;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) out[j] = make_uint4(0, 0, 0, 0);
-            } else if (FMT == PMOE_W_INT4_G32_BF16) {
-                const uint4 q = *(const uint4 *)(slot + p16(0, td));
-                const uint32_t sb = spick(*(const uint32_t *)(slot + 256 * 16 + p4(0, td)),
-                                          row * (a.Kst >> 5) + (k0 >> 5));
-                const uint32_t s2 = sb | (sb << 16);
-                const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t p[4];
-                    int4x8_pairs(words[j], s2, p);
-                    out[j].x = prmt(p[0], p[1], 0x5410);
-                    out[j].y = prmt(p[2], p[3], 0x5410);
-                    out[j].z = prmt(p[0], p[1], 0x7632);
-                    out[j].w = prmt(p[2], p[3], 0x7632);
-                }
-            } else if (FMT == PMOE_W_MXFP4_G32_E8M0) {
-                const uint4 q = *(const uint4 *)(slot + p16(0, td));
-                const float sc = e8m0_value(spick(*(const uint32_t *)(slot + 256 * 16 + p4(0, td)),
-                                                  row * (a.Kst >> 5) + (k0 >> 5)));
-                const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t w = words[j], o[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        o[e] = pack_bf2(__fmul_rn(e2m1_value((w >> (8 * e)) & 15u), sc),
-                                        __fmul_rn(e2m1_value((w >> (8 * e + 4)) & 15u), sc));
-                    out[j] = make_uint4(o[0], o[1], o[2], o[3]);
-                }
-            } else if (FMT == PMOE_W_FP8_B128_F32) {
-                const uint4 q0 = *(const uint4 *)(slot + p16(0, td));
-                const uint4 q1 = *(const uint4 *)(slot + p16(1, td));
-                const float sc = *(const float *)(slot + 2 * 256 * 16 + p4(0, td));
-                const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t o[4];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t w = words[2 * j + h];
-                        __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3);
-                        __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
-                        const float2 fl = __half22float2(*(const __half2 *)&lo);
-                        const float2 fh = __half22float2(*(const __half2 *)&hi);
-                        o[2 * h] = pack_bf2(__fmul_rn(fl.x, sc), __fmul_rn(fl.y, sc));
-                        o[2 * h + 1] = pack_bf2(__fmul_rn(fh.x, sc), __fmul_rn(fh.y, sc));
-                    }
-                    out[j] = make_uint4(o[0], o[1], o[2], o[3]);
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) out[j] = *(const uint4 *)(slot + p16(j, td));
-            }
-            const uint32_t rowaddr = sA + m * 128;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int c = 4 * half + j;
-                st_shared_v4(rowaddr + ((c ^ (m & 7)) << 4), out[j]);
-            }
-        } else {
-            // transposed: A[m][k] = W[k0 + k][f0 + m] (contraction over stored rows)
-            // lanes vary kb (K chunks of one row m): the 8-byte stores of a warp
-            // cover whole 128-byte rows, conflict-free
-            const int kb = td & 15, mb = td >> 4;
-            const int mg0 = f0 + 8 * mb;
-            const int64_t n0 = (int64_t)ks * kBK + 4 * kb;
-            uint32_t v[8][2];   // for each m: (k0,k1), (k2,k3)
-            if (!lv) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[i][0] = v[i][1] = 0;
-            } else if (FMT == PMOE_W_INT4_G32_BF16) {
-                uint32_t p[4][4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t w = *(const uint32_t *)(slot + p4(j, td));
-                    const uint32_t sb = spick(*(const uint32_t *)(slot + 4 * 256 * 4 + p4(j, td)),
-                                              (n0 + j) * (a.Kst >> 5) + (mg0 >> 5));
-                    int4x8_pairs(w, sb | (sb << 16), p[j]);
-                }
-                // p[j][i & 3] holds (m = i, m = i + 4) of row j
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t sel = i < 4 ? 0x5410u : 0x7632u;
-                    v[i][0] = prmt(p[0][i & 3], p[1][i & 3], sel);
-                    v[i][1] = prmt(p[2][i & 3], p[3][i & 3], sel);
-                }
-            } else {
-                float f[4][8];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if (FMT == PMOE_W_MXFP4_G32_E8M0) {
-                        const uint32_t w = *(const uint32_t *)(slot + p4(j, td));
-                        const float sc = e8m0_value(spick(*(const uint32_t *)(slot + 4 * 256 * 4 + p4(j, td)),
-                                                          (n0 + j) * (a.Kst >> 5) + (mg0 >> 5)));
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) f[j][i] = __fmul_rn(e2m1_value((w >> (4 * i)) & 15u), sc);
-                    } else {
-                        const uint2 w = *(const uint2 *)(slot + p8(j, td));
-                        const float sc = *(const float *)(slot + 4 * 256 * 8 + p4(j, td));
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            f[j][i] = __fmul_rn(e4m3_value(((i < 4 ? w.x : w.y) >> (8 * (i & 3))) & 255u), sc);
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    v[i][0] = pack_bf2(f[0][i], f[1][i]);
-                    v[i][1] = pack_bf2(f[2][i], f[3][i]);
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int m = 8 * mb + i;
-                st_shared_v2(sA + m * 128 + ((((kb >> 1)) ^ (m & 7)) << 4) + (kb & 1) * 8, v[i][0],
-                             v[i][1]);
-            }
-        }
+        for (int j = 0; j < 4; ++j) st_shared_v4(base + (((4 * (mq & 1) + j) ^ r) << 4), out[j]);
     }
 };
 
@@ -717,26 +593,50 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                     const int r = g % PP::kRawTma;
                     if (!(ok = mbar_wait(raw_empty(r), ((g / PP::kRawTma) & 1) ^ 1, a.err, 7))) break;
                     const uint32_t dst = raw0 + r * PP::kRawTile;
-                    if (lane == 0) {
-                        mbar_expect_tx(raw_full(r), 128 * PP::kRowBytes);
-                        const int x = ks * PP::kRowBytes;
-                        const int y = (int)(widx * a.Nst) + f0;
-                        if (KIND == GK_FWD_GU) {
-                            tma_load_2d(dst, &tmA, x, y, raw_full(r));
-                            tma_load_2d(dst + 64 * PP::kRowBytes, &tmA, x, y + a.I, raw_full(r));
-                        } else {
-                            tma_load_2d(dst, &tmA, x, y, raw_full(r));
-                        }
-                    }
                     const uint8_t *ws = a.ws + widx * a.ws_stride;
+                    if constexpr (PP::kTrans) {
+                        // 64 stored rows ks*64 .. +63, columns f0 .. f0+127
+                        if (lane == 0) {
+                            mbar_expect_tx(raw_full(r), 64 * PP::kRowBytes);
+                            tma_load_2d(dst, &tmA, PP::kFp8 ? f0 : f0 >> 1,
+                                        (int)(widx * a.Nst) + ks * kBK, raw_full(r));
+                        }
+                        // columns past Mtot (a 64-wide last tile) get no scales
+                        const bool full = f0 + 128 <= a.Mtot;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int rr = lane + 32 * i;
-                        const bool lv = KIND == GK_FWD_GU || f0 + rr < a.Mtot;
-                        if (lv)
-                            cpa4(dst + 128 * PP::kRowBytes + 4 * rr,
-                                 ws + Dequant<KIND, FMT>::scale_word(
-                                          a, Dequant<KIND, FMT>::stored_row(a, f0, rr), ks));
+                        for (int i = 0; i < 2; ++i) {
+                            const int k = lane + 32 * i;
+                            const int64_t row = (int64_t)ks * kBK + k;
+                            const uint8_t *src = ws + Dequant<KIND, FMT>::scale_word_t(a, row, f0);
+                            const uint32_t sd = dst + PP::kScaleOff + 8 * k;
+                            cpa4(sd, src);
+                            const bool second = FMT == PMOE_W_INT4_G32_BF16 ? full
+                                              : FMT == PMOE_W_MXFP4_G32_E8M0
+                                                  ? full && ((row * (a.Kst >> 5)) & 3) != 0
+                                                  : false;
+                            if (second) cpa4(sd + 4, src + 4);
+                        }
+                    } else {
+                        if (lane == 0) {
+                            mbar_expect_tx(raw_full(r), 128 * PP::kRowBytes);
+                            const int x = ks * PP::kRowBytes;
+                            const int y = (int)(widx * a.Nst) + f0;
+                            if (KIND == GK_FWD_GU) {
+                                tma_load_2d(dst, &tmA, x, y, raw_full(r));
+                                tma_load_2d(dst + 64 * PP::kRowBytes, &tmA, x, y + a.I, raw_full(r));
+                            } else {
+                                tma_load_2d(dst, &tmA, x, y, raw_full(r));
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int rr = lane + 32 * i;
+                            const bool lv = KIND == GK_FWD_GU || f0 + rr < a.Mtot;
+                            if (lv)
+                                cpa4(dst + PP::kScaleOff + 4 * rr,
+                                     ws + Dequant<KIND, FMT>::scale_word(
+                                              a, Dequant<KIND, FMT>::stored_row(a, f0, rr), ks));
+                        }
                     }
                     cpa_mbar_arrive(raw_full(r));
                 }
@@ -780,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++li) {
                 const Tile tl = a.tiles[tbeg + item / nft];
                 const int N = (tl.nrows + 15) & ~15;
-                const uint32_t idesc = idesc_bf16(kM, N);
+                const uint32_t idesc = idesc_bf16(kM, N, PP::kTrans);
                 const int acc = li & 1;
                 if (!(ok = mbar_wait(tempty(acc), ((li >> 1) & 1) ^ 1, a.err, 2))) break;
                 tc_fence_after();
@@ -792,9 +692,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                     if (!(ok = mbar_wait(full_b(s), ph, a.err, 4))) break;
                     tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        umma(d, sdesc(sA0 + s * kABytes + kk * 32), sdesc(sB0 + s * kBBytes + kk * 32),
-                             idesc, (ks | kk) != 0);
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        // K step of 16: +32 B inside the K-major swizzle row, or
+                        // two 8-row K groups (2 x 2048 B) of the MN-major tile
+                        const uint64_t ad = PP::kTrans ? sdesc_mn(sA0 + s * kABytes + kk * 4096)
+                                                       : sdesc(sA0 + s * kABytes + kk * 32);
+                        umma(d, ad, sdesc(sB0 + s * kBBytes + kk * 32), idesc, (ks | kk) != 0);
+                    }
                     umma_commit(empty(s));
                 }
                 if (ok) umma_commit(tfull(acc));
@@ -813,12 +717,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             const int grp = td / kTPG, tg = td % kTPG;
             const int my_items = n_items > (int)blockIdx.x ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
             const uint32_t total = (uint32_t)my_items * nk;
+            static_assert(!PP::kTrans || kEPT == 32, "backward converters take 32 elements each");
             auto compute = [&](uint32_t j, uint4 (&o)[kEPT / 8]) -> bool {
                 const int item = (int)blockIdx.x + (int)(j / nk) * (int)gridDim.x;
                 const int r = j % PP::kRawTma;
                 if (!mbar_wait(raw_full(r), (j / PP::kRawTma) & 1, a.err, 8)) return false;
-                Dequant<KIND, FMT>::template compute_tma<kEPT>(a, (item % nft) * a.m_tile, (int)(j % nk),
-                                                               tg, smem + PP::kRawOff + r * PP::kRawTile, o);
+                const uint8_t *rawt = smem + PP::kRawOff + r * PP::kRawTile;
+                if constexpr (PP::kTrans)
+                    Dequant<KIND, FMT>::compute_t(a, (item % nft) * a.m_tile, (int)(j % nk), tg, rawt, o);
+                else
+                    Dequant<KIND, FMT>::template compute_tma<kEPT>(a, (item % nft) * a.m_tile,
+                                                                   (int)(j % nk), tg, rawt, o);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(raw_empty(r));
                 return true;
@@ -828,7 +737,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             for (uint32_t g = grp; ok && g < total; g += kConvGroups) {
                 const int s = g % kStages;
                 if (!mbar_wait(empty(s), ((g / kStages) & 1) ^ 1, a.err, 5)) break;
-                Dequant<KIND, FMT>::template store_tma<kEPT>(tg, cur, sA0 + s * kABytes);
+                if constexpr (PP::kTrans)
+                    Dequant<KIND, FMT>::store_t(tg, cur, sA0 + s * kABytes);
+                else
+                    Dequant<KIND, FMT>::template store_tma<kEPT>(tg, cur, sA0 + s * kABytes);
                 if (g + kConvGroups < total) ok = compute(g + kConvGroups, nxt);
                 fence_proxy_async();
                 __syncwarp();
@@ -836,57 +748,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
 #pragma unroll
                 for (int c = 0; c < kEPT / 8; ++c) cur[c] = nxt[c];
             }
-        } else if constexpr (PP::kTrans) {
-            // transposed kinds: the first 256 converter threads convert, the
-            // other warps only take part in the stage handshake
-            const bool worker = td < 256;
-        // ---------------- dequant producers: packed weights prefetched
-        // kRawStages - 1 steps ahead with cp.async, converted into the A stage
-        uint8_t *raw = smem + PP::kRawOff;
-        const uint32_t raw_a = smem_u32(raw);
-        const int my_items = n_items > (int)blockIdx.x ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-        const uint32_t total = (uint32_t)my_items * nk;
-        constexpr uint32_t kRing = PP::kRawStages, kRingStride = 256 * PP::kSlot;
-        // work-item context, reloaded only when a step starts a new item
-        struct Ctx {
-            int li = -1, f0 = 0;
-            const uint8_t *wq = nullptr, *ws = nullptr;
-        };
-        auto load_ctx = [&](Ctx &c, int li) {
-            if (c.li == li) return;
-            const int item = (int)blockIdx.x + li * (int)gridDim.x;
-            const Tile tl = a.tiles[tbeg + item / nft];
-            c.li = li;
-            c.f0 = (item % nft) * a.m_tile;
-            const int64_t widx = a.slot_index ? (tl.chunk & 0xffff) : tl.expert;
-            c.wq = a.wq + widx * a.wq_stride + (FMT == kFmtBF16 ? 2 * a.w_off_elems : 0);
-            c.ws = a.ws ? a.ws + widx * a.ws_stride : nullptr;
-        };
-        Ctx cur, ahead;
-        auto issue_step = [&](uint32_t j) {
-            if (worker && j < total) {
-                load_ctx(ahead, (int)(j / nk));
-                Dequant<KIND, FMT>::issue(a, ahead.wq, ahead.ws, ahead.f0, (int)(j % nk), td,
-                                          raw_a + (j % kRing) * kRingStride);
-            }
-            cpa_commit();
-        };
-        for (uint32_t j = 0; j + 1 < kRing; ++j) issue_step(j);
-        for (uint32_t g = 0; g < total; ++g) {
-            issue_step(g + kRing - 1);
-            load_ctx(cur, (int)(g / nk));
-            cpa_wait<kRing - 1>();
-            const int s = g % kStages;
-            const uint32_t ph = (g / kStages) & 1;
-            if (!mbar_wait(empty(s), ph ^ 1, a.err, 5)) break;
-            if (worker)
-                Dequant<KIND, FMT>::convert(a, cur.f0, (int)(g % nk), td,
-                                            raw + (g % kRing) * kRingStride, sA0 + s * kABytes);
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(full_a(s));
-        }
-        cpa_wait<0>();
         }
     } else {
         // ---------------- epilogue (warps 0-3: TMEM lanes 32*warp .. +31)

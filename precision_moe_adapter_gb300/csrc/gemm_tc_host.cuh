@@ -10,9 +10,10 @@ namespace pmoe {
 namespace tc {
 
 bool make_rows_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int box_rows);
-// uint8 [rows, row_bytes] tensor, box of box_rows x box_bytes, no swizzle
+// uint8 [rows, row_bytes] tensor, box of box_rows x box_bytes, swizzle of
+// swizzle_bytes (0: none, 64 or 128; box_bytes must then equal it)
 bool make_bytes_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t row_bytes,
-                     int box_bytes, int box_rows);
+                     int box_bytes, int box_rows, int swizzle_bytes);
 // BF16 scratch slots [slots][rows][cols], box 64 cols x box_rows, 128-byte swizzle
 bool make_slots_tmap(CUtensorMap *m, const void *base, int64_t slots, int64_t rows, int64_t cols,
                      int64_t slot_bytes, int box_rows);
@@ -33,8 +34,9 @@ bool launch_kind(const CUtensorMap (&tmB)[4], const TcArgs &a, int64_t nmat, cud
     if constexpr (PP::kTmaRaw) {
         // packed weights of all experts as one [nmat * Nst, row bytes] byte tensor
         const int64_t rb = FMT == PMOE_W_FP8_B128_F32 ? a.Kst : a.Kst / 2;
-        if (!make_bytes_tmap(&tmA, a.wq, nmat * a.Nst, rb, PP::kRowBytes,
-                             KIND == GK_FWD_GU ? 64 : 128))
+        const int box_rows = PP::kTrans ? 64 : KIND == GK_FWD_GU ? 64 : 128;
+        if (!make_bytes_tmap(&tmA, a.wq, nmat * a.Nst, rb, PP::kRowBytes, box_rows,
+                             PP::kTrans ? PP::kRowBytes : 0))
             return false;
     } else if constexpr (PP::kBf16) {
         if (!make_slots_tmap(&tmA, a.wq + 2 * a.w_off_elems, nmat, a.Nst, a.Kst, a.wq_stride,

@@ -123,6 +123,22 @@ def test_ragged_feature_tile():
     assert_close(bits_to_f64(got), want, "ragged", rel_fro=3e-3, max_abs=1e-2)
 
 
+@pytest.mark.parametrize("fmt", [gi.INT4, gi.MXFP4])
+def test_transposed_ragged_feature_tile_is_exact(fmt):
+    """Contraction over the stored rows with 320 stored columns: the last
+    feature tile is 64 wide, and rows of 10 scale groups start at scale
+    words that are not 4-byte aligned (MXFP4) or 8-byte aligned (INT4)."""
+    E, N, K = 3, 192, 320
+    q, s = gi.gen_matrix(fmt, E, N, K, seed=11, qsid="w13", ssid="s13")
+    A = np.tile(gi.f32_to_bf16_bits(np.eye(N, dtype=np.float32)), (E, 1))
+    got, st = run(fmt, q, s, E, N, K, 1, A, [N] * E)
+    assert st == pmoe.PMOE_OK
+    z = lambda x: np.where((x & 0x7FFF) == 0, 0, x).astype(np.uint16)
+    for e in range(E):
+        want = z(oracle.dequant(fmt, q[e], s[e], N, K))
+        assert np.array_equal(z(got[e * N:(e + 1) * N]), want), e
+
+
 @pytest.mark.parametrize("offsets", [[0, 5, 3, 8], [0, 4, 8, 9], [1, 4, 6, 8]])
 def test_inconsistent_offsets_are_rejected(offsets):
     E, N, K, rows = 3, 128, 128, 8
