@@ -75,6 +75,82 @@ __global__ void __launch_bounds__(4 * B) k_cayley(const float *__restrict__ S,
     }
 }
 
+// The same elimination with one warp per block matrix (b = 16, 32, 64), so
+// no block-wide barrier is needed: lane (row group rg = lane / 8, column
+// group cg = lane % 8) keeps rows rg*b/4 .. +b/4-1 and columns cg*b/8 ..
+// +b/8-1 in registers.  For pivot k the lanes fetch, by shuffles, the old
+// column k for their rows, the pivot row for their columns and the pivot
+// itself; every element then takes one fused multiply-add.  Operation for
+// operation this is the elimination above, so the results are identical.
+template <int B>
+__global__ void __launch_bounds__(128) k_cayley_warp(int nblk, const float *__restrict__ S,
+                                                     uint16_t *__restrict__ Rb, float *__restrict__ Rf)
+{
+    constexpr int RL = B / 4, CL = B / 8;
+    static_assert(RL == 2 * CL && CL >= 2, "b = 16, 32 or 64");
+    const int lane = threadIdx.x & 31;
+    const int blk = blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (blk >= nblk) return;
+    const int rg = lane >> 3, cg = lane & 7;
+    const int64_t off = (int64_t)blk * B * B;
+    float v[RL][CL];
+#pragma unroll
+    for (int i = 0; i < RL; ++i) {
+        const int row = rg * RL + i;
+#pragma unroll
+        for (int j = 0; j < CL; j += 2) {
+            const int col = cg * CL + j;
+            const float2 sv = *(const float2 *)(S + off + row * B + col);
+            v[i][j] = (row == col ? 1.f : 0.f) - sv.x;
+            v[i][j + 1] = (row == col + 1 ? 1.f : 0.f) - sv.y;
+        }
+    }
+    for (int g = 0; g < 4; ++g) {
+        const bool in_g = rg == g;   // this lane holds part of the pivot rows
+#pragma unroll
+        for (int kk = 0; kk < RL; ++kk) {
+            const int jj = kk % CL;               // pivot column inside its group
+            const int h = 2 * g + kk / CL;        // column group of pivot k
+            const bool in_h = cg == h;
+            float f[RL], ps[CL];
+#pragma unroll
+            for (int i = 0; i < RL; ++i) f[i] = __shfl_sync(0xffffffffu, v[i][jj], (lane & ~7) | h);
+#pragma unroll
+            for (int j = 0; j < CL; ++j) ps[j] = __shfl_sync(0xffffffffu, v[kk][j], (g << 3) | cg);
+            const float p = 1.f / __shfl_sync(0xffffffffu, v[kk][jj], (g << 3) | h);
+#pragma unroll
+            for (int j = 0; j < CL; ++j) ps[j] *= p;
+            if (in_g) f[kk] = 0.f;   // the pivot row is only rescaled
+#pragma unroll
+            for (int i = 0; i < RL; ++i)
+#pragma unroll
+                for (int j = 0; j < CL; ++j) v[i][j] = fmaf(-f[i], ps[j], v[i][j]);
+            if (in_g) {
+#pragma unroll
+                for (int j = 0; j < CL; ++j) v[kk][j] = ps[j];
+            }
+            if (in_h) {   // column k becomes column k of the inverse
+#pragma unroll
+                for (int i = 0; i < RL; ++i) v[i][jj] = fmaf(-f[i], p, 0.f);   // +0, never -0
+                if (in_g) v[kk][jj] = p;
+            }
+        }
+    }
+    // v holds A = (I - S)^{-1}; R = 2A - I
+#pragma unroll
+    for (int i = 0; i < RL; ++i) {
+        const int row = rg * RL + i;
+#pragma unroll
+        for (int j = 0; j < CL; j += 2) {
+            const int col = cg * CL + j;
+            const float r0 = 2.f * v[i][j] - (row == col ? 1.f : 0.f);
+            const float r1 = 2.f * v[i][j + 1] - (row == col + 1 ? 1.f : 0.f);
+            if (Rf) *(float2 *)(Rf + off + row * B + col) = make_float2(r0, r1);
+            if (Rb) *(uint32_t *)(Rb + off + row * B + col) = pack_bf2(r0, r1);
+        }
+    }
+}
+
 // Small blocks (b <= 8): one thread per block matrix, the same in-place
 // elimination in registers.
 template <int B>
@@ -186,11 +262,92 @@ __global__ void __launch_bounds__(256) k_cayley_grad(const float *__restrict__ R
     }
 }
 
+// The same gradient for b >= 8 with every operand read as row segments:
+// I + R, its transpose and G are staged in shared memory (pitch b + 4,
+// float4-aligned), each thread computes 4 x 4 output tiles as sums of outer
+// products, T = (I+R)^T G goes back transposed over G, and
+// M = T (I+R)^T / 2 over I + R, so dS = M - M^T reads M twice.
+template <int B>
+__global__ void __launch_bounds__(256) k_cayley_grad4(const float *__restrict__ Rf,
+                                                      const float *__restrict__ G,
+                                                      float *__restrict__ dS)
+{
+    extern __shared__ __align__(16) float sm[];
+    constexpr int P = B + 4;
+    constexpr int NT = (B / 4) * (B / 4);          // 4 x 4 tiles
+    constexpr int NTT = (NT + 255) / 256;          // tiles per thread
+    float *Ip = sm, *IpT = sm + B * P, *W = sm + 2 * B * P;
+    const int64_t off = (int64_t)blockIdx.x * B * B;
+    for (int i = threadIdx.x; i < B * B; i += blockDim.x) {
+        const int r = i / B, c = i % B;
+        const float x = Rf[off + i] + (r == c ? 1.f : 0.f);
+        Ip[r * P + c] = x;
+        IpT[c * P + r] = x;
+        W[r * P + c] = G[off + i];
+    }
+    __syncthreads();
+    // C[r][c] = sum_m L[m][r] Q[m][c] for the thread's tiles
+    auto outer = [&](const float *L, const float *Q, float (&acc)[NTT][4][4]) {
+#pragma unroll
+        for (int u = 0; u < NTT; ++u) {
+            const int t = threadIdx.x + 256 * u;
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) acc[u][a][b] = 0.f;
+            if (t >= NT) continue;
+            const int r0 = (t / (B / 4)) * 4, c0 = (t % (B / 4)) * 4;
+#pragma unroll 8
+            for (int m = 0; m < B; ++m) {
+                const float4 x = *(const float4 *)(L + m * P + r0);
+                const float4 y = *(const float4 *)(Q + m * P + c0);
+                const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) acc[u][a][b] = fmaf(xs[a], ys[b], acc[u][a][b]);
+            }
+        }
+    };
+    float acc[NTT][4][4];
+    outer(Ip, W, acc);              // T = (I+R)^T G
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < NTT; ++u) {  // W <- T^T
+        const int t = threadIdx.x + 256 * u;
+        if (t >= NT) continue;
+        const int r0 = (t / (B / 4)) * 4, c0 = (t % (B / 4)) * 4;
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            *(float4 *)(W + (c0 + b) * P + r0) =
+                make_float4(acc[u][0][b], acc[u][1][b], acc[u][2][b], acc[u][3][b]);
+    }
+    __syncthreads();
+    outer(W, IpT, acc);             // 2M = T (I+R)^T: L[m][r] = T[r][m], Q[m][c] = (I+R)[c][m]
+#pragma unroll
+    for (int u = 0; u < NTT; ++u) {  // Ip <- M (no longer read)
+        const int t = threadIdx.x + 256 * u;
+        if (t >= NT) continue;
+        const int r0 = (t / (B / 4)) * 4, c0 = (t % (B / 4)) * 4;
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+            *(float4 *)(Ip + (r0 + a) * P + c0) = make_float4(0.5f * acc[u][a][0], 0.5f * acc[u][a][1],
+                                                              0.5f * acc[u][a][2], 0.5f * acc[u][a][3]);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < B * B; i += blockDim.x) {
+        const int r = i / B, c = i % B;
+        dS[off + i] = Ip[r * P + c] - Ip[c * P + r];
+    }
+}
+
 template <int B>
 static void cayley_b(int nblk, const float *S, uint16_t *Rb, float *Rf, cudaStream_t st)
 {
     if constexpr (B < 16)
         k_cayley_small<B><<<(int)cdiv(nblk, 128), 128, 0, st>>>(nblk, S, Rb, Rf);
+    else if constexpr (B <= 64)
+        k_cayley_warp<B><<<(int)cdiv(nblk, 4), 128, 0, st>>>(nblk, S, Rb, Rf);
     else
         k_cayley<B><<<nblk, 4 * B, 0, st>>>(S, Rb, Rf);
 }
@@ -200,11 +357,19 @@ static void cayley_grad_b(int nblk, const float *Rf, const float *dR, float *dS,
 {
     const size_t sm = 3 * (size_t)B * (B + 4) * sizeof(float);
     static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_cayley_grad<B>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-        attr = true;
+    if constexpr (B >= 8) {
+        if (!attr) {
+            cudaFuncSetAttribute(k_cayley_grad4<B>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+            attr = true;
+        }
+        k_cayley_grad4<B><<<nblk, 256, sm, st>>>(Rf, dR, dS);
+    } else {
+        if (!attr) {
+            cudaFuncSetAttribute(k_cayley_grad<B>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+            attr = true;
+        }
+        k_cayley_grad<B><<<nblk, 256, sm, st>>>(Rf, dR, dS);
     }
-    k_cayley_grad<B><<<nblk, 256, sm, st>>>(Rf, dR, dS);
 }
 
 bool cayley_block_ok(int b) { return b == 2 || b == 4 || b == 8 || b == 16 || b == 32 || b == 64 || b == 128; }
