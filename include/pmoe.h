@@ -153,6 +153,35 @@ pmoe_status moe_permute(pmoe_dims dims, const int32_t *idx, const pmoe_routing *
                         void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * moe_permute_noalloc -- moe_permute for callers that cannot provide a
+ * workspace (an operator or plugin hook that is handed only its tensors, or
+ * code running where it must not allocate).  The pages have no counterpart:
+ * this is a convenience of the library, not a step of the method.
+ *
+ * Same arguments, outputs and results as moe_permute (bit-identical), but
+ * the per-block histogram lives in a fixed buffer of
+ * PMOE_PERMUTE_NOALLOC_SCRATCH_BYTES of device memory inside the library
+ * image; nothing is allocated, on the device or through another library.
+ *   Size limit: ceil(T*k / 1024) * E * 4 bytes must not exceed
+ *   PMOE_PERMUTE_NOALLOC_SCRATCH_BYTES, else PMOE_ERR_WORKSPACE (checked on
+ *   the host before any device work; e.g. E = 384 allows T*k <= 699392).
+ *   Nothing has to be zeroed first: each call overwrites what it reads.
+ *   There is no device error word: an id outside [0, E) is left out of
+ *   counts and gets inv_perm = -1, so offsets[E] < T*k reveals it.
+ *   The buffer is one per device for the whole process: calls that can
+ *   overlap in time (different streams, or different host threads without
+ *   ordering) race on it; order them.  The first call on a device looks up
+ *   the buffer's device address (a runtime call); make that first call
+ *   outside any stream capture.
+ * Errors: PMOE_ERR_INVALID_ARG as moe_permute; PMOE_ERR_WORKSPACE when the
+ * problem exceeds the buffer; PMOE_ERR_CUDA if the address lookup or the
+ * launch fails.
+ */
+#define PMOE_PERMUTE_NOALLOC_SCRATCH_BYTES (1u << 20)
+pmoe_status moe_permute_noalloc(pmoe_dims dims, const int32_t *idx, const pmoe_routing *out,
+                                cudaStream_t stream);
+
+/*
  * moe_chunked_forward -- the layer (page 1, 技艺细节): active experts are
  * taken C at a time in ascending id order; each chunk's experts are
  * dequantized to BF16 (FUSED: tile by tile in shared memory, no global

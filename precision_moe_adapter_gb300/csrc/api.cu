@@ -86,7 +86,7 @@ struct Carver {
     }
 };
 
-static bool dims_ok(const pmoe_dims &d)
+bool dims_ok(const pmoe_dims &d)
 {
     if (d.T < 0 || d.d <= 0 || d.inter <= 0 || d.E <= 0 || d.k <= 0) return false;
     if (d.k > d.E || d.E > 4096 || d.k > 32) return false;

@@ -9,6 +9,9 @@
 
 namespace pmoe {
 
+// api.cu: the shape checks every entry point applies
+bool dims_ok(const pmoe_dims &d);
+
 // route_permute.cu
 void launch_logits_f32(int T, int d, int E, const uint16_t *X, const float *Wr, float *out,
                        cudaStream_t st);

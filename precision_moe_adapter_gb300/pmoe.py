@@ -26,7 +26,8 @@ EXPORTS = ("moe_route", "moe_permute", "moe_chunked_forward", "moe_backward_data
            "adapter_apply", "adapter_grad", "adapter_cayley", "adapter_cayley_grad",
            "moe_workspace_bytes", "moe_scratch_bytes", "moe_clear_status", "moe_query_status",
            "pmoe_status_string", "pmoe_launch_count", "pmoe_kernel_timing", "pmoe_kernel_time",
-           "moe_grouped_gemm", "moe_grouped_gemm_ws_bytes")
+           "moe_grouped_gemm", "moe_grouped_gemm_ws_bytes", "moe_permute_noalloc")
+PERMUTE_NOALLOC_SCRATCH_BYTES = 1 << 20
 KT_GEMM_GATE_UP, KT_GEMM_DOWN, KT_GEMM_BWD_G, KT_GEMM_BWD_DX, KT_ROUTER = 0, 1, 2, 3, 4
 
 
@@ -81,6 +82,7 @@ def _declare(L):
     sig = {
         "moe_route": [D, p, p, p, p, p, p, ctypes.c_int, p, sz, p],
         "moe_permute": [D, p, PR, p, sz, p],
+        "moe_permute_noalloc": [D, p, PR, p],
         "moe_chunked_forward": [D, PW, PA, PR, p, i32, ctypes.c_int, p, p, p, sz, p],
         "moe_backward_data": [D, PW, PA, PR, p, p, p, i32, p, p, p, p, p, sz, p],
         "moe_dequant": [ctypes.c_int, p, p, i64, i64, p, p],
@@ -177,6 +179,11 @@ def moe_route(dm, X, Wr, bias, logits, idx, w, ws, mode=ROUTE_FAST, stream=None)
 def moe_permute(dm, idx, rt: Routing, ws, stream=None):
     _check(lib().moe_permute(dm, _ptr(idx), ctypes.byref(rt), _ptr(ws), _nbytes(ws),
                              _stream(stream)), "moe_permute")
+
+
+def moe_permute_noalloc(dm, idx, rt: Routing, stream=None):
+    _check(lib().moe_permute_noalloc(dm, _ptr(idx), ctypes.byref(rt), _stream(stream)),
+           "moe_permute_noalloc")
 
 
 def moe_chunked_forward(dm, wts: Weights, adp, rt: Routing, X, chunk_C, mode, Y, ctx, ws,
