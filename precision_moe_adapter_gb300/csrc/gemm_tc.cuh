@@ -41,9 +41,10 @@ constexpr int kABytes = kM * kBK * 2;        // 16 KB
 constexpr int kBBytes = kNmax * kBK * 2;     // 32 KB
 constexpr int kBoxRows = 32;                 // smallest TMA box: 32 token rows x 64 K
 constexpr int kEpiWarps = 4;
-constexpr int kProdWarp = 4;
+constexpr int kRawWarp = 4;                  // packed weight tiles + scale words
 constexpr int kMmaWarp = 5;
-constexpr int kDqWarp0 = 6;
+constexpr int kBWarp = 6;                    // token tiles (and BF16 weight tiles)
+constexpr int kDqWarp0 = 7;
 constexpr int kDqWarps = 16;
 #ifndef PMOE_CONV_GROUPS
 #define PMOE_CONV_GROUPS 2
@@ -296,12 +297,20 @@ struct Pipe {
     static constexpr bool kBf16 = FMT == kFmtBF16;
     static constexpr bool kTmaRaw = !kBf16;
     static constexpr bool kFp8 = FMT == PMOE_W_FP8_B128_F32;
+#ifdef PMOE_AB_STAGES
+    static constexpr int kStagesAB = kFp8 ? 3 : PMOE_AB_STAGES;
+#else
     static constexpr int kStagesAB = kFp8 ? 3 : 4;
+#endif
     static constexpr int kRawRows = kTrans ? 64 : 128;
     static constexpr int kRowBytes = kTrans ? (kFp8 ? 128 : 64) : (kFp8 ? 64 : 32);
     static constexpr int kScaleOff = kRawRows * kRowBytes;   // scale words after the data
     static constexpr int kRawTile = kTrans ? (kScaleOff + 64 * 8 + 1023) & ~1023 : kScaleOff + 128 * 4;
-    static constexpr int kRawTma = 4;      // raw ring stages
+#ifdef PMOE_RAW_STAGES
+    static constexpr int kRawTma = kFp8 ? 8 : PMOE_RAW_STAGES;
+#else
+    static constexpr int kRawTma = kFp8 ? 8 : 6;   // raw ring stages
+#endif
     static constexpr int kRawBytes = kTmaRaw ? kRawTma * kRawTile : 0;
     static constexpr int kNumBars = 3 * kStagesAB + 4 + 2 * kRawTma;
     static constexpr int kBarOff = kStagesAB * (kABytes + kBBytes);
@@ -436,18 +445,32 @@ struct Dequant {
         const bool lv = KIND == GK_FWD_GU || f0 + m < a.Mtot;
         const uint8_t *row = rawt + rr * PP::kRowBytes;
         const uint32_t sw = *(const uint32_t *)(rawt + PP::kScaleOff + 4 * rr);
+        // the thread's packed bytes are contiguous: load them as vectors
+        constexpr int kB = FMT == PMOE_W_FP8_B128_F32 ? EPT : EPT / 2;
+        uint32_t wv[kB / 4];
+        const uint8_t *src = row + (FMT == PMOE_W_FP8_B128_F32 ? e0 : e0 / 2);
+        if constexpr (kB >= 16) {
+#pragma unroll
+            for (int v = 0; v < kB / 16; ++v) {
+                const uint4 q = *(const uint4 *)(src + 16 * v);
+                wv[4 * v] = q.x, wv[4 * v + 1] = q.y, wv[4 * v + 2] = q.z, wv[4 * v + 3] = q.w;
+            }
+        } else {
+            const uint2 q = *(const uint2 *)src;
+            wv[0] = q.x, wv[1] = q.y;
+        }
 #pragma unroll
         for (int c = 0; c < EPT / 8; ++c) {
             const int e = e0 + 8 * c, grp = e >> 5;
             if (!lv) {
                 out[c] = make_uint4(0, 0, 0, 0);
             } else if (FMT == PMOE_W_INT4_G32_BF16) {
-                out[c] = chunk4(*(const uint32_t *)(row + (e >> 1)), grp ? sw >> 16 : sw & 0xFFFFu);
+                out[c] = chunk4(wv[c], grp ? sw >> 16 : sw & 0xFFFFu);
             } else if (FMT == PMOE_W_MXFP4_G32_E8M0) {
                 const int64_t gi = stored_row(a, f0, rr) * (a.Kst >> 5) + 2 * ks + grp;
-                out[c] = chunk4(*(const uint32_t *)(row + (e >> 1)), (sw >> (8 * (gi & 3))) & 0xFFu);
+                out[c] = chunk4(wv[c], (sw >> (8 * (gi & 3))) & 0xFFu);
             } else {
-                out[c] = chunk8(*(const uint2 *)(row + e), __uint_as_float(sw));
+                out[c] = chunk8(make_uint2(wv[2 * c], wv[2 * c + 1]), __uint_as_float(sw));
             }
         }
     }
@@ -576,20 +599,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *(volatile uint32_t *)tmem_slot;
 
-    if (warp == kProdWarp) {
-        // ---------------- producer: token tiles (TMA), packed weight tiles
-        // (TMA) with their scale words (cp.async by the 32 lanes), or BF16
-        // weight tiles (TMA into the swizzled A stage)
-        uint32_t g = 0;
-        bool ok = true;
-        for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-            const Tile tl = a.tiles[tbeg + item / nft];
-            // token rows covered: round up to 32, in boxes of 256/128/64/32 rows
-            const int brows = (tl.nrows + kBoxRows - 1) & ~(kBoxRows - 1);
-            const int f0 = (item % nft) * a.m_tile;
-            const int64_t widx = a.slot_index ? (tl.chunk & 0xffff) : tl.expert;
-            for (int ks = 0; ks < nk; ++ks, ++g) {
-                if constexpr (PP::kTmaRaw) {
+    if (warp == kRawWarp) {
+        // ---------------- weight producer: packed weight tiles (TMA) with
+        // their scale words (cp.async by the 32 lanes).  It runs ahead of
+        // the token producer by up to the depth of the raw ring, so HBM
+        // latency of the weights overlaps the conversion of earlier tiles.
+        if constexpr (PP::kTmaRaw) {
+            uint32_t g = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+                const Tile tl = a.tiles[tbeg + item / nft];
+                const int f0 = (item % nft) * a.m_tile;
+                const int64_t widx = a.slot_index ? (tl.chunk & 0xffff) : tl.expert;
+                for (int ks = 0; ks < nk; ++ks, ++g) {
                     const int r = g % PP::kRawTma;
                     if (!(ok = mbar_wait(raw_empty(r), ((g / PP::kRawTma) & 1) ^ 1, a.err, 7))) break;
                     const uint32_t dst = raw0 + r * PP::kRawTile;
@@ -640,6 +662,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                     }
                     cpa_mbar_arrive(raw_full(r));
                 }
+            }
+        }
+    } else if (warp == kBWarp) {
+        // ---------------- token producer: token tiles (TMA), or BF16 weight
+        // tiles (TMA into the swizzled A stage)
+        uint32_t g = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+            const Tile tl = a.tiles[tbeg + item / nft];
+            // token rows covered: round up to 32, in boxes of 256/128/64/32 rows
+            const int brows = (tl.nrows + kBoxRows - 1) & ~(kBoxRows - 1);
+            const int f0 = (item % nft) * a.m_tile;
+            const int64_t widx = a.slot_index ? (tl.chunk & 0xffff) : tl.expert;
+            (void)f0;
+            (void)widx;
+            for (int ks = 0; ks < nk; ++ks, ++g) {
                 const int s = g % kStages;
                 const uint32_t ph = (g / kStages) & 1;
                 if (!(ok = mbar_wait(empty(s), ph ^ 1, a.err, 1))) break;
@@ -718,22 +756,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             const int my_items = n_items > (int)blockIdx.x ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
             const uint32_t total = (uint32_t)my_items * nk;
             static_assert(!PP::kTrans || kEPT == 32, "backward converters take 32 elements each");
-            auto compute = [&](uint32_t j, uint4 (&o)[kEPT / 8]) -> bool {
-                const int item = (int)blockIdx.x + (int)(j / nk) * (int)gridDim.x;
-                const int r = j % PP::kRawTma;
-                if (!mbar_wait(raw_full(r), (j / PP::kRawTma) & 1, a.err, 8)) return false;
+            // position of a step in this CTA's work: K step ks of the item's
+            // feature tile f0, advanced incrementally (no divisions per step)
+            struct Cur {
+                uint32_t j;
+                int ks, li, f0;
+            };
+            auto at = [&](uint32_t j) {
+                Cur c;
+                c.j = j;
+                c.li = (int)(j / nk);
+                c.ks = (int)(j - (uint32_t)c.li * nk);
+                c.f0 = (((int)blockIdx.x + c.li * (int)gridDim.x) % nft) * a.m_tile;
+                return c;
+            };
+            auto advance = [&](Cur &c) {
+                c.j += kConvGroups;
+                c.ks += kConvGroups;
+                if (c.ks >= nk) c = at(c.j);
+            };
+            auto compute = [&](const Cur &c, uint4 (&o)[kEPT / 8]) -> bool {
+                const int r = c.j % PP::kRawTma;
+                if (!mbar_wait(raw_full(r), (c.j / PP::kRawTma) & 1, a.err, 8)) return false;
                 const uint8_t *rawt = smem + PP::kRawOff + r * PP::kRawTile;
                 if constexpr (PP::kTrans)
-                    Dequant<KIND, FMT>::compute_t(a, (item % nft) * a.m_tile, (int)(j % nk), tg, rawt, o);
+                    Dequant<KIND, FMT>::compute_t(a, c.f0, c.ks, tg, rawt, o);
                 else
-                    Dequant<KIND, FMT>::template compute_tma<kEPT>(a, (item % nft) * a.m_tile,
-                                                                   (int)(j % nk), tg, rawt, o);
+                    Dequant<KIND, FMT>::template compute_tma<kEPT>(a, c.f0, c.ks, tg, rawt, o);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(raw_empty(r));
                 return true;
             };
             uint4 cur[kEPT / 8], nxt[kEPT / 8];
-            bool ok = (uint32_t)grp >= total || compute(grp, cur);
+            Cur nc = at((uint32_t)grp);
+            bool ok = (uint32_t)grp >= total || compute(nc, cur);
             for (uint32_t g = grp; ok && g < total; g += kConvGroups) {
                 const int s = g % kStages;
                 if (!mbar_wait(empty(s), ((g / kStages) & 1) ^ 1, a.err, 5)) break;
@@ -741,7 +797,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                     Dequant<KIND, FMT>::store_t(tg, cur, sA0 + s * kABytes);
                 else
                     Dequant<KIND, FMT>::template store_tma<kEPT>(tg, cur, sA0 + s * kABytes);
-                if (g + kConvGroups < total) ok = compute(g + kConvGroups, nxt);
+                advance(nc);
+                if (nc.j < total) ok = compute(nc, nxt);
                 fence_proxy_async();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(full_a(s));
