@@ -194,6 +194,9 @@ struct PermWs {
     DevErr *err;
     int32_t *hist;
     float *logits;
+    uint16_t *wr3;        // router weight split [E, 3d] bf16
+    Tile *rtiles;         // router token tiles
+    int32_t *rchunk;      // [2]
 };
 static PermWs carve_perm(void *ws, const pmoe_dims &d, size_t *bytes)
 {
@@ -202,6 +205,9 @@ static PermWs carve_perm(void *ws, const pmoe_dims &d, size_t *bytes)
     w.err = c.take<DevErr>(kHdrBytes / sizeof(DevErr));
     w.hist = c.take<int32_t>(permute_ws_bytes(d.T * d.k, d.E) / sizeof(int32_t));
     w.logits = c.take<float>((int64_t)d.T * d.E);
+    w.wr3 = c.take<uint16_t>((int64_t)d.E * 3 * d.d);
+    w.rtiles = c.take<Tile>(cdiv(d.T > 0 ? d.T : 1, 16));
+    w.rchunk = c.take<int32_t>(2);
     if (bytes) *bytes = c.off;
     return w;
 }
@@ -311,7 +317,26 @@ pmoe_status moe_route(pmoe_dims dims, const void *X, const float *Wr, const floa
     if (dims.T == 0) return PMOE_OK;
     {
         ScopedTimer tm(PMOE_KT_ROUTER, stream);
-        launch_logits_f32(dims.T, dims.d, dims.E, (const uint16_t *)X, Wr, pw.logits, stream);
+        const int rows = router_tile_rows(dims.T, dims.E, gemm_num_sms());
+        launch_router_prep(dims.T, dims.d, dims.E, Wr, pw.wr3, pw.rtiles, pw.rchunk, rows, stream);
+        GemmArgs g{};
+        g.kind = GK_ROUTER;
+        g.fmt = kFmtBF16;
+        g.wq = (const uint8_t *)pw.wr3;
+        g.wq_stride = (int64_t)dims.E * 3 * dims.d * 2;
+        g.Nst = dims.E;
+        g.Kst = 3 * (int64_t)dims.d;
+        g.nmat = 1;
+        g.A = (const uint16_t *)X;
+        g.K = 3 * dims.d;
+        g.Kb = dims.d;
+        g.Nout = dims.E;
+        g.tiles = pw.rtiles;
+        g.chunk_tiles = pw.rchunk;
+        g.c0 = 0;
+        g.c1 = 1;
+        g.outf = pw.logits;
+        if (!launch_gemm_tc(g, dims.T, pw.err, stream)) return PMOE_ERR_CUDA;
     }
     launch_route_topk(dims.T, dims.E, dims.k, pw.logits, bias, idx, w, logits, stream);
     return launched(stream);

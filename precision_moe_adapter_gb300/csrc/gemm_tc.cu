@@ -95,6 +95,8 @@ int num_sms()
 
 }  // namespace tc
 
+int gemm_num_sms() { return tc::num_sms(); }
+
 bool launch_gemm_tc(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st)
 {
     switch (g.fmt) {

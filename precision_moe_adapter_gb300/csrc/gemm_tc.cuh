@@ -264,6 +264,7 @@ struct TcArgs {
     int64_t Nst;                // rows of one expert's stored matrix
     int64_t w_off_elems;        // BF16 scratch: element offset of the matrix in a slot
     int K;                      // contraction length
+    int Kb;                     // columns of the token operand (K, or d for the router)
     int Mtot;                   // output features
     int m_tile;                 // output features per tile (64 gate/up pairs, else 128)
     const Tile *tiles;
@@ -277,6 +278,7 @@ struct TcArgs {
     const int32_t *perm;
     const uint16_t *ht;
     float *dtw_part;
+    float *outf;
     DevErr *err;
 };
 
@@ -688,7 +690,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                         const CUtensorMap *tm = left >= 256 ? &tmB256 : left >= 128 ? &tmB128
                                               : left >= 64 ? &tmB64 : &tmB32;
                         const int rows = left >= 256 ? 256 : left >= 128 ? 128 : left >= 64 ? 64 : 32;
-                        tma_load_2d(sB0 + s * kBBytes + r0 * kBK * 2, tm, ks * kBK, tl.row0 + r0, full_b(s));
+                        const int xb = KIND == GK_ROUTER ? (ks * kBK) % a.Kb : ks * kBK;
+                        tma_load_2d(sB0 + s * kBBytes + r0 * kBK * 2, tm, xb, tl.row0 + r0, full_b(s));
                         r0 += rows;
                     }
                     if constexpr (PP::kBf16) {
@@ -869,6 +872,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                             for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
                             if (fl && lane == 0 && jj < ncol)
                                 a.dtw_part[r * (a.Mtot / 32) + (f0 + 32 * q) / 32] = part;
+                        }
+                    }
+                } else if (KIND == GK_ROUTER) {
+                    const int f = f0 + 32 * q + lane;
+                    if (f < a.Mtot) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int col = c0 + j;
+                            if (col < tl.nrows) a.outf[(int64_t)(tl.row0 + col) * a.Mtot + f] = v[j];
                         }
                     }
                 } else {

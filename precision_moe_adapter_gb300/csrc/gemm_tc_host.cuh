@@ -53,8 +53,9 @@ bool launch_fmt(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st)
 {
     if (P <= 0) return true;
     CUtensorMap tm[4];   // token tiles in boxes of 256, 128, 64 and 32 rows
+    const int Kb = g.Kb ? g.Kb : g.K;
     for (int i = 0; i < 4; ++i)
-        if (!make_rows_tmap(&tm[i], g.A, P, g.K, 256 >> i)) return false;
+        if (!make_rows_tmap(&tm[i], g.A, P, Kb, 256 >> i)) return false;
     TcArgs a{};
     a.wq = g.wq;
     a.ws = g.ws;
@@ -64,6 +65,7 @@ bool launch_fmt(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st)
     a.Nst = g.Nst;
     a.w_off_elems = g.w_off_elems;
     a.K = g.K;
+    a.Kb = Kb;
     a.Mtot = g.Nout;
     a.m_tile = g.kind == GK_FWD_GU ? 64 : 128;
     a.tiles = g.tiles;
@@ -78,6 +80,7 @@ bool launch_fmt(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st)
     a.perm = g.perm;
     a.ht = g.ht;
     a.dtw_part = g.dtw_part;
+    a.outf = g.outf;
     a.err = err;
     switch (g.kind) {
     case GK_FWD_GU: return launch_kind<GK_FWD_GU, FMT>(tm, a, g.nmat, st);
@@ -87,6 +90,9 @@ bool launch_fmt(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st)
         return false;
     case GK_BWD_DX:
         if constexpr (FMT != kFmtBF16) return launch_kind<GK_BWD_DX, FMT>(tm, a, g.nmat, st);
+        return false;
+    case GK_ROUTER:
+        if constexpr (FMT == kFmtBF16) return launch_kind<GK_ROUTER, FMT>(tm, a, g.nmat, st);
         return false;
     }
     return false;

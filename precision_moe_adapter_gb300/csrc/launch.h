@@ -13,8 +13,11 @@ namespace pmoe {
 bool dims_ok(const pmoe_dims &d);
 
 // route_permute.cu
-void launch_logits_f32(int T, int d, int E, const uint16_t *X, const float *Wr, float *out,
-                       cudaStream_t st);
+// Wr [d, E] f32 -> WrT3 [E, 3d] bf16 with WrT3[e][s*d + c] the s-th term of
+// the exact three-term BF16 split of Wr[c][e]; and the router's token tiles.
+void launch_router_prep(int T, int d, int E, const float *Wr, uint16_t *WrT3, Tile *tiles,
+                        int32_t *chunk_tiles, int tile_rows, cudaStream_t st);
+int router_tile_rows(int T, int E, int num_sms);
 void launch_route_topk(int T, int E, int k, const float *logits, const float *bias, int32_t *idx,
                        float *w, float *logits_out, cudaStream_t st);
 size_t permute_ws_bytes(int P, int E);
@@ -41,7 +44,9 @@ void launch_cayley_grad(int nblk, int b, const float *S, const float *Rf, const 
                         float *dS, cudaStream_t st);
 
 // grouped GEMM (gemm_tc*.cu)
-enum GemmKind { GK_FWD_GU = 0, GK_FWD_DOWN = 1, GK_BWD_G = 2, GK_BWD_DX = 3 };
+// GK_ROUTER: FP32 logits X Wr with Wr split into three BF16 terms stacked
+// along K (A = [E, 3d]); the token operand X [T, d] is read three times.
+enum GemmKind { GK_FWD_GU = 0, GK_FWD_DOWN = 1, GK_BWD_G = 2, GK_BWD_DX = 3, GK_ROUTER = 4 };
 constexpr int kFmtBF16 = 3;  // weights already dequantized (scratch mode)
 struct GemmArgs {
     int kind;
@@ -54,6 +59,7 @@ struct GemmArgs {
     int64_t w_off_elems;     // element offset of the matrix inside a scratch slot
     const uint16_t *A;       // activations [P, K] bf16, expert-sorted rows
     int K;                   // contraction length
+    int Kb;                  // columns of A (the token operand); 0: K
     int Nout;                // output features
     const Tile *tiles;
     const int32_t *chunk_tiles;  // tile range [chunk_tiles[c0], chunk_tiles[c1])
@@ -66,10 +72,12 @@ struct GemmArgs {
     const int32_t *perm;
     const uint16_t *ht;      // BWD_G: h~ [P, I]
     float *dtw_part;         // BWD_G: [P, I/32]
+    float *outf;             // ROUTER: [P, Nout] f32
 };
 // tcgen05 grouped GEMM (returns false if the request cannot be
 // launched, e.g. the TMA descriptor could not be encoded)
 bool launch_gemm_tc(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st);
+int gemm_num_sms();   // SMs of the current device (cached)
 // counts / active / num_active of experts from row offsets [E+1]
 void launch_offsets_to_active(int E, int rows, const int32_t *offsets, int32_t *counts,
                               int32_t *active, int32_t *num_active, DevErr *err, cudaStream_t st);

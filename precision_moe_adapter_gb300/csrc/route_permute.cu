@@ -1,6 +1,8 @@
 // route_permute.cu -- router top-k and the grouping of (token, slot) pairs
 // by expert ("Active-expert-chunked dequantization", page 1, 技艺细节: the
 // router's selected experts are gathered into fixed-size batches).
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -336,59 +338,71 @@ void launch_offsets_to_active(int E, int rows, const int32_t *offsets, int32_t *
 }
 
 // ------------------------------------------------------------------ router logits
-// FP32 logits = X Wr on CUDA cores: 64 x 64 output tile per CTA, 4 x 4 per
-// thread, K step 32.  (X bf16 [T, d], Wr f32 [d, E].)
-__global__ void __launch_bounds__(256) k_logits_f32(int T, int d, int E,
-                                                    const uint16_t *__restrict__ X,
-                                                    const float *__restrict__ Wr,
-                                                    float *__restrict__ out)
+// On the tensor cores: Wr = hi + mid + lo exactly, with hi = bf16(Wr),
+// mid = bf16(Wr - hi), lo = bf16(Wr - hi - mid) (each difference is exact in
+// FP32, and the three terms hold all 24 bits of the FP32 value).  The
+// logits X Wr = [X | X | X] [hi; mid; lo] are then one BF16 contraction of
+// length 3d whose products are exact and whose sums are FP32.
+__global__ void __launch_bounds__(256) k_router_split(int d, int E, const float *__restrict__ Wr,
+                                                      uint16_t *__restrict__ WrT3)
 {
-    __shared__ float As[32][64 + 4];
-    __shared__ float Bs[32][64 + 4];
-    int t0 = blockIdx.y * 64, e0 = blockIdx.x * 64;
-    int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-    float acc[4][4] = {};
-    for (int k0 = 0; k0 < d; k0 += 32) {
-        for (int i = threadIdx.x; i < 64 * 32; i += 256) {
-            int r = i / 32, c = i % 32;
-            int t = t0 + r;
-            As[c][r] = t < T ? bf2f(X[(int64_t)t * d + k0 + c]) : 0.f;
-            int kk = i / 64, e = e0 + i % 64;
-            Bs[kk][i % 64] = e < E ? Wr[(int64_t)(k0 + kk) * E + e] : 0.f;
-        }
-        __syncthreads();
-#pragma unroll 8
-        for (int kk = 0; kk < 32; ++kk) {
-            float a[4], b[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-        }
-        __syncthreads();
+    __shared__ float t[32][33];
+    const int c0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    for (int i = ty; i < 32; i += 8) {
+        const int c = c0 + i, e = e0 + tx;
+        t[i][tx] = (c < d && e < E) ? Wr[(int64_t)c * E + e] : 0.f;
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        int t = t0 + ty * 4 + i;
-        if (t >= T) continue;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            int e = e0 + tx * 4 + j;
-            if (e < E) out[(int64_t)t * E + e] = acc[i][j];
-        }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+        const int e = e0 + i, c = c0 + tx;
+        if (e >= E || c >= d) continue;
+        const float w = t[tx][i];
+        const uint16_t hi = f2bf(w);
+        const float r1 = w - bf2f(hi);
+        const uint16_t mid = f2bf(r1);
+        const uint16_t lo = f2bf(r1 - bf2f(mid));
+        uint16_t *row = WrT3 + (int64_t)e * 3 * d;
+        row[c] = hi;
+        row[d + c] = mid;
+        row[2 * d + c] = lo;
     }
 }
 
-void launch_logits_f32(int T, int d, int E, const uint16_t *X, const float *Wr, float *out,
-                       cudaStream_t st)
+__global__ void k_router_tiles(int T, int rows, Tile *__restrict__ tiles, int32_t *__restrict__ chunk_tiles)
 {
-    if (T <= 0) return;
-    dim3 grid((unsigned)cdiv(E, 64), (unsigned)cdiv(T, 64));
-    k_logits_f32<<<grid, 256, 0, st>>>(T, d, E, X, Wr, out);
+    const int n = (T + rows - 1) / rows;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        Tile tl;
+        tl.expert = 0;
+        tl.row0 = i * rows;
+        tl.nrows = min(rows, T - i * rows);
+        tl.chunk = 0;
+        tiles[i] = tl;
+    }
+    if (threadIdx.x == 0) {
+        chunk_tiles[0] = 0;
+        chunk_tiles[1] = n;
+    }
+}
+
+// Token rows per tile: enough tiles to give every SM one work item (three
+// 128-expert feature tiles at E = 384), multiples of 16, at most 256.
+int router_tile_rows(int T, int E, int num_sms)
+{
+    const int64_t nft = cdiv(E, 128);
+    int64_t r = cdiv((int64_t)T * nft, num_sms > 0 ? num_sms : 1);
+    r = (r + 15) & ~(int64_t)15;
+    return (int)std::min<int64_t>(256, std::max<int64_t>(16, r));
+}
+
+void launch_router_prep(int T, int d, int E, const float *Wr, uint16_t *WrT3, Tile *tiles,
+                        int32_t *chunk_tiles, int tile_rows, cudaStream_t st)
+{
+    dim3 grid((unsigned)cdiv(d, 32), (unsigned)cdiv(E, 32));
+    k_router_split<<<grid, 256, 0, st>>>(d, E, Wr, WrT3);
+    note_launch();
+    k_router_tiles<<<1, 256, 0, st>>>(T, tile_rows, tiles, chunk_tiles);
     note_launch();
 }
 
