@@ -48,6 +48,26 @@ def parse():
     return ap.parse_args()
 
 
+def max_over_ranks(x: float) -> float:
+    """The largest x over all ranks (x itself outside a process group):
+    every rank times its own replica and the job takes the slowest."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    dev = (torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl"
+           else torch.device("cpu"))
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, steps: int, ms: float, world: int) -> float:
+    """Units per second of the whole job: every rank processed
+    units_per_rank per step, and the job took ms (max over ranks)."""
+    return world * units_per_rank * steps / (ms / 1e3)
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -321,14 +341,9 @@ def main():
     kt = {name: pmoe.pmoe_kernel_time(i) for i, name in enumerate(
         ("gemm_gate_up", "gemm_down", "gemm_bwd_g", "gemm_bwd_dx", "router"))}
     pmoe.pmoe_kernel_timing(False)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-        if dist.get_rank() != 0:
-            pass
+    ms = max_over_ranks(ms)
     ms_step = ms / args.steps
-    tokens_per_s = world * cfg.T * args.steps / (ms / 1e3)
+    tokens_per_s = whole_job_rate(cfg.T, args.steps, ms, world)
     P = cfg.P
     f_fwd, f_bwd = flops_of(cfg, P)
     pk = peaks()
@@ -370,13 +385,9 @@ def main():
             dXh.copy_(dX, non_blocking=True)
         ev1.record(stream)
         torch.cuda.synchronize()
-        e_ms = ev0.elapsed_time(ev1)
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(ev0.elapsed_time(ev1))
         nb = X.numel() * 2
-        e2e = {"value": world * cfg.T * args.steps / (e_ms / 1e3), "unit": "tokens/s",
+        e2e = {"value": whole_job_rate(cfg.T, args.steps, e_ms, world), "unit": "tokens/s",
                "h2d_bytes_per_step": 2 * nb, "d2h_bytes_per_step": 2 * nb,
                "ms_per_step": e_ms / args.steps}
 
