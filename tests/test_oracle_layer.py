@@ -328,6 +328,47 @@ def test_forward_rounding_points_against_torch():
     g, u = xt @ W13[:cfg.I].T, xt @ W13[cfg.I:].T
     h = r(g / (1 + np.exp(-g)) * u)
     ht = r(h @ _blockdiag(bf(Rd[0])))
-    want = ht @ W2.T
+    want = r(ht @ W2.T)              # each pair's output o is a BF16 tensor
     assert np.allclose(Y64, want, rtol=1e-12, atol=1e-12)
-    assert np.array_equal(bf(Y), r(want))
+    assert np.array_equal(bf(Y), want)
+
+
+def test_backward_rounding_points_against_torch():
+    """The backward of a BF16 training step: dh~, dg, du, dx~ and the
+    rotated dx are BF16 tensors, and the saved g, u are read back as BF16;
+    checked against a torch-rounded computation (one expert, k = 1, a
+    routing weight other than one)."""
+    import torch
+    cfg, (w13, s13, w2, s2) = _small(E=1, k=1, T=4)
+    X, dY = gi.gen_x(cfg), gi.gen_dy(cfg)
+    Su = gi.gen_skew(1, cfg.d, cfg.b, 0, "S_up", 0.05)
+    Sd = gi.gen_skew(1, cfg.I, cfg.b, 0, "S_down", 0.05)
+    rb = lambda S: gi.f32_to_bf16_bits(oracle.cayley(S.reshape(-1, cfg.b, cfg.b)).astype(np.float32)).reshape(S.shape)
+    Ru, Rd = rb(Su), rb(Sd)
+    L = oracle.Layer(cfg.T, cfg.d, 1, 1, cfg.I, cfg.b, cfg.fmt, w13, s13, w2, s2, R_up=Ru, R_down=Rd)
+    idx, w = np.zeros((cfg.T, 1), np.int32), np.full((cfg.T, 1), 0.75, np.float32)
+    ob = L.backward(X, dY, idx, w)
+    r = lambda a: torch.from_numpy(a).to(torch.bfloat16).to(torch.float64).numpy()
+    W13 = _dense(cfg.fmt, w13[0], s13[0], 2 * cfg.I, cfg.d)
+    Wg, Wu = W13[:cfg.I], W13[cfg.I:]
+    W2 = _dense(cfg.fmt, w2[0], s2[0], cfg.d, cfg.I)
+    BU, BD = _blockdiag(bf(Ru[0])), _blockdiag(bf(Rd[0]))
+    x = bf(X)
+    xt = r(x @ BU)
+    g, u = xt @ Wg.T, xt @ Wu.T
+    h = r(g / (1 + np.exp(-g)) * u)
+    ht = r(h @ BD)
+    G = bf(dY) @ W2
+    dht = r(0.75 * G)
+    dh = dht @ BD.T
+    gb, ub = r(g), r(u)
+    sg = 1 / (1 + np.exp(-gb))
+    dg = r(dh * ub * sg * (1 + gb * (1 - sg)))
+    du = r(dh * (gb / (1 + np.exp(-gb))))
+    dxt = r(dg @ Wg + du @ Wu)
+    dxp = r(dxt @ BU.T)
+    assert np.allclose(ob["dX64"], dxp, rtol=1e-12, atol=1e-12)
+    assert np.allclose(ob["d_topk_w"][:, 0], np.sum(G * ht, axis=1), rtol=1e-6)
+    nb = lambda a: a.reshape(cfg.T, -1, cfg.b)
+    assert np.allclose(ob["dR_up"][0], np.einsum("tbr,tbc->brc", nb(x), nb(dxt)), rtol=1e-12, atol=1e-12)
+    assert np.allclose(ob["dR_down"][0], np.einsum("tbr,tbc->brc", nb(h), nb(dht)), rtol=1e-12, atol=1e-12)
