@@ -153,6 +153,26 @@ def gen_matrix(fmt: int, E: int, N: int, K: int, seed: int, qsid: str, ssid: str
     return q, s
 
 
+def gen_fp8_matrix_on_device(E: int, N: int, K: int, seed: int, qsid: str, ssid: str, device):
+    """Full-size FP8 weights, drawn where the host recipe would take minutes
+    (tens of GB of codes): codes = E4M3(z), z ~ N(0, 1) from torch's seeded
+    device generator, one expert at a time; the FP32 block scales come from
+    the host stream exactly as in gen_matrix.  Returns (q uint8 [E, N, K] on
+    the device, s f32 [E, N/128, K/128] on the host).  The codes differ from
+    gen_matrix's (another generator), the distribution is the same."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(1_000_003 * seed + _SID[qsid])
+    q = torch.empty((E, N, K), dtype=torch.uint8, device=device)
+    for e in range(E):
+        z = torch.randn((N, K), generator=g, device=device, dtype=torch.float32)
+        q[e] = z.to(torch.float8_e4m3fn).view(torch.uint8)
+    rs = _rng(seed, ssid)
+    s = (rs.random((E, N // 128, K // 128), dtype=np.float32) * np.float32(0.015)
+         + np.float32(0.005)).astype(np.float32)
+    return q, s
+
+
 def gen_weights(cfg: LayerConfig):
     """(w13, s13, w2, s2): gate rows 0..I-1 and up rows I..2I-1 of w13."""
     w13, s13 = gen_matrix(cfg.fmt, cfg.E, 2 * cfg.I, cfg.d, cfg.seed, "w13", "s13")

@@ -20,7 +20,9 @@ from . import pmoe
 from .inputs import LayerConfig
 
 
-def _dev(a: np.ndarray, device) -> torch.Tensor:
+def _dev(a, device) -> torch.Tensor:
+    if isinstance(a, torch.Tensor):   # already a tensor (e.g. drawn on the device)
+        return a.to(device)
     t = torch.from_numpy(np.ascontiguousarray(a))
     if t.dtype == torch.uint16:
         t = t.view(torch.int16)

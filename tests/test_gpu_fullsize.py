@@ -1,0 +1,175 @@
+"""Parity at the full workload sizes, in the launch configuration the
+benchmark times: device Cayley map of the adapter parameters, device router,
+grouping, the fused chunked forward at the workload's chunk size and the
+backward-data pass.
+
+At these sizes the oracle cannot run the whole layer, so it computes
+sampled outputs one by one (each token's Y, dX and d_topk_w depend only on
+its own routing, and an expert's adapter gradient only on the pairs routed
+to it):
+  - routing: every token's logits within the FP32 bound and its selection
+    valid; selections equal to the oracle's wherever they are certified
+  - Y, dX, d_topk_w on sampled tokens whose routing equals the oracle's
+  - dR_up[e], dR_down[e] of sampled experts all of whose pairs are such tokens
+The oracle uses its own routing and its own (FP64) Cayley map; nothing it
+reads comes from the device path.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import assert_close, bits_to_f64, check_routing, t2np_bits
+from precision_moe_adapter_gb300 import build, pmoe
+from precision_moe_adapter_gb300 import inputs as gi
+from precision_moe_adapter_gb300.layer import DeviceLayer
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    build.build()
+    pmoe.lib()
+    oracle.build()
+
+
+def rbits(S, b):
+    return gi.f32_to_bf16_bits(oracle.cayley(S.reshape(-1, b, b)).astype(np.float32)).reshape(S.shape)
+
+
+def run_device(cfg, w13, s13, w2, s2, Wr, bias, Su, Sd, X, dY, chunks=None, backward=True,
+               pick=None):
+    """The benchmark's step on the device; returns host copies.  With
+    pick(out) -> tokens, a second backward runs with dY zero outside those
+    tokens, so its adapter gradients (dRu_s, dRd_s) hold their pairs only."""
+    L = DeviceLayer(cfg, w13, s13, w2, s2, Wr=Wr, bias=bias, S_up=Su, S_down=Sd)
+    rt = L.new_routing()
+    Xd = torch.from_numpy(X).view(torch.int16).cuda()
+    logits = torch.empty((cfg.T, cfg.E), dtype=torch.float32, device="cuda")
+    L.route(Xd, rt, logits)
+    L.permute(rt)
+    out = dict(logits=logits.cpu().numpy(), idx=rt.idx.cpu().numpy(), w=rt.w.cpu().numpy(),
+               counts=rt.counts.cpu().numpy())
+    Y = torch.empty_like(Xd)
+    ctx = torch.empty((cfg.P, 3 * cfg.I), dtype=torch.int16, device="cuda") if backward else None
+    out["Y"] = {}
+    for C in (chunks or [cfg.C]):
+        L.forward(Xd, rt, Y, C=C, mode=pmoe.MODE_FUSED, ctx=ctx)
+        out["Y"][C] = t2np_bits(Y)
+    if backward:
+        dX = torch.empty_like(Xd)
+        dtw = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device="cuda")
+        dRu, dRd = L.grads()
+        dYd = torch.from_numpy(dY).view(torch.int16).cuda()
+        L.backward(Xd, dYd, ctx, rt, dX, dtw, dRu, dRd, C=cfg.C)
+        out.update(dX=t2np_bits(dX), dtw=dtw.cpu().numpy(), dRu=dRu.cpu().numpy(),
+                   dRd=dRd.cpu().numpy())
+        if pick is not None:
+            toks = pick(out)
+            keep = torch.zeros(cfg.T, dtype=torch.bool, device="cuda")
+            keep[torch.from_numpy(toks).long().cuda()] = True
+            dYd = torch.where(keep[:, None], dYd, torch.zeros_like(dYd))
+            L.backward(Xd, dYd, ctx, rt, dX, dtw, dRu, dRd, C=cfg.C)
+            out.update(toks=toks, dRu_s=dRu.cpu().numpy(), dRd_s=dRd.cpu().numpy())
+    torch.cuda.synchronize()
+    assert L.status() == pmoe.PMOE_OK
+    del L
+    torch.cuda.empty_cache()
+    return out
+
+
+def sampled(exact, n, seed):
+    rng = np.random.default_rng(seed)
+    return np.sort(rng.choice(exact, size=min(n, len(exact)), replace=False))
+
+
+def sampled_disjoint(exact, idx, n, seed):
+    """Up to n tokens from `exact` whose expert sets are pairwise disjoint,
+    so each expert reached by the sample holds exactly one sampled pair."""
+    rng = np.random.default_rng(seed)
+    used, out = set(), []
+    for t in rng.permutation(exact):
+        ex = set(idx[t].tolist())
+        if ex & used:
+            continue
+        used |= ex
+        out.append(t)
+        if len(out) == n:
+            break
+    return np.sort(np.array(out, dtype=np.int32))
+
+
+@pytest.mark.parametrize("name", ["qwen3_30b_a3b", "kimi_k2", "deepseek_v3_mxfp4"])
+def test_full_size_step_on_sampled_tokens_and_experts(name):
+    cfg = gi.CONFIGS[name]
+    X, dY = gi.gen_x(cfg), gi.gen_dy(cfg)
+    w13, s13, w2, s2 = gi.gen_weights(cfg)
+    Wr, bias = gi.gen_router(cfg)
+    Su, Sd = gi.gen_adapter_params(cfg)
+    state = {}
+
+    def pick(out):
+        state["exact"] = check_routing(X, Wr, bias, cfg.k, out["logits"], out["idx"], out["w"])
+        return sampled_disjoint(state["exact"], out["idx"], 6, cfg.seed + 1)
+
+    g = run_device(cfg, w13, s13, w2, s2, Wr, bias, Su, Sd, X, dY, pick=pick)
+    assert int(g["counts"].sum()) == cfg.P
+    exact, toks = state["exact"], g["toks"]
+    assert len(exact) >= cfg.T - cfg.T // 100      # near-ties are rare
+
+    _, o_idx, o_w = oracle.route(X, Wr, bias, cfg.k)
+    OL = oracle.Layer(cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.b, cfg.fmt, w13, s13, w2, s2,
+                      R_up=rbits(Su, cfg.b), R_down=rbits(Sd, cfg.b))
+    _, Y64 = OL.forward(X, o_idx, o_w, toks=toks)
+    ob = OL.backward(X, dY, o_idx, o_w, toks=toks)
+    assert_close(bits_to_f64(g["Y"][cfg.C])[toks], Y64[toks], f"{name} Y")
+    assert_close(bits_to_f64(g["dX"])[toks], ob["dX64"][toks], f"{name} dX")
+    assert_close(g["dtw"][toks].astype(np.float64), ob["d_topk_w"][toks].astype(np.float64),
+                 f"{name} d_topk_w")
+    # adapter gradients of the sampled tokens' pairs (dY zero elsewhere;
+    # the sampled tokens share no expert, so each reached expert holds one
+    # pair's outer product): they match the oracle, every other expert is zero
+    assert len(toks) >= 4
+    hit = np.unique(o_idx[toks])
+    assert_close(g["dRu_s"][hit].astype(np.float64), ob["dR_up"][hit], f"{name} dR_up")
+    assert_close(g["dRd_s"][hit].astype(np.float64), ob["dR_down"][hit], f"{name} dR_down")
+    rest = np.setdiff1d(np.arange(cfg.E), hit)
+    assert not g["dRu_s"][rest].any() and not g["dRd_s"][rest].any()
+
+
+@pytest.mark.parametrize("fmt", [gi.INT4, gi.FP8])
+def test_decode_sweep_full_size(fmt):
+    """Kimi-K2 shape, forward only, T in {1, 8, 64, 512}: chunk sizes 8, 32
+    and all experts give bit-identical outputs; sampled tokens match the
+    oracle."""
+    base = gi.decode_config(1, fmt)
+    if fmt == gi.FP8:
+        q13, s13 = gi.gen_fp8_matrix_on_device(base.E, 2 * base.I, base.d, base.seed, "w13", "s13",
+                                               "cuda")
+        q2, s2 = gi.gen_fp8_matrix_on_device(base.E, base.d, base.I, base.seed, "w2", "s2", "cuda")
+        torch.cuda.synchronize()
+        w13, w2 = q13.cpu().numpy(), q2.cpu().numpy()
+        del q13, q2
+        torch.cuda.empty_cache()
+    else:
+        w13, s13, w2, s2 = gi.gen_weights(base)
+    Su, Sd = gi.gen_adapter_params(base)
+    Ru, Rd = rbits(Su, base.b), rbits(Sd, base.b)
+    OL = None
+    for T in (1, 8, 64, 512):
+        cfg = gi.decode_config(T, fmt)
+        X = gi.gen_x(cfg)
+        Wr, bias = gi.gen_router(cfg)
+        g = run_device(cfg, w13, s13, w2, s2, Wr, bias, Su, Sd, X, None,
+                       chunks=[8, 32, cfg.E], backward=False)
+        assert np.array_equal(g["Y"][8], g["Y"][32]) and np.array_equal(g["Y"][8], g["Y"][cfg.E])
+        exact = check_routing(X, Wr, bias, cfg.k, g["logits"], g["idx"], g["w"])
+        _, o_idx, o_w = oracle.route(X, Wr, bias, cfg.k)
+        OL = oracle.Layer(T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.b, cfg.fmt, w13, s13, w2, s2,
+                          R_up=Ru, R_down=Rd)
+        toks = sampled(exact, 3, T)
+        if len(toks) == 0:
+            continue
+        _, Y64 = OL.forward(X, o_idx, o_w, toks=toks)
+        assert_close(bits_to_f64(g["Y"][32])[toks], Y64[toks], f"decode T={T} fmt={fmt} Y")

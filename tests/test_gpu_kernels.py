@@ -9,7 +9,7 @@ import torch
 import oracle
 from precision_moe_adapter_gb300 import build, pmoe
 from precision_moe_adapter_gb300 import inputs as gi
-from helpers import assert_close, bits_to_f64, t2np_bits
+from helpers import assert_close, bits_to_f64, check_routing, t2np_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -141,38 +141,6 @@ def _gpu_route(cfg, X, Wr, bias):
     pmoe.moe_route(dm, dev(X), dev(Wr), None if bias is None else dev(bias), logits, idx, w, ws)
     torch.cuda.synchronize()
     return logits.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
-
-
-def check_routing(X, Wr, bias, k, g_logits, g_idx, g_w, toks=None):
-    """Logits within the FP32 bound; selections valid everywhere and equal
-    to the oracle's wherever the oracle's decision is certified unique.
-    Returns the tokens whose routing equals the oracle's exactly."""
-    o_logits, o_idx, o_w = oracle.route(X, Wr, bias, k, toks=toks)
-    T = X.shape[0]
-    toks = np.arange(T) if toks is None else np.asarray(toks)
-    x = bits_to_f64(X[toks])
-    beta = 1e-5 * (1.0 + np.abs(x) @ np.abs(Wr.astype(np.float64)))       # [n, E]
-    ol, gl = o_logits[toks].astype(np.float64), g_logits[toks].astype(np.float64)
-    assert np.all(np.abs(gl - ol) <= beta), np.max(np.abs(gl - ol) / beta)
-    exact = []
-    for n, t in enumerate(toks):
-        b2 = 2 * beta[n].max()
-        sel = g_idx[t]
-        assert len(set(sel.tolist())) == k
-        rest = np.setdiff1d(np.arange(Wr.shape[1]), sel)
-        if len(rest):
-            assert ol[n][sel].min() >= ol[n][rest].max() - b2
-        assert np.all(np.diff(ol[n][sel]) <= b2)
-        order = np.lexsort((np.arange(Wr.shape[1]), -ol[n]))
-        srt = ol[n][order]
-        gaps = -np.diff(srt[:min(k + 1, len(srt))])
-        if np.all(gaps > b2):
-            assert np.array_equal(sel, o_idx[t]), t
-        if np.array_equal(sel, o_idx[t]):
-            exact.append(t)
-            wb = 4 * b2 * g_w[t] + 2e-6
-            assert np.all(np.abs(g_w[t] - o_w[t]) <= wb)
-    return np.array(exact)
 
 
 @pytest.mark.parametrize("name,T", [("tiny", None), ("qwen3_30b_a3b", 256), ("kimi_k2", 96)])

@@ -192,7 +192,7 @@ def test_tiny_end_to_end_from_the_router():
     L.backward(Xd, dev(dY), ctx, rt, dX, None, *L.grads())
     torch.cuda.synchronize()
     assert L.status() == pmoe.PMOE_OK
-    from test_gpu_kernels import check_routing
+    from helpers import check_routing
     exact = check_routing(X, Wr, bias, cfg.k, logits.cpu().numpy(), rt.idx.cpu().numpy(),
                           rt.w.cpu().numpy())
     assert len(exact) >= cfg.T - 2
