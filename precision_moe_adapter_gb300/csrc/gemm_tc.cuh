@@ -90,8 +90,21 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
 }
 // Bounded wait: gives up after kWaitNs, records PMOE_ERR_TIMEOUT with the
 // waiting role and returns false (the caller then leaves its loop).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, DevErr *err, int where)
 {
+#ifdef PMOE_TEST_WAIT
+    if (mbar_test(bar, parity)) return true;
+#endif
     if (mbar_try(bar, parity)) return true;
     uint64_t t0 = globaltimer();
     while (true) {
@@ -161,6 +174,24 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, ui
         "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(
             d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(accum)
+        : "memory");
+}
+// The same two, called by a whole converged warp: one elected lane issues.
+// Keeping the warp converged lets the issue loop's operands stay uniform.
+__device__ __forceinline__ void umma_warp(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accum)
+{
+    asm volatile(
+        "{ .reg .pred e, p; elect.sync _|e, 0xffffffff; setp.ne.b32 p, %4, 0;\n"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accum)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit_warp(uint32_t bar)
+{
+    asm volatile(
+        "{ .reg .pred e; elect.sync _|e, 0xffffffff;\n"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0]; }" ::"r"(bar)
         : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar)
@@ -558,7 +589,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     const uint32_t bar0 = sB0 + kStages * kBBytes;
     uint32_t *tmem_slot = (uint32_t *)(smem + PP::kBarOff + 8 * PP::kNumBars);
     auto full_a = [&](int s) { return bar0 + 8 * s; };
-    auto full_b = [&](int s) { return bar0 + 8 * (kStages + s); };
     auto empty = [&](int s) { return bar0 + 8 * (2 * kStages + s); };
     auto tfull = [&](int c) { return bar0 + 8 * (3 * kStages + c); };
     auto tempty = [&](int c) { return bar0 + 8 * (3 * kStages + 2 + c); };
@@ -574,8 +604,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(full_a(s), PP::kBf16 ? 1 : PP::kTmaRaw ? kDqWarps / kConvGroups : kDqWarps);
-            mbar_init(full_b(s), 1);
+            // one barrier per stage: the converter warps of the stage's group
+            // and the token producer's arrive with the stage's TMA bytes
+            mbar_init(full_a(s), PP::kBf16 ? 1 : kDqWarps / kConvGroups + 1);
             mbar_init(empty(s), 1);
         }
         for (int c = 0; c < 2; ++c) {
@@ -684,18 +715,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                 const uint32_t ph = (g / kStages) & 1;
                 if (!(ok = mbar_wait(empty(s), ph ^ 1, a.err, 1))) break;
                 if (lane == 0) {
-                    mbar_expect_tx(full_b(s), brows * kBK * 2);
+                    mbar_expect_tx(full_a(s), brows * kBK * 2 + (PP::kBf16 ? kABytes : 0));
                     for (int r0 = 0; r0 < brows;) {
                         const int left = brows - r0;
                         const CUtensorMap *tm = left >= 256 ? &tmB256 : left >= 128 ? &tmB128
                                               : left >= 64 ? &tmB64 : &tmB32;
                         const int rows = left >= 256 ? 256 : left >= 128 ? 128 : left >= 64 ? 64 : 32;
                         const int xb = KIND == GK_ROUTER ? (ks * kBK) % a.Kb : ks * kBK;
-                        tma_load_2d(sB0 + s * kBBytes + r0 * kBK * 2, tm, xb, tl.row0 + r0, full_b(s));
+                        tma_load_2d(sB0 + s * kBBytes + r0 * kBK * 2, tm, xb, tl.row0 + r0, full_a(s));
                         r0 += rows;
                     }
                     if constexpr (PP::kBf16) {
-                        mbar_expect_tx(full_a(s), kABytes);
                         const int slot = (int)widx;
                         if (KIND == GK_FWD_GU) {
                             // A rows 32q .. 32q+15: gate f0+16q ..; 32q+16 .. 32q+31: up
@@ -714,35 +744,43 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             }
         }
     } else if (warp == kMmaWarp) {
-        // ---------------- MMA issuer
-        if (lane == 0) {
+        // ---------------- MMA issuer (the whole warp runs the loop; one
+        // elected lane issues each MMA and commit)
+        {
             uint32_t g = 0, li = 0;
             bool ok = true;
+            // descriptors of stage 0; a stage or K step moves only the start
+            // address field (address / 16, bits 0-13), so they are plain adds
+            const uint64_t adesc0 = PP::kTrans ? sdesc_mn(sA0) : sdesc(sA0);
+            const uint64_t bdesc0 = sdesc(sB0);
+            constexpr uint32_t kAStep = PP::kTrans ? 4096 >> 4 : 32 >> 4;   // per K step of 16
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++li) {
                 const Tile tl = a.tiles[tbeg + item / nft];
                 const int N = (tl.nrows + 15) & ~15;
                 const uint32_t idesc = idesc_bf16(kM, N, PP::kTrans);
                 const int acc = li & 1;
-                if (!(ok = mbar_wait(tempty(acc), ((li >> 1) & 1) ^ 1, a.err, 2))) break;
+                // every lane waits; the outcome is made warp-uniform so that the
+                // lanes stay converged for the elected issue
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(tempty(acc), ((li >> 1) & 1) ^ 1, a.err, 2))))
+                    break;
                 tc_fence_after();
                 const uint32_t d = tmem + acc * (kTmemCols / 2);
                 for (int ks = 0; ks < nk; ++ks, ++g) {
                     const int s = g % kStages;
                     const uint32_t ph = (g / kStages) & 1;
-                    if (!(ok = mbar_wait(full_a(s), ph, a.err, 3))) break;
-                    if (!(ok = mbar_wait(full_b(s), ph, a.err, 4))) break;
+                    if (!(ok = __all_sync(0xffffffffu, mbar_wait(full_a(s), ph, a.err, 3)))) break;
                     tc_fence_after();
+                    // K step of 16: +32 B inside the K-major swizzle row, or two
+                    // 8-row K groups (2 x 2048 B) of the MN-major tile
+                    const uint64_t ad = adesc0 + (uint32_t)(s * (kABytes >> 4));
+                    const uint64_t bd = bdesc0 + (uint32_t)(s * (kBBytes >> 4));
+                    umma_warp(d, ad, bd, idesc, ks != 0);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        // K step of 16: +32 B inside the K-major swizzle row, or
-                        // two 8-row K groups (2 x 2048 B) of the MN-major tile
-                        const uint64_t ad = PP::kTrans ? sdesc_mn(sA0 + s * kABytes + kk * 4096)
-                                                       : sdesc(sA0 + s * kABytes + kk * 32);
-                        umma(d, ad, sdesc(sB0 + s * kBBytes + kk * 32), idesc, (ks | kk) != 0);
-                    }
-                    umma_commit(empty(s));
+                    for (int kk = 1; kk < kBK / 16; ++kk)
+                        umma_warp(d, ad + kk * kAStep, bd + kk * (32 >> 4), idesc, 1u);
+                    umma_commit_warp(empty(s));
                 }
-                if (ok) umma_commit(tfull(acc));
+                if (ok) umma_commit_warp(tfull(acc));
             }
         }
     } else if (warp >= kDqWarp0) {
