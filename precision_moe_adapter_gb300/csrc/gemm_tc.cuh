@@ -45,7 +45,10 @@ constexpr int kRawWarp = 4;                  // packed weight tiles + scale word
 constexpr int kMmaWarp = 5;
 constexpr int kBWarp = 6;                    // token tiles (and BF16 weight tiles)
 constexpr int kDqWarp0 = 7;
-constexpr int kDqWarps = 16;
+#ifndef PMOE_DQ_WARPS
+#define PMOE_DQ_WARPS 16
+#endif
+constexpr int kDqWarps = PMOE_DQ_WARPS;
 #ifndef PMOE_CONV_GROUPS
 #define PMOE_CONV_GROUPS 2
 #endif
@@ -90,21 +93,8 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
 }
 // Bounded wait: gives up after kWaitNs, records PMOE_ERR_TIMEOUT with the
 // waiting role and returns false (the caller then leaves its loop).
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, DevErr *err, int where)
 {
-#ifdef PMOE_TEST_WAIT
-    if (mbar_test(bar, parity)) return true;
-#endif
     if (mbar_try(bar, parity)) return true;
     uint64_t t0 = globaltimer();
     while (true) {
@@ -330,11 +320,20 @@ struct Pipe {
     static constexpr bool kBf16 = FMT == kFmtBF16;
     static constexpr bool kTmaRaw = !kBf16;
     static constexpr bool kFp8 = FMT == PMOE_W_FP8_B128_F32;
-#ifdef PMOE_AB_STAGES
-    static constexpr int kStagesAB = kFp8 ? 3 : PMOE_AB_STAGES;
+    // A (converted weights, 16 KB) and B (token tiles, up to 32 KB) rings of
+    // different depths: the converters may run kStagesA steps ahead of the
+    // MMA, the token producer kStagesB steps (kStagesB <= kStagesA)
+#ifdef PMOE_A_STAGES
+    static constexpr int kStagesA = kFp8 ? 3 : PMOE_A_STAGES;
 #else
-    static constexpr int kStagesAB = kFp8 ? 3 : 4;
+    static constexpr int kStagesA = kFp8 ? 3 : 4;
 #endif
+#ifdef PMOE_B_STAGES
+    static constexpr int kStagesB = kFp8 ? 3 : PMOE_B_STAGES;
+#else
+    static constexpr int kStagesB = kFp8 ? 3 : 4;
+#endif
+    static_assert(kStagesB <= kStagesA, "token ring no deeper than the weight ring");
     static constexpr int kRawRows = kTrans ? 64 : 128;
     static constexpr int kRowBytes = kTrans ? (kFp8 ? 128 : 64) : (kFp8 ? 64 : 32);
     static constexpr int kScaleOff = kRawRows * kRowBytes;   // scale words after the data
@@ -345,8 +344,8 @@ struct Pipe {
     static constexpr int kRawTma = kFp8 ? 8 : 6;   // raw ring stages
 #endif
     static constexpr int kRawBytes = kTmaRaw ? kRawTma * kRawTile : 0;
-    static constexpr int kNumBars = 3 * kStagesAB + 4 + 2 * kRawTma;
-    static constexpr int kBarOff = kStagesAB * (kABytes + kBBytes);
+    static constexpr int kNumBars = 2 * kStagesA + 4 + 2 * kRawTma;
+    static constexpr int kBarOff = kStagesA * kABytes + kStagesB * kBBytes;
     static constexpr int kBarBytes = 8 * kNumBars + 16;
     static constexpr int kRawOff = (kBarOff + kBarBytes + 1023) & ~1023;
     static constexpr size_t kSmem = (size_t)kRawOff + kRawBytes + 1024;
@@ -581,19 +580,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                                                          const TcArgs a)
 {
     using PP = Pipe<KIND, FMT>;
-    constexpr int kStages = PP::kStagesAB;
+    constexpr int kStages = PP::kStagesA;    // weight ring; step g uses A slot g % kStages
+    constexpr int kStagesB = PP::kStagesB;   // token ring; step g uses B slot g % kStagesB
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sA0 = smem_u32(smem);
     const uint32_t sB0 = sA0 + kStages * kABytes;
-    const uint32_t bar0 = sB0 + kStages * kBBytes;
+    const uint32_t bar0 = sB0 + kStagesB * kBBytes;
     uint32_t *tmem_slot = (uint32_t *)(smem + PP::kBarOff + 8 * PP::kNumBars);
+    // full_a(s): step g's A and B are in place (s = g % kStages); empty(s):
+    // the MMAs of the step that last used A slot s have completed
     auto full_a = [&](int s) { return bar0 + 8 * s; };
-    auto empty = [&](int s) { return bar0 + 8 * (2 * kStages + s); };
-    auto tfull = [&](int c) { return bar0 + 8 * (3 * kStages + c); };
-    auto tempty = [&](int c) { return bar0 + 8 * (3 * kStages + 2 + c); };
-    auto raw_full = [&](int r) { return bar0 + 8 * (3 * kStages + 4 + r); };
-    auto raw_empty = [&](int r) { return bar0 + 8 * (3 * kStages + 4 + PP::kRawTma + r); };
+    auto empty = [&](int s) { return bar0 + 8 * (kStages + s); };
+    auto tfull = [&](int c) { return bar0 + 8 * (2 * kStages + c); };
+    auto tempty = [&](int c) { return bar0 + 8 * (2 * kStages + 2 + c); };
+    auto raw_full = [&](int r) { return bar0 + 8 * (2 * kStages + 4 + r); };
+    auto raw_empty = [&](int r) { return bar0 + 8 * (2 * kStages + 4 + PP::kRawTma + r); };
     const uint32_t raw0 = smem_u32(smem + PP::kRawOff);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -711,9 +713,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             (void)f0;
             (void)widx;
             for (int ks = 0; ks < nk; ++ks, ++g) {
-                const int s = g % kStages;
-                const uint32_t ph = (g / kStages) & 1;
-                if (!(ok = mbar_wait(empty(s), ph ^ 1, a.err, 1))) break;
+                const int s = g % kStages, sb = g % kStagesB;
+                // B slot sb was last read by step g - kStagesB: wait for its
+                // MMAs (which also frees A slot s for the BF16 weight tiles)
+                if (g >= (uint32_t)kStagesB) {
+                    const uint32_t gp = g - kStagesB;
+                    if (!(ok = mbar_wait(empty(gp % kStages), (gp / kStages) & 1, a.err, 1))) break;
+                }
                 if (lane == 0) {
                     mbar_expect_tx(full_a(s), brows * kBK * 2 + (PP::kBf16 ? kABytes : 0));
                     for (int r0 = 0; r0 < brows;) {
@@ -722,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                                               : left >= 64 ? &tmB64 : &tmB32;
                         const int rows = left >= 256 ? 256 : left >= 128 ? 128 : left >= 64 ? 64 : 32;
                         const int xb = KIND == GK_ROUTER ? (ks * kBK) % a.Kb : ks * kBK;
-                        tma_load_2d(sB0 + s * kBBytes + r0 * kBK * 2, tm, xb, tl.row0 + r0, full_a(s));
+                        tma_load_2d(sB0 + sb * kBBytes + r0 * kBK * 2, tm, xb, tl.row0 + r0, full_a(s));
                         r0 += rows;
                     }
                     if constexpr (PP::kBf16) {
@@ -773,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                     // K step of 16: +32 B inside the K-major swizzle row, or two
                     // 8-row K groups (2 x 2048 B) of the MN-major tile
                     const uint64_t ad = adesc0 + (uint32_t)(s * (kABytes >> 4));
-                    const uint64_t bd = bdesc0 + (uint32_t)(s * (kBBytes >> 4));
+                    const uint64_t bd = bdesc0 + (uint32_t)((g % kStagesB) * (kBBytes >> 4));
                     umma_warp(d, ad, bd, idesc, ks != 0);
 #pragma unroll
                     for (int kk = 1; kk < kBK / 16; ++kk)
