@@ -289,7 +289,9 @@ def main():
             e.record()
             phase_ev.append((name, e))
 
-    def step(Xs, dYs, timed=False):
+    def step(Xs, dYs, timed=False, Yo=None, dXo=None):
+        Yo = Y if Yo is None else Yo
+        dXo = dX if dXo is None else dXo
         mark("cayley", timed)
         if L.S_up is not None:   # R = Cayley(S) for the adapter of this step
             pmoe.adapter_cayley(L.S_up.numel() // (b * b), b, L.S_up, L.R_up, L.Rf_up)
@@ -299,9 +301,9 @@ def main():
         mark("permute", timed)
         L.permute(rt)
         mark("forward", timed)
-        L.forward(Xs, rt, Y, C=cfg.C, mode=mode, ctx=ctx)
+        L.forward(Xs, rt, Yo, C=cfg.C, mode=mode, ctx=ctx)
         mark("backward", timed)
-        L.backward(Xs, dYs, ctx, rt, dX, dtw, dRu, dRd, C=cfg.C)
+        L.backward(Xs, dYs, ctx, rt, dXo, dtw, dRu, dRd, C=cfg.C)
         mark("cayley_grad", timed)
         if L.S_up is not None:
             pmoe.adapter_cayley_grad(L.S_up.numel() // (b * b), b, L.S_up, L.Rf_up, dRu, dSu)
@@ -368,21 +370,48 @@ def main():
     # ---- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
+        # every step copies its X and dY in from pinned host memory and its Y
+        # and dX back out; the copies run on their own stream, double-buffered,
+        # so step i's copies overlap the compute of steps i-1 and i+1
         Xh = torch.from_numpy(host["X"]).view(torch.int16).pin_memory()
         dYh = torch.from_numpy(host["dY"]).view(torch.int16).pin_memory()
-        Yh = torch.empty_like(Xh).pin_memory()
-        dXh = torch.empty_like(Xh).pin_memory()
-        Xd, dYd = torch.empty_like(X), torch.empty_like(dY)
+        Yh = [torch.empty_like(Xh).pin_memory() for _ in range(2)]
+        dXh = [torch.empty_like(Xh).pin_memory() for _ in range(2)]
+        Xd = [torch.empty_like(X) for _ in range(2)]
+        dYd = [torch.empty_like(dY) for _ in range(2)]
+        Yd = [torch.empty_like(Y) for _ in range(2)]
+        dXd = [torch.empty_like(dX) for _ in range(2)]
+        cs = torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
         ev0.record(stream)
-        for _ in range(args.steps):
-            Xd.copy_(Xh, non_blocking=True)
-            dYd.copy_(dYh, non_blocking=True)
-            step(Xd, dYd)
-            Yh.copy_(Y, non_blocking=True)
-            dXh.copy_(dX, non_blocking=True)
+        cs.wait_stream(stream)
+        with torch.cuda.stream(cs):
+            Xd[0].copy_(Xh, non_blocking=True)
+            dYd[0].copy_(dYh, non_blocking=True)
+            ev_in[0].record(cs)
+        for i in range(args.steps):
+            bi = i % 2
+            stream.wait_event(ev_in[bi])
+            if i >= 2:
+                stream.wait_event(ev_out[bi])      # step i-2's outputs are out
+            step(Xd[bi], dYd[bi], Yo=Yd[bi], dXo=dXd[bi])
+            ev_done[bi].record(stream)
+            with torch.cuda.stream(cs):
+                if i + 1 < args.steps:             # buffer (i+1)%2 was freed by step i-1
+                    nb_ = (i + 1) % 2
+                    Xd[nb_].copy_(Xh, non_blocking=True)
+                    dYd[nb_].copy_(dYh, non_blocking=True)
+                    ev_in[nb_].record(cs)
+                cs.wait_event(ev_done[bi])
+                Yh[bi].copy_(Yd[bi], non_blocking=True)
+                dXh[bi].copy_(dXd[bi], non_blocking=True)
+                ev_out[bi].record(cs)
+        stream.wait_stream(cs)
         ev1.record(stream)
         torch.cuda.synchronize()
         e_ms = max_over_ranks(ev0.elapsed_time(ev1))
