@@ -151,6 +151,100 @@ __global__ void __launch_bounds__(128) k_cayley_warp(int nblk, const float *__re
     }
 }
 
+// b = 64 with two warps per block matrix (32 rows each), so a lane keeps
+// 8 x 8 elements (about 100 registers instead of 255) and four times as
+// many warps fit an SM.  Lane (row group rg = lane / 8, column group
+// cg = lane % 8) of warp half h keeps rows 32h + 8rg .. +7, columns
+// 8cg .. +7.  For pivot k the warp holding row k scales it and puts it in
+// shared memory (double-buffered, one 64-thread barrier per pivot); the
+// column-k values come by shuffles inside each warp.  Operation for
+// operation this is the same elimination as above (identical results).
+__global__ void __launch_bounds__(128) k_cayley_pair64(int nblk, const float *__restrict__ S,
+                                                       uint16_t *__restrict__ Rb,
+                                                       float *__restrict__ Rf)
+{
+    constexpr int B = 64;
+    __shared__ __align__(16) float prow[2][2][B + 4];   // [matrix][buffer][64 + p]
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int mloc = w >> 1, half = w & 1;
+    const int blk = blockIdx.x * 2 + mloc;
+    const bool live = blk < nblk;   // both warps of a matrix agree
+    const int rg = lane >> 3, cg = lane & 7;
+    const int64_t off = (int64_t)(live ? blk : 0) * B * B;
+    float v[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int row = 32 * half + 8 * rg + i;
+#pragma unroll
+        for (int j = 0; j < 8; j += 4) {
+            const int col = 8 * cg + j;
+            const float4 sv = live ? *(const float4 *)(S + off + row * B + col) : make_float4(0, 0, 0, 0);
+            v[i][j] = (row == col ? 1.f : 0.f) - sv.x;
+            v[i][j + 1] = (row == col + 1 ? 1.f : 0.f) - sv.y;
+            v[i][j + 2] = (row == col + 2 ? 1.f : 0.f) - sv.z;
+            v[i][j + 3] = (row == col + 3 ? 1.f : 0.f) - sv.w;
+        }
+    }
+    for (int kb = 0; kb < 8; ++kb) {       // pivots k = 8 kb .. 8 kb + 7
+        const int owner = kb >> 2, g = kb & 3;
+        const bool in_g = half == owner && rg == g;
+        const bool in_h = cg == kb;
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+            const int k = 8 * kb + jj;
+            float *pr = prow[mloc][k & 1];
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = __shfl_sync(0xffffffffu, v[i][jj], (lane & ~7) | kb);
+            if (half == owner) {
+                const float piv = __shfl_sync(0xffffffffu, v[jj][jj], (g << 3) | kb);
+                const float p = 1.f / piv;
+                if (rg == g) {
+                    *(float4 *)(pr + 8 * cg) =
+                        make_float4(v[jj][0] * p, v[jj][1] * p, v[jj][2] * p, v[jj][3] * p);
+                    *(float4 *)(pr + 8 * cg + 4) =
+                        make_float4(v[jj][4] * p, v[jj][5] * p, v[jj][6] * p, v[jj][7] * p);
+                    if (cg == kb) pr[B] = p;
+                }
+            }
+            asm volatile("bar.sync %0, 64;" ::"r"(1 + mloc) : "memory");
+            const float4 q0 = *(const float4 *)(pr + 8 * cg), q1 = *(const float4 *)(pr + 8 * cg + 4);
+            const float p = pr[B];
+            const float ps[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+            if (in_g) f[jj] = 0.f;   // the pivot row is only rescaled
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[i][j] = fmaf(-f[i], ps[j], v[i][j]);
+            if (in_g) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[jj][j] = ps[j];
+            }
+            if (in_h) {   // column k becomes column k of the inverse
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i][jj] = fmaf(-f[i], p, 0.f);
+                if (in_g) v[jj][jj] = p;
+            }
+        }
+    }
+    if (!live) return;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int row = 32 * half + 8 * rg + i;
+        float r[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) r[j] = 2.f * v[i][j] - (row == 8 * cg + j ? 1.f : 0.f);
+        if (Rf) {
+            *(float4 *)(Rf + off + row * B + 8 * cg) = make_float4(r[0], r[1], r[2], r[3]);
+            *(float4 *)(Rf + off + row * B + 8 * cg + 4) = make_float4(r[4], r[5], r[6], r[7]);
+        }
+        if (Rb)
+            *(uint4 *)(Rb + off + row * B + 8 * cg) =
+                make_uint4(pack_bf2(r[0], r[1]), pack_bf2(r[2], r[3]), pack_bf2(r[4], r[5]),
+                           pack_bf2(r[6], r[7]));
+    }
+}
+
 // Small blocks (b <= 8): one thread per block matrix, the same in-place
 // elimination in registers.
 template <int B>
@@ -346,7 +440,9 @@ static void cayley_b(int nblk, const float *S, uint16_t *Rb, float *Rf, cudaStre
 {
     if constexpr (B < 16)
         k_cayley_small<B><<<(int)cdiv(nblk, 128), 128, 0, st>>>(nblk, S, Rb, Rf);
-    else if constexpr (B <= 64)
+    else if constexpr (B == 64)
+        k_cayley_pair64<<<(int)cdiv(nblk, 2), 128, 0, st>>>(nblk, S, Rb, Rf);
+    else if constexpr (B <= 32)
         k_cayley_warp<B><<<(int)cdiv(nblk, 4), 128, 0, st>>>(nblk, S, Rb, Rf);
     else
         k_cayley<B><<<nblk, 4 * B, 0, st>>>(S, Rb, Rf);

@@ -41,10 +41,16 @@ constexpr int kABytes = kM * kBK * 2;        // 16 KB
 constexpr int kBBytes = kNmax * kBK * 2;     // 32 KB
 constexpr int kBoxRows = 32;                 // smallest TMA box: 32 token rows x 64 K
 constexpr int kEpiWarps = 4;
-constexpr int kRawWarp = 4;                  // packed weight tiles + scale words
+#ifndef PMOE_PROD_SPLIT
+#define PMOE_PROD_SPLIT 2
+#endif
+// producers: kProd warps for the weight tiles and kProd for the token tiles;
+// producer warp p of a kind takes the K steps g = p (mod kProd)
+constexpr int kProd = PMOE_PROD_SPLIT;
+constexpr int kRawWarp = 4;                  // packed weight tiles + scale words: warps 4, 7, ...
 constexpr int kMmaWarp = 5;
-constexpr int kBWarp = 6;                    // token tiles (and BF16 weight tiles)
-constexpr int kDqWarp0 = 7;
+constexpr int kBWarp = 6;                    // token tiles (and BF16 weight tiles): warps 6, 8, ...
+constexpr int kDqWarp0 = 5 + 2 * kProd;
 #ifndef PMOE_DQ_WARPS
 #define PMOE_DQ_WARPS 16
 #endif
@@ -634,7 +640,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *(volatile uint32_t *)tmem_slot;
 
-    if (warp == kRawWarp) {
+    const bool raw_prod = warp == kRawWarp || (kProd > 1 && warp == 7);
+    const bool b_prod = warp == kBWarp || (kProd > 1 && warp == 8);
+    const uint32_t prod_part = (kProd > 1 && (warp == 7 || warp == 8)) ? 1u : 0u;
+    if (raw_prod) {
         // ---------------- weight producer: packed weight tiles (TMA) with
         // their scale words (cp.async by the 32 lanes).  It runs ahead of
         // the token producer by up to the depth of the raw ring, so HBM
@@ -647,6 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                 const int f0 = (item % nft) * a.m_tile;
                 const int64_t widx = a.slot_index ? (tl.chunk & 0xffff) : tl.expert;
                 for (int ks = 0; ks < nk; ++ks, ++g) {
+                    if (kProd > 1 && g % kProd != prod_part) continue;
                     const int r = g % PP::kRawTma;
                     if (!(ok = mbar_wait(raw_empty(r), ((g / PP::kRawTma) & 1) ^ 1, a.err, 7))) break;
                     const uint32_t dst = raw0 + r * PP::kRawTile;
@@ -699,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                 }
             }
         }
-    } else if (warp == kBWarp) {
+    } else if (b_prod) {
         // ---------------- token producer: token tiles (TMA), or BF16 weight
         // tiles (TMA into the swizzled A stage)
         uint32_t g = 0;
@@ -713,6 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             (void)f0;
             (void)widx;
             for (int ks = 0; ks < nk; ++ks, ++g) {
+                if (kProd > 1 && g % kProd != prod_part) continue;
                 const int s = g % kStages, sb = g % kStagesB;
                 // B slot sb was last read by step g - kStagesB: wait for its
                 // MMAs (which also frees A slot s for the BF16 weight tiles)
