@@ -97,6 +97,10 @@ def _declare(L):
     L.or_adapter_apply.argtypes = [_i, _i, _i, _p, _p, _p]
     L.or_adapter_grad.argtypes = [_i, _i, _i, _p, _p, _p, _p, _p]
     L.or_cayley.argtypes = [_i, _i, _p, _p]
+    L.or_dense_forward.argtypes = [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _i, _p, _p]
+    L.or_dense_forward.restype = None
+    L.or_dense_backward.argtypes = [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _i, _p, _p, _p]
+    L.or_dense_backward.restype = None
     L.or_cayley.restype = _i
     L.or_cayley_grad.argtypes = [_i, _i, _p, _p, _p]
     L.or_cayley_grad.restype = _i
@@ -229,6 +233,42 @@ def adapter_grad(X, dXr, R, b: int, want_dx: bool = True):
     dR = np.empty((dim // b, b, b), np.float64)
     _L().or_adapter_grad(rows, dim, b, _ptr(X), _ptr(dXr), _ptr(R), _ptr(dX), _ptr(dR))
     return dX, dR
+
+
+# ---------------------------------------------------------------- dense linear
+
+def dense_forward(fmt, q, s, N, K, b, R, X, no_round=False, R64=None, X64=None):
+    """Dense bypass-base-weight-grad linear with the OFT adapter (see
+    or_dense_forward).  q/s: one packed [N, K] matrix; R: BF16 bits
+    [K/b, b, b] or None (R64: doubles instead).  X: BF16 bits [rows, K]
+    (or X64 doubles).  Returns (Y bf16 bits [rows, N], Y64)."""
+    q = _c(q, np.uint8)
+    s = np.ascontiguousarray(s)
+    R, R64, X64 = _c(R, np.uint16), _c(R64, np.float64), _c(X64, np.float64)
+    X = _c(X, np.uint16)
+    rows = (X if X is not None else X64).shape[0]
+    Y = np.zeros((rows, N), np.uint16)
+    Y64 = np.zeros((rows, N), np.float64)
+    _L().or_dense_forward(rows, N, K, b, fmt, _ptr(q), _ptr(s), _ptr(R), _ptr(R64), _ptr(X),
+                          _ptr(X64), NO_ROUND if no_round else 0, _ptr(Y), _ptr(Y64))
+    return Y, Y64
+
+
+def dense_backward(fmt, q, s, N, K, b, R, X, dY, no_round=False, R64=None, X64=None):
+    """Backward-data of the dense linear: dict(dX bf16 bits, dX64, dR double
+    [K/b, b, b] or None)."""
+    q = _c(q, np.uint8)
+    s = np.ascontiguousarray(s)
+    R, R64, X64 = _c(R, np.uint16), _c(R64, np.float64), _c(X64, np.float64)
+    X, dY = _c(X, np.uint16), _c(dY, np.uint16)
+    rows = dY.shape[0]
+    dX = np.zeros((rows, K), np.uint16)
+    dX64 = np.zeros((rows, K), np.float64)
+    dR = None if R is None and R64 is None else np.zeros((K // b, b, b), np.float64)
+    _L().or_dense_backward(rows, N, K, b, fmt, _ptr(q), _ptr(s), _ptr(R), _ptr(R64), _ptr(X),
+                           _ptr(X64), _ptr(dY), NO_ROUND if no_round else 0, _ptr(dX),
+                           _ptr(dX64), _ptr(dR))
+    return dict(dX=dX, dX64=dX64, dR=dR)
 
 
 # ---------------------------------------------------------------- layer

@@ -800,6 +800,91 @@ void or_backward(const or_layer *L, const uint16_t *X, const double *X64, const 
     free(xs); free(dxts); free(hs); free(dhts);
 }
 
+/*
+ * Dense bypass-base-weight-grad linear with the OFT adapter: one frozen
+ * low-precision projection outside the experts ("Orbit ... 技艺细节": the
+ * frozen base needs no weight gradient; "Orbit：把万亿模型 RL 后训练改写成部署
+ * 一致性问题", 机制拆解: the adapter is a local orthogonal transform of the
+ * activations).  W is [N, K] in the packed format fmt, R (nullable) is one
+ * block-diagonal rotation [K/b, b, b] (BF16 bits, or doubles in R64).
+ *   forward:  x~ = bf16(x R);  y = x~ W^T;  Y = bf16(y)
+ *   backward: G = dY W;  dx~ = bf16(G);  dR = sum_rows x_blk^T dx~_blk;
+ *             dX = bf16(dx~ R^T)        (without R: dX = bf16(G))
+ * Rounding points as in the layer (OR_NO_ROUND removes them); X64 replaces
+ * the BF16 input for finite differences.
+ */
+void or_dense_forward(int rows, int N, int K, int b, int fmt, const uint8_t *q, const void *s,
+                      const uint16_t *R, const double *R64, const uint16_t *X, const double *X64,
+                      int flags, uint16_t *Y, double *Y64)
+{
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < rows; ++i) {
+        double *x = malloc(sizeof(double) * (size_t)K * 2), *xt = x + K;
+        for (int c = 0; c < K; ++c)
+            x[c] = X64 ? X64[(int64_t)i * K + c] : or_bf16_to_double(X[(int64_t)i * K + c]);
+        if (R || R64) {
+            rotate_row64(x, R, R64, K, b, xt);
+            for (int c = 0; c < K; ++c)
+                xt[c] = rbf(xt[c], flags);
+        } else {
+            memcpy(xt, x, sizeof(double) * (size_t)K);
+        }
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int c = 0; c < K; ++c)
+                acc += xt[c] * dequant_elem(fmt, q, s, K, n, c);
+            if (Y) Y[(int64_t)i * N + n] = or_bf16_round(acc);
+            if (Y64) Y64[(int64_t)i * N + n] = acc;
+        }
+        free(x);
+    }
+}
+
+void or_dense_backward(int rows, int N, int K, int b, int fmt, const uint8_t *q, const void *s,
+                       const uint16_t *R, const double *R64, const uint16_t *X, const double *X64,
+                       const uint16_t *dY, int flags, uint16_t *dX, double *dX64, double *dR)
+{
+    const int has_r = R || R64;
+    double *dxts = malloc(sizeof(double) * (size_t)(rows > 0 ? rows : 1) * K);
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < rows; ++i) {
+        double *dxt = dxts + (int64_t)i * K;
+        double *dx = malloc(sizeof(double) * (size_t)K);
+        for (int c = 0; c < K; ++c) {
+            double a = 0.0;
+            for (int n = 0; n < N; ++n)
+                a += or_bf16_to_double(dY[(int64_t)i * N + n]) * dequant_elem(fmt, q, s, K, n, c);
+            dxt[c] = has_r ? rbf(a, flags) : a;
+        }
+        if (has_r)
+            rotate_row_t64(dxt, R, R64, K, b, dx);
+        else
+            memcpy(dx, dxt, sizeof(double) * (size_t)K);
+        for (int c = 0; c < K; ++c) {
+            if (dX) dX[(int64_t)i * K + c] = or_bf16_round(dx[c]);
+            if (dX64) dX64[(int64_t)i * K + c] = dx[c];
+        }
+        free(dx);
+    }
+    if (dR && has_r) {
+        int nblk = K / b;
+#pragma omp parallel for schedule(static)
+        for (int beta = 0; beta < nblk; ++beta) {
+            double *D = dR + (int64_t)beta * b * b;
+            for (int r = 0; r < b * b; ++r)
+                D[r] = 0.0;
+            for (int i = 0; i < rows; ++i)
+                for (int r = 0; r < b; ++r) {
+                    int64_t o = (int64_t)i * K + (int64_t)beta * b;
+                    double xr = X64 ? X64[o + r] : or_bf16_to_double(X[o + r]);
+                    for (int c = 0; c < b; ++c)
+                        D[r * b + c] += xr * dxts[o + c];
+                }
+        }
+    }
+    free(dxts);
+}
+
 /* Number of OpenMP threads the oracle runs with. */
 int or_num_threads(void)
 {
