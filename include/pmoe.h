@@ -275,6 +275,33 @@ pmoe_status adapter_grad(int32_t rows, int32_t dim, int32_t b, const void *X, co
                          const void *R, void *dX, float *dR, cudaStream_t stream);
 
 /*
+ * dense_linear_forward / dense_linear_backward -- one frozen low-precision
+ * projection outside the experts, with the orthogonal adapter on its input
+ * and no gradient for the frozen weight (the Orbit article, technical
+ * details: bypass-base-weight-grad; the Orbit analysis, OFT section: a
+ * local orthogonal transform of the activations).
+ *   forward:  x~ = bf16(X blockdiag(R));  Y = bf16(x~ W^T)
+ *   backward: dx~ = bf16(dY W);  dR = sum_rows x_blk^T dx~_blk (FP32);
+ *             dX = bf16(dx~ blockdiag(R)^T)      (R NULL: dX = bf16(dY W))
+ *   q, s   W [N, K] in the packed format fmt (as one expert of pmoe_weights)
+ *   R      bf16 [K/block, block, block] or NULL (no adapter); block in
+ *          {16, 32, 64, 128}, K % block == 0
+ *   X      bf16 [rows, K] (in)          Y  bf16 [rows, N] (out)
+ *   dY     bf16 [rows, N] (in)          dX bf16 [rows, K] (out)
+ *   dR     f32 [K/block, block, block] (out, overwritten; required iff R)
+ *   ws     >= dense_linear_ws_bytes(rows, N, K) bytes, 16-byte aligned
+ * N % 64 == 0 and K % 64 == 0 (FP8: % 128).  All pointers 16-byte aligned.
+ */
+size_t dense_linear_ws_bytes(int32_t rows, int32_t N, int32_t K);
+pmoe_status dense_linear_forward(pmoe_wfmt fmt, const void *q, const void *s, int32_t N, int32_t K,
+                                 int32_t block, const void *R, int32_t rows, const void *X, void *Y,
+                                 void *ws, size_t ws_bytes, cudaStream_t stream);
+pmoe_status dense_linear_backward(pmoe_wfmt fmt, const void *q, const void *s, int32_t N, int32_t K,
+                                  int32_t block, const void *R, int32_t rows, const void *X,
+                                  const void *dY, void *dX, float *dR, void *ws, size_t ws_bytes,
+                                  cudaStream_t stream);
+
+/*
  * adapter_cayley -- R = (I + S)(I - S)^{-1} for nblk skew-symmetric b x b
  * blocks S (f32 [nblk, b, b]; only skew input is meaningful: the symmetric
  * part of I - S must be I); R written as bf16 (R_bf16, nullable) and f32

@@ -744,6 +744,130 @@ pmoe_status adapter_grad(int32_t rows, int32_t dim, int32_t b, const void *X, co
     return launched(stream);
 }
 
+// ------------------------------------------------------------------ dense linear
+namespace pmoe {
+struct DenseWs {
+    GgWs g;
+    int32_t *offsets;
+    uint16_t *buf;   // x~ (forward) or dx~ (backward), [rows, K] bf16
+};
+static DenseWs carve_dense(void *ws, int rows, int K, size_t *bytes)
+{
+    size_t gb;
+    DenseWs w;
+    w.g = carve_gg(ws, 1, rows, &gb);
+    Carver c(ws);
+    c.off = gb;
+    w.offsets = c.take<int32_t>(2);
+    w.buf = c.take<uint16_t>((int64_t)(rows > 0 ? rows : 1) * K);
+    if (bytes) *bytes = c.off;
+    return w;
+}
+static bool dense_shape_ok(pmoe_wfmt fmt, int N, int K, int b, int rows)
+{
+    if (N <= 0 || K <= 0 || N % 64 || K % 64 || rows < 0 || N > 65536 || K > 65536) return false;
+    if (fmt != PMOE_W_INT4_G32_BF16 && fmt != PMOE_W_MXFP4_G32_E8M0 && fmt != PMOE_W_FP8_B128_F32)
+        return false;
+    if (fmt == PMOE_W_FP8_B128_F32 && (N % 128 || K % 128)) return false;
+    return block_ok(b) && K % b == 0;
+}
+// One frozen [N, K] matrix as a single-expert grouped GEMM over rows 0..rows-1.
+static pmoe_status dense_gemm(pmoe_wfmt fmt, const void *q, const void *s, int N, int K, bool trans,
+                              const void *A, int rows, void *out, DenseWs &w, cudaStream_t st)
+{
+    launch_set_offsets(w.offsets, rows, st);
+    launch_offsets_to_active(1, rows, w.offsets, w.g.counts, w.g.active, w.g.num_active, w.g.err, st);
+    launch_build_tiles(1, 1, kGemmRows, kGemmAlign, w.g.counts, w.offsets, w.g.active,
+                       w.g.num_active, w.g.tiles, w.g.chunk_tiles, w.g.chunk_rows, st);
+    GemmArgs g{};
+    g.kind = trans ? GK_BWD_DX : GK_FWD_DOWN;
+    g.fmt = fmt;
+    g.wq = (const uint8_t *)q;
+    g.ws = (const uint8_t *)s;
+    g.wq_stride = wq_bytes(fmt, N, K);
+    g.ws_stride = ws_bytes_of(fmt, N, K);
+    g.Nst = N;
+    g.Kst = K;
+    g.A = (const uint16_t *)A;
+    g.K = trans ? N : K;
+    g.Nout = trans ? K : N;
+    g.tiles = w.g.tiles;
+    g.chunk_tiles = w.g.chunk_tiles;
+    g.c0 = 0;
+    g.c1 = 1;
+    g.out = (uint16_t *)out;
+    g.I = N;
+    g.nmat = 1;
+    return run_gemm(g, rows, w.g.err, st);
+}
+}  // namespace pmoe
+
+size_t dense_linear_ws_bytes(int32_t rows, int32_t N, int32_t K)
+{
+    if (rows < 0 || N <= 0 || K <= 0) return 0;
+    size_t b;
+    pmoe::carve_dense(nullptr, rows, K, &b);
+    return b;
+}
+
+pmoe_status dense_linear_forward(pmoe_wfmt fmt, const void *q, const void *s, int32_t N, int32_t K,
+                                 int32_t block, const void *R, int32_t rows, const void *X, void *Y,
+                                 void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    using namespace pmoe;
+    if (!dense_shape_ok(fmt, N, K, block, rows)) return PMOE_ERR_INVALID_ARG;
+    if (!q || !s || (rows > 0 && (!X || !Y))) return PMOE_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(s) || !aligned16(R) || !aligned16(X) || !aligned16(Y))
+        return PMOE_ERR_INVALID_ARG;
+    size_t need;
+    DenseWs w = carve_dense(ws, rows, K, &need);
+    if (!ws || ws_bytes < need || !aligned16(ws)) return PMOE_ERR_WORKSPACE;
+    if (rows == 0) return PMOE_OK;
+    const void *A = X;
+    if (R) {   // x~ = bf16(x blockdiag(R))
+        launch_rotate_tc(block, false, false, (const uint16_t *)X, K, false, nullptr, 1, nullptr,
+                         (const uint16_t *)R, 0, K, w.buf, K, nullptr, nullptr, nullptr, 0, rows,
+                         nullptr, stream);
+        A = w.buf;
+    }
+    pmoe_status st = dense_gemm(fmt, q, s, N, K, false, A, rows, Y, w, stream);
+    if (st != PMOE_OK) return st;
+    return launched(stream);
+}
+
+pmoe_status dense_linear_backward(pmoe_wfmt fmt, const void *q, const void *s, int32_t N, int32_t K,
+                                  int32_t block, const void *R, int32_t rows, const void *X,
+                                  const void *dY, void *dX, float *dR, void *ws, size_t ws_bytes,
+                                  cudaStream_t stream)
+{
+    using namespace pmoe;
+    if (!dense_shape_ok(fmt, N, K, block, rows)) return PMOE_ERR_INVALID_ARG;
+    if (!q || !s || (R && !dR) || (rows > 0 && (!dY || !dX || (R && !X)))) return PMOE_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(s) || !aligned16(R) || !aligned16(X) || !aligned16(dY) ||
+        !aligned16(dX) || !aligned16(dR))
+        return PMOE_ERR_INVALID_ARG;
+    size_t need;
+    DenseWs w = carve_dense(ws, rows, K, &need);
+    if (!ws || ws_bytes < need || !aligned16(ws)) return PMOE_ERR_WORKSPACE;
+    if (rows == 0) {
+        if (R && cudaMemsetAsync(dR, 0, (size_t)K * block * sizeof(float), stream) != cudaSuccess)
+            return PMOE_ERR_CUDA;
+        return PMOE_OK;
+    }
+    // G = dY W (contraction over the stored rows); with an adapter it is
+    // the BF16 tensor dx~, then dX = bf16(dx~ R^T) and dR = sum x^T dx~
+    pmoe_status st = dense_gemm(fmt, q, s, N, K, true, dY, rows, R ? (void *)w.buf : dX, w, stream);
+    if (st != PMOE_OK) return st;
+    if (R) {
+        launch_outer_tc(1, rows, K, block, (const uint16_t *)X, K, false, nullptr, 1, w.buf, K,
+                        nullptr, dR, stream);
+        launch_rotate_tc(block, true, false, w.buf, K, false, nullptr, 1, nullptr,
+                         (const uint16_t *)R, 0, K, (uint16_t *)dX, K, nullptr, nullptr, nullptr, 0,
+                         rows, nullptr, stream);
+    }
+    return launched(stream);
+}
+
 pmoe_status adapter_cayley(int32_t nblk, int32_t b, const float *S, void *R_bf16, float *R_f32,
                            cudaStream_t stream)
 {

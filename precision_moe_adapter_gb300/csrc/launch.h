@@ -100,6 +100,8 @@ constexpr int kRotTileRows = 64;
 // layer.cu
 void launch_combine(int T, int d, int k, const uint16_t *o, const int32_t *inv_perm,
                     const float *w, uint16_t *Y, cudaStream_t st);
+// offsets = [0, rows] (a single-matrix work list)
+void launch_set_offsets(int32_t *offsets, int rows, cudaStream_t st);
 void launch_gather_rows(int P, int d, int k, const uint16_t *src, const int32_t *perm,
                         uint16_t *out, cudaStream_t st);
 void launch_dtw_reduce(int P, int nparts, const float *part, const int32_t *perm, float *dtw,

@@ -77,4 +77,18 @@ void launch_dtw_reduce(int P, int nparts, const float *part, const int32_t *perm
     note_launch();
 }
 
+__global__ void k_set_offsets(int32_t *offsets, int rows)
+{
+    if (threadIdx.x == 0) {
+        offsets[0] = 0;
+        offsets[1] = rows;
+    }
+}
+
+void launch_set_offsets(int32_t *offsets, int rows, cudaStream_t st)
+{
+    k_set_offsets<<<1, 32, 0, st>>>(offsets, rows);
+    note_launch();
+}
+
 }  // namespace pmoe

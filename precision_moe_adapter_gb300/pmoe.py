@@ -26,7 +26,8 @@ EXPORTS = ("moe_route", "moe_permute", "moe_chunked_forward", "moe_backward_data
            "adapter_apply", "adapter_grad", "adapter_cayley", "adapter_cayley_grad",
            "moe_workspace_bytes", "moe_scratch_bytes", "moe_clear_status", "moe_query_status",
            "pmoe_status_string", "pmoe_launch_count", "pmoe_kernel_timing", "pmoe_kernel_time",
-           "moe_grouped_gemm", "moe_grouped_gemm_ws_bytes", "moe_permute_noalloc")
+           "moe_grouped_gemm", "moe_grouped_gemm_ws_bytes", "moe_permute_noalloc",
+           "dense_linear_ws_bytes", "dense_linear_forward", "dense_linear_backward")
 PERMUTE_NOALLOC_SCRATCH_BYTES = 1 << 20
 KT_GEMM_GATE_UP, KT_GEMM_DOWN, KT_GEMM_BWD_G, KT_GEMM_BWD_DX, KT_ROUTER = 0, 1, 2, 3, 4
 
@@ -83,6 +84,8 @@ def _declare(L):
         "moe_route": [D, p, p, p, p, p, p, ctypes.c_int, p, sz, p],
         "moe_permute": [D, p, PR, p, sz, p],
         "moe_permute_noalloc": [D, p, PR, p],
+        "dense_linear_forward": [ctypes.c_int, p, p, i32, i32, i32, p, i32, p, p, p, sz, p],
+        "dense_linear_backward": [ctypes.c_int, p, p, i32, i32, i32, p, i32, p, p, p, p, p, sz, p],
         "moe_chunked_forward": [D, PW, PA, PR, p, i32, ctypes.c_int, p, p, p, sz, p],
         "moe_backward_data": [D, PW, PA, PR, p, p, p, i32, p, p, p, p, p, sz, p],
         "moe_dequant": [ctypes.c_int, p, p, i64, i64, p, p],
@@ -102,6 +105,8 @@ def _declare(L):
     L.moe_workspace_bytes.restype = sz
     L.moe_grouped_gemm_ws_bytes.argtypes = [i32, i32]
     L.moe_grouped_gemm_ws_bytes.restype = sz
+    L.dense_linear_ws_bytes.argtypes = [i32, i32, i32]
+    L.dense_linear_ws_bytes.restype = sz
     L.moe_scratch_bytes.argtypes = [D, i32, ctypes.c_int]
     L.moe_scratch_bytes.restype = sz
     L.pmoe_status_string.argtypes = [st]
@@ -181,9 +186,26 @@ def moe_permute(dm, idx, rt: Routing, ws, stream=None):
                              _stream(stream)), "moe_permute")
 
 
+def dense_linear_ws_bytes(rows, N, K) -> int:
+    return int(lib().dense_linear_ws_bytes(rows, N, K))
+
+
+def dense_linear_forward(fmt, q, s, N, K, block, R, rows, X, Y, ws, stream=None):
+    _check(lib().dense_linear_forward(fmt, _ptr(q), _ptr(s), N, K, block, _ptr(R), rows, _ptr(X),
+                                      _ptr(Y), _ptr(ws), _nbytes(ws), _stream(stream)),
+           "dense_linear_forward")
+
+
+def dense_linear_backward(fmt, q, s, N, K, block, R, rows, X, dY, dX, dR, ws, stream=None):
+    _check(lib().dense_linear_backward(fmt, _ptr(q), _ptr(s), N, K, block, _ptr(R), rows, _ptr(X),
+                                       _ptr(dY), _ptr(dX), _ptr(dR), _ptr(ws), _nbytes(ws),
+                                       _stream(stream)), "dense_linear_backward")
+
+
 def moe_permute_noalloc(dm, idx, rt: Routing, stream=None):
     _check(lib().moe_permute_noalloc(dm, _ptr(idx), ctypes.byref(rt), _stream(stream)),
-           "moe_permute_noalloc")
+           "moe_permute_noalloc",
+           "dense_linear_ws_bytes", "dense_linear_forward", "dense_linear_backward")
 
 
 def moe_chunked_forward(dm, wts: Weights, adp, rt: Routing, X, chunk_C, mode, Y, ctx, ws,
