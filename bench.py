@@ -48,6 +48,13 @@ def parse():
     return ap.parse_args()
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch
+# of the GEMM classes, from one ncu capture of this kernel version on the
+# default workload (profiles/k_gemm_tc_kimi_k2_int4.md); None elsewhere.
+TRAFFIC_BYTES = {("kimi_k2", "fused", "gemm_gate_up"): 8.564e9,
+                 ("kimi_k2", "fused", "gemm_bwd_dx"): 7.800e9}
+
+
 def max_over_ranks(x: float) -> float:
     """The largest x over all ranks (x itself outside a process group):
     every rank times its own replica and the job takes the slowest."""
@@ -361,9 +368,11 @@ def main():
                  "router": 2 * cfg.T * cfg.d * cfg.E}[dom]
     dom_avg_ms = dom_ms / max(dom_n, 1)
     dom_tf = dom_flops / (dom_avg_ms / 1e3) / 1e12
+    default_load = not (args.tokens or args.experts or args.chunk)
+    traffic = TRAFFIC_BYTES.get((cfg.name, args.mode, dom)) if default_load else None
     roofline = {"kernel": dom, "bound": "tensor", "achieved": round(dom_tf, 3),
                 "peak": pk["bf16_sus"], "unit": "TFLOP/s", "frac": round(dom_tf / pk["bf16_sus"], 5),
-                "traffic": None, "peak_source": f"{pk['src']} bf16 sustained",
+                "traffic": traffic, "peak_source": f"{pk['src']} bf16 sustained",
                 "launch_ms": round(dom_avg_ms, 4), "launches": dom_n,
                 "algorithmic_flops_per_launch": dom_flops}
 
