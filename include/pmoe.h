@@ -205,6 +205,37 @@ pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const p
                                 cudaStream_t stream);
 
 /*
+ * Adapter slots for rollout while training publishes (the Orbit analysis:
+ * the BF16 adapter is the only thing the trainer sends to the rollout side,
+ * and the rollout engine must switch to a new adapter without tearing a
+ * step).  Two device copies of the adapter and one control word:
+ *   ctrl   device uint64, 8-byte aligned: (version << 32) | active_slot
+ * moe_adapter_publish stores a new control word with one atomic 64-bit
+ * write, ordered after the earlier work of its stream (so the new slot's
+ * contents, copied on that stream, are in place first).
+ * moe_chunked_forward_slots is moe_chunked_forward with the adapter taken
+ * from the active slot: its first kernel reads the control word once and
+ * every rotation of that forward uses the slot it names, so a forward
+ * running while a publish lands uses one adapter throughout; the version it
+ * used is written to *version_out (device uint32, may be NULL).
+ * Protocol: write only the inactive slot, and rewrite a slot only after
+ * every forward that reported that slot's version has completed.
+ */
+typedef struct {
+    const void *R_up[2], *R_down[2];   /* bf16, as pmoe_adapter; R_down[] both NULL or both set */
+    int64_t stride_up, stride_down;
+    const uint64_t *ctrl;
+} pmoe_adapter_slots;
+
+pmoe_status moe_adapter_publish(uint64_t *ctrl, uint32_t slot, uint32_t version,
+                                cudaStream_t stream);
+pmoe_status moe_chunked_forward_slots(pmoe_dims dims, const pmoe_weights *wts,
+                                      const pmoe_adapter_slots *slots, const pmoe_routing *rt,
+                                      const void *X, int32_t chunk_C, int mode, void *Y, void *ctx,
+                                      uint32_t *version_out, void *ws, size_t ws_bytes,
+                                      cudaStream_t stream);
+
+/*
  * moe_backward_data -- backward through the frozen experts with no base
  * weight gradient (page 1, 技艺细节: bypass-base-weight-grad GEMM backward;
  * page 2, 机制拆解: the base takes no backward update cost).  Routing and

@@ -149,6 +149,7 @@ struct FwdWs {
     DevErr *err;
     Lists l;
     uint16_t *xt, *h, *ht, *o, *scratch;
+    uint64_t *snap;   // adapter-slot snapshot of this forward
 };
 static FwdWs carve_fwd(void *ws, const pmoe_dims &d, int C, int mode, size_t *bytes)
 {
@@ -163,6 +164,7 @@ static FwdWs carve_fwd(void *ws, const pmoe_dims &d, int C, int mode, size_t *by
     w.o = c.take<uint16_t>(P * d.d);
     int64_t slots = mode == PMOE_MODE_SCRATCH ? std::min(C, d.E) : 0;
     w.scratch = c.take<uint16_t>(slots * 3 * (int64_t)d.inter * d.d);
+    w.snap = c.take<uint64_t>(2);
     if (bytes) *bytes = c.off;
     return w;
 }
@@ -380,17 +382,16 @@ static bool adapter_ok(const pmoe_adapter *ad)
     return aligned16(ad->R_up) && aligned16(ad->R_down);
 }
 
-pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const pmoe_adapter *adp,
+namespace pmoe {
+// The forward for one adapter, or for two adapter slots picked on the device
+// by a snapshot of the slot control word (slots: R_*_alt is slot 1).
+static pmoe_status forward_impl(pmoe_dims dims, const pmoe_weights *wts, const uint16_t *R_up,
+                                const uint16_t *R_up_alt, const uint16_t *R_dn,
+                                const uint16_t *R_dn_alt, int64_t su, int64_t sd,
+                                const uint64_t *ctrl, uint32_t *version_out,
                                 const pmoe_routing *rt, const void *X, int32_t chunk_C, int mode,
-                                void *Y, void *ctx, void *ws, size_t ws_bytes,
-                                cudaStream_t stream)
+                                void *Y, void *ctx, void *ws, size_t ws_bytes, cudaStream_t stream)
 {
-    if (!dims_ok(dims) || !weights_ok(wts, dims) || !adapter_ok(adp) || !routing_ok(rt, dims))
-        return PMOE_ERR_INVALID_ARG;
-    if (chunk_C < 1 || (mode != PMOE_MODE_FUSED && mode != PMOE_MODE_SCRATCH))
-        return PMOE_ERR_INVALID_ARG;
-    if (dims.T > 0 && (!X || !Y)) return PMOE_ERR_INVALID_ARG;
-    if (!aligned16(X) || !aligned16(Y) || !aligned16(ctx)) return PMOE_ERR_INVALID_ARG;
     const int C = std::min(chunk_C, dims.E);
     size_t need;
     FwdWs w = carve_fwd(ws, dims, C, mode, &need);
@@ -400,9 +401,11 @@ pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const p
     const int d = dims.d, I = dims.inter, b = dims.block, k = dims.k;
     const int P = dims.T * k;
     const int fmt = wts->fmt;
-    const uint16_t *R_up = adp ? (const uint16_t *)adp->R_up : nullptr;
-    const uint16_t *R_dn = adp && R_up ? (const uint16_t *)adp->R_down : nullptr;
-    const int64_t su = adp ? adp->stride_up : 0, sd = adp ? adp->stride_down : 0;
+    const uint64_t *sel = nullptr;
+    if (ctrl) {   // every rotation of this forward reads one snapshot of the slot word
+        launch_adapter_snapshot(ctrl, w.snap, version_out, stream);
+        sel = w.snap;
+    }
     const int nch = nchunks_of(dims, C);
     const int maxrt = max_rot_tiles_of(dims);
     const Lists &L = w.l;
@@ -410,7 +413,7 @@ pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const p
     // x~ = bf16(x R_up[e]) for every pair, gathered into expert-sorted order
     launch_rotate_tc(b, false, false, (const uint16_t *)X, d, true, rt->perm, k, rt->idx, R_up, su,
                      d, w.xt, d, L.rtiles, L.chunk_rtiles, L.chunk_rtiles + nch, maxrt, 0, nullptr,
-                     stream);
+                     stream, R_up_alt, sel);
 
     GemmArgs gu{};
     gu.kind = GK_FWD_GU;
@@ -458,7 +461,7 @@ pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const p
         if (R_dn)
             launch_rotate_tc(b, false, false, w.h, I, false, rt->perm, k, rt->idx, R_dn, sd, I, w.ht,
                              I, L.rtiles, L.chunk_rtiles, L.chunk_rtiles + nch, maxrt, 0, nullptr,
-                             stream);
+                             stream, R_dn_alt, sel);
         {
             ScopedTimer tm(PMOE_KT_GEMM_DOWN, stream);
             if ((gs = run_gemm(dn, P, w.err, stream)) != PMOE_OK) return gs;
@@ -487,7 +490,7 @@ pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const p
             if (R_dn)
                 launch_rotate_tc(b, false, false, w.h, I, false, rt->perm, k, rt->idx, R_dn, sd, I,
                                  w.ht, I, L.rtiles, L.chunk_rtiles + c, L.chunk_rtiles + c + 1,
-                                 maxrt, 0, nullptr, stream);
+                                 maxrt, 0, nullptr, stream, R_dn_alt, sel);
             {
                 ScopedTimer tm(PMOE_KT_GEMM_DOWN, stream);
                 if ((gs = run_gemm(dn, P, w.err, stream)) != PMOE_OK) return gs;
@@ -496,6 +499,60 @@ pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const p
     }
     launch_combine(dims.T, d, k, w.o, rt->inv_perm, rt->w, (uint16_t *)Y, stream);
     return launched(stream);
+}
+}  // namespace pmoe
+
+pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const pmoe_adapter *adp,
+                                const pmoe_routing *rt, const void *X, int32_t chunk_C, int mode,
+                                void *Y, void *ctx, void *ws, size_t ws_bytes,
+                                cudaStream_t stream)
+{
+    using namespace pmoe;
+    if (!dims_ok(dims) || !weights_ok(wts, dims) || !adapter_ok(adp) || !routing_ok(rt, dims))
+        return PMOE_ERR_INVALID_ARG;
+    if (chunk_C < 1 || (mode != PMOE_MODE_FUSED && mode != PMOE_MODE_SCRATCH))
+        return PMOE_ERR_INVALID_ARG;
+    if (dims.T > 0 && (!X || !Y)) return PMOE_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Y) || !aligned16(ctx)) return PMOE_ERR_INVALID_ARG;
+    const uint16_t *R_up = adp ? (const uint16_t *)adp->R_up : nullptr;
+    const uint16_t *R_dn = adp && R_up ? (const uint16_t *)adp->R_down : nullptr;
+    const int64_t su = adp ? adp->stride_up : 0, sd = adp ? adp->stride_down : 0;
+    return forward_impl(dims, wts, R_up, nullptr, R_dn, nullptr, su, sd, nullptr, nullptr, rt, X,
+                        chunk_C, mode, Y, ctx, ws, ws_bytes, stream);
+}
+
+pmoe_status moe_adapter_publish(uint64_t *ctrl, uint32_t slot, uint32_t version,
+                                cudaStream_t stream)
+{
+    using namespace pmoe;
+    if (!ctrl || slot > 1 || ((uintptr_t)ctrl & 7)) return PMOE_ERR_INVALID_ARG;
+    launch_adapter_publish(ctrl, slot, version, stream);
+    return launched(stream);
+}
+
+pmoe_status moe_chunked_forward_slots(pmoe_dims dims, const pmoe_weights *wts,
+                                      const pmoe_adapter_slots *slots, const pmoe_routing *rt,
+                                      const void *X, int32_t chunk_C, int mode, void *Y, void *ctx,
+                                      uint32_t *version_out, void *ws, size_t ws_bytes,
+                                      cudaStream_t stream)
+{
+    using namespace pmoe;
+    if (!dims_ok(dims) || !weights_ok(wts, dims) || !routing_ok(rt, dims) || !slots || !slots->ctrl)
+        return PMOE_ERR_INVALID_ARG;
+    if (!slots->R_up[0] || !slots->R_up[1] || ((uintptr_t)slots->ctrl & 7) ||
+        (!slots->R_down[0]) != (!slots->R_down[1]))
+        return PMOE_ERR_INVALID_ARG;
+    for (int i = 0; i < 2; ++i)
+        if (!aligned16(slots->R_up[i]) || !aligned16(slots->R_down[i])) return PMOE_ERR_INVALID_ARG;
+    if (slots->stride_up < 0 || slots->stride_down < 0) return PMOE_ERR_INVALID_ARG;
+    if (chunk_C < 1 || (mode != PMOE_MODE_FUSED && mode != PMOE_MODE_SCRATCH))
+        return PMOE_ERR_INVALID_ARG;
+    if (dims.T > 0 && (!X || !Y)) return PMOE_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Y) || !aligned16(ctx)) return PMOE_ERR_INVALID_ARG;
+    return forward_impl(dims, wts, (const uint16_t *)slots->R_up[0], (const uint16_t *)slots->R_up[1],
+                        (const uint16_t *)slots->R_down[0], (const uint16_t *)slots->R_down[1],
+                        slots->stride_up, slots->stride_down, slots->ctrl, version_out, rt, X,
+                        chunk_C, mode, Y, ctx, ws, ws_bytes, stream);
 }
 
 pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmoe_adapter *adp,

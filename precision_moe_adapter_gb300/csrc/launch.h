@@ -90,7 +90,8 @@ void launch_rotate_tc(int b, bool trans, bool swiglu_bwd, const uint16_t *src, i
                       bool gather, const int32_t *perm, int k, const int32_t *idx_flat,
                       const uint16_t *R, int64_t stride, int dim, uint16_t *out, int64_t out_ld,
                       const Tile *tiles, const int32_t *tbeg, const int32_t *tend, int max_tiles,
-                      int nrows, const uint16_t *ctx, cudaStream_t st);
+                      int nrows, const uint16_t *ctx, cudaStream_t st,
+                      const uint16_t *R_alt = nullptr, const uint64_t *sel = nullptr);
 // dR[s][beta] = sum over rows of set s of a_blk^T g_blk on mma.sync
 void launch_outer_tc(int nsets, int nrows, int dim, int b, const uint16_t *a, int64_t a_ld,
                      bool gather, const int32_t *perm, int k, const uint16_t *g, int64_t g_ld,
@@ -100,6 +101,11 @@ constexpr int kRotTileRows = 64;
 // layer.cu
 void launch_combine(int T, int d, int k, const uint16_t *o, const int32_t *inv_perm,
                     const float *w, uint16_t *Y, cudaStream_t st);
+// adapter slots: snap = *ctrl (one atomic 64-bit read), *version_out =
+// snap >> 32 when given; publish: *ctrl = version << 32 | slot (atomic)
+void launch_adapter_snapshot(const uint64_t *ctrl, uint64_t *snap, uint32_t *version_out,
+                             cudaStream_t st);
+void launch_adapter_publish(uint64_t *ctrl, uint32_t slot, uint32_t version, cudaStream_t st);
 // offsets = [0, rows] (a single-matrix work list)
 void launch_set_offsets(int32_t *offsets, int rows, cudaStream_t st);
 void launch_gather_rows(int P, int d, int k, const uint16_t *src, const int32_t *perm,

@@ -77,6 +77,36 @@ void launch_dtw_reduce(int P, int nparts, const float *part, const int32_t *perm
     note_launch();
 }
 
+__global__ void k_adapter_snapshot(const uint64_t *ctrl, uint64_t *snap, uint32_t *version_out)
+{
+    if (threadIdx.x == 0) {
+        const uint64_t v = atomicAdd((unsigned long long *)ctrl, 0ull);
+        *snap = v;
+        if (version_out) *version_out = (uint32_t)(v >> 32);
+    }
+}
+
+void launch_adapter_snapshot(const uint64_t *ctrl, uint64_t *snap, uint32_t *version_out,
+                             cudaStream_t st)
+{
+    k_adapter_snapshot<<<1, 32, 0, st>>>(ctrl, snap, version_out);
+    note_launch();
+}
+
+__global__ void k_adapter_publish(uint64_t *ctrl, uint64_t word)
+{
+    if (threadIdx.x == 0) {
+        __threadfence();   // earlier writes of this stream (the new slot) come first
+        atomicExch((unsigned long long *)ctrl, (unsigned long long)word);
+    }
+}
+
+void launch_adapter_publish(uint64_t *ctrl, uint32_t slot, uint32_t version, cudaStream_t st)
+{
+    k_adapter_publish<<<1, 32, 0, st>>>(ctrl, ((uint64_t)version << 32) | (slot & 1u));
+    note_launch();
+}
+
 __global__ void k_set_offsets(int32_t *offsets, int rows)
 {
     if (threadIdx.x == 0) {

@@ -75,6 +75,8 @@ struct RotArgs {
     const int32_t *tbeg, *tend;   // device range of tiles to process
     int nrows;                 // rows when tiles == NULL
     const uint16_t *ctx;       // ROT_SWIGLU_BWD: [g | u | h] rows of 3*dim
+    const uint16_t *R_alt;     // second adapter slot (NULL: none)
+    const uint64_t *sel;       // adapter snapshot: low bit of the low word picks R_alt
 };
 
 // smem row pitch (elements): b + 8 keeps ldmatrix rows on distinct banks
@@ -112,7 +114,7 @@ __global__ void __launch_bounds__(128) k_rotate_mma(RotArgs a)
             tl.nrows = min(kRotRows, a.nrows - tl.row0);
         }
         const int bg = (int)(it % ngroups);
-        const uint16_t *Re = a.R;
+        const uint16_t *Re = (a.sel && (*a.sel & 1u)) ? a.R_alt : a.R;
         if (Re && a.stride) Re += (int64_t)tl.expert * a.stride;
         for (int beta = bg * kRotBlocks; beta < min(nblk, (bg + 1) * kRotBlocks); ++beta) {
             __syncthreads();
@@ -263,10 +265,11 @@ void launch_rotate_tc(int b, bool trans, bool swiglu_bwd, const uint16_t *src, i
                       bool gather, const int32_t *perm, int k, const int32_t *idx_flat,
                       const uint16_t *R, int64_t stride, int dim, uint16_t *out, int64_t out_ld,
                       const Tile *tiles, const int32_t *tbeg, const int32_t *tend, int max_tiles,
-                      int nrows, const uint16_t *ctx, cudaStream_t st)
+                      int nrows, const uint16_t *ctx, cudaStream_t st, const uint16_t *R_alt,
+                      const uint64_t *sel)
 {
     RotArgs a{src, src_ld, gather ? 1 : 0, perm, k, idx_flat, R, stride, dim, out, out_ld, tiles,
-              tbeg, tend, nrows, ctx};
+              tbeg, tend, nrows, ctx, R_alt, sel};
     if (!tiles) max_tiles = (nrows + kRotRows - 1) / kRotRows;
     if (swiglu_bwd) rot_dispatch<true, ROT_SWIGLU_BWD>(b, a, max_tiles, st);
     else if (trans) rot_dispatch<true, ROT_STORE>(b, a, max_tiles, st);

@@ -27,7 +27,8 @@ EXPORTS = ("moe_route", "moe_permute", "moe_chunked_forward", "moe_backward_data
            "moe_workspace_bytes", "moe_scratch_bytes", "moe_clear_status", "moe_query_status",
            "pmoe_status_string", "pmoe_launch_count", "pmoe_kernel_timing", "pmoe_kernel_time",
            "moe_grouped_gemm", "moe_grouped_gemm_ws_bytes", "moe_permute_noalloc",
-           "dense_linear_ws_bytes", "dense_linear_forward", "dense_linear_backward")
+           "dense_linear_ws_bytes", "dense_linear_forward", "dense_linear_backward",
+           "moe_adapter_publish", "moe_chunked_forward_slots")
 PERMUTE_NOALLOC_SCRATCH_BYTES = 1 << 20
 KT_GEMM_GATE_UP, KT_GEMM_DOWN, KT_GEMM_BWD_G, KT_GEMM_BWD_DX, KT_ROUTER = 0, 1, 2, 3, 4
 
@@ -51,6 +52,12 @@ class Weights(ctypes.Structure):
 class Adapter(ctypes.Structure):
     _fields_ = [("R_up", ctypes.c_void_p), ("R_down", ctypes.c_void_p),
                 ("stride_up", ctypes.c_int64), ("stride_down", ctypes.c_int64)]
+
+
+class AdapterSlots(ctypes.Structure):
+    _fields_ = [("R_up", ctypes.c_void_p * 2), ("R_down", ctypes.c_void_p * 2),
+                ("stride_up", ctypes.c_int64), ("stride_down", ctypes.c_int64),
+                ("ctrl", ctypes.c_void_p)]
 
 
 class Routing(ctypes.Structure):
@@ -84,6 +91,9 @@ def _declare(L):
         "moe_route": [D, p, p, p, p, p, p, ctypes.c_int, p, sz, p],
         "moe_permute": [D, p, PR, p, sz, p],
         "moe_permute_noalloc": [D, p, PR, p],
+        "moe_adapter_publish": [p, ctypes.c_uint32, ctypes.c_uint32, p],
+        "moe_chunked_forward_slots": [D, PW, ctypes.POINTER(AdapterSlots), PR, p, i32, ctypes.c_int,
+                                      p, p, p, p, sz, p],
         "dense_linear_forward": [ctypes.c_int, p, p, i32, i32, i32, p, i32, p, p, p, sz, p],
         "dense_linear_backward": [ctypes.c_int, p, p, i32, i32, i32, p, i32, p, p, p, p, p, sz, p],
         "moe_chunked_forward": [D, PW, PA, PR, p, i32, ctypes.c_int, p, p, p, sz, p],
@@ -186,6 +196,27 @@ def moe_permute(dm, idx, rt: Routing, ws, stream=None):
                              _stream(stream)), "moe_permute")
 
 
+def adapter_slots(R_up0, R_up1, R_down0, R_down1, stride_up, stride_down, ctrl) -> AdapterSlots:
+    a = AdapterSlots()
+    a.R_up[0], a.R_up[1] = _ptr(R_up0), _ptr(R_up1)
+    a.R_down[0], a.R_down[1] = _ptr(R_down0), _ptr(R_down1)
+    a.stride_up, a.stride_down, a.ctrl = stride_up, stride_down, _ptr(ctrl)
+    return a
+
+
+def moe_adapter_publish(ctrl, slot, version, stream=None):
+    _check(lib().moe_adapter_publish(_ptr(ctrl), slot, version, _stream(stream)),
+           "moe_adapter_publish")
+
+
+def moe_chunked_forward_slots(dm, wts: Weights, slots: AdapterSlots, rt: Routing, X, chunk_C, mode,
+                              Y, ctx, version_out, ws, stream=None):
+    _check(lib().moe_chunked_forward_slots(dm, ctypes.byref(wts), ctypes.byref(slots),
+                                           ctypes.byref(rt), _ptr(X), chunk_C, mode, _ptr(Y),
+                                           _ptr(ctx), _ptr(version_out), _ptr(ws), _nbytes(ws),
+                                           _stream(stream)), "moe_chunked_forward_slots")
+
+
 def dense_linear_ws_bytes(rows, N, K) -> int:
     return int(lib().dense_linear_ws_bytes(rows, N, K))
 
@@ -205,7 +236,8 @@ def dense_linear_backward(fmt, q, s, N, K, block, R, rows, X, dY, dX, dR, ws, st
 def moe_permute_noalloc(dm, idx, rt: Routing, stream=None):
     _check(lib().moe_permute_noalloc(dm, _ptr(idx), ctypes.byref(rt), _stream(stream)),
            "moe_permute_noalloc",
-           "dense_linear_ws_bytes", "dense_linear_forward", "dense_linear_backward")
+           "dense_linear_ws_bytes", "dense_linear_forward", "dense_linear_backward",
+           "moe_adapter_publish", "moe_chunked_forward_slots")
 
 
 def moe_chunked_forward(dm, wts: Weights, adp, rt: Routing, X, chunk_C, mode, Y, ctx, ws,
