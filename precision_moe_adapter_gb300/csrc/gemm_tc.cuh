@@ -350,6 +350,13 @@ struct Pipe {
     static constexpr int kRawTma = kFp8 ? 8 : 6;   // raw ring stages
 #endif
     static constexpr int kRawBytes = kTmaRaw ? kRawTma * kRawTile : 0;
+    // With kProd weight-producer warps taking alternate K steps, each warp
+    // must always reuse its own raw slots: then a warp waiting on a slot's
+    // release barrier is never more than one phase behind it.  With an odd
+    // ring two warps share a slot, one can wait for a phase two completions
+    // ahead, and the parity test passes early (it re-arms the slot's
+    // transaction barrier while the tile is in use).
+    static_assert(kRawTma % kProd == 0, "raw ring size must be a multiple of the producer warps");
     static constexpr int kNumBars = 2 * kStagesA + 4 + 2 * kRawTma;
     static constexpr int kBarOff = kStagesA * kABytes + kStagesB * kBBytes;
     static constexpr int kBarBytes = 8 * kNumBars + 16;
@@ -609,6 +616,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     const int nft = (a.Mtot + a.m_tile - 1) / a.m_tile;
     const int n_items = (tend - tbeg) * nft;
     const int nk = a.K / kBK;
+    // barrier of K step g (one per A slot) and the parity of its use
+    auto fb = [&](uint32_t g) { return (int)(g % (uint32_t)kStages); };
+    auto fph = [&](uint32_t g) { return (uint32_t)((g / (uint32_t)kStages) & 1u); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -729,17 +739,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                 // MMAs (which also frees A slot s for the BF16 weight tiles)
                 if (g >= (uint32_t)kStagesB) {
                     const uint32_t gp = g - kStagesB;
-                    if (!(ok = mbar_wait(empty(gp % kStages), (gp / kStages) & 1, a.err, 1))) break;
+                    if (!(ok = mbar_wait(empty(fb(gp)), fph(gp), a.err, 1))) break;
                 }
+                const uint32_t fbar = full_a(fb(g));
                 if (lane == 0) {
-                    mbar_expect_tx(full_a(s), brows * kBK * 2 + (PP::kBf16 ? kABytes : 0));
+                    mbar_expect_tx(fbar, brows * kBK * 2 + (PP::kBf16 ? kABytes : 0));
                     for (int r0 = 0; r0 < brows;) {
                         const int left = brows - r0;
                         const CUtensorMap *tm = left >= 256 ? &tmB256 : left >= 128 ? &tmB128
                                               : left >= 64 ? &tmB64 : &tmB32;
                         const int rows = left >= 256 ? 256 : left >= 128 ? 128 : left >= 64 ? 64 : 32;
                         const int xb = KIND == GK_ROUTER ? (ks * kBK) % a.Kb : ks * kBK;
-                        tma_load_2d(sB0 + sb * kBBytes + r0 * kBK * 2, tm, xb, tl.row0 + r0, full_a(s));
+                        tma_load_2d(sB0 + sb * kBBytes + r0 * kBK * 2, tm, xb, tl.row0 + r0, fbar);
                         r0 += rows;
                     }
                     if constexpr (PP::kBf16) {
@@ -749,12 +760,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
 #pragma unroll
                             for (int qq = 0; qq < 4; ++qq) {
                                 tma_load_3d(sA0 + s * kABytes + (32 * qq) * 128, &tmA, ks * kBK,
-                                            f0 + 16 * qq, slot, full_a(s));
+                                            f0 + 16 * qq, slot, fbar);
                                 tma_load_3d(sA0 + s * kABytes + (32 * qq + 16) * 128, &tmA, ks * kBK,
-                                            a.I + f0 + 16 * qq, slot, full_a(s));
+                                            a.I + f0 + 16 * qq, slot, fbar);
                             }
                         } else {
-                            tma_load_3d(sA0 + s * kABytes, &tmA, ks * kBK, f0, slot, full_a(s));
+                            tma_load_3d(sA0 + s * kABytes, &tmA, ks * kBK, f0, slot, fbar);
                         }
                     }
                 }
@@ -784,8 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                 const uint32_t d = tmem + acc * (kTmemCols / 2);
                 for (int ks = 0; ks < nk; ++ks, ++g) {
                     const int s = g % kStages;
-                    const uint32_t ph = (g / kStages) & 1;
-                    if (!(ok = __all_sync(0xffffffffu, mbar_wait(full_a(s), ph, a.err, 3)))) break;
+                    if (!(ok = __all_sync(0xffffffffu, mbar_wait(full_a(fb(g)), fph(g), a.err, 3)))) break;
                     tc_fence_after();
                     // K step of 16: +32 B inside the K-major swizzle row, or two
                     // 8-row K groups (2 x 2048 B) of the MN-major tile
@@ -795,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
 #pragma unroll
                     for (int kk = 1; kk < kBK / 16; ++kk)
                         umma_warp(d, ad + kk * kAStep, bd + kk * (32 >> 4), idesc, 1u);
-                    umma_commit_warp(empty(s));
+                    umma_commit_warp(empty(fb(g)));
                 }
                 if (ok) umma_commit_warp(tfull(acc));
             }
@@ -850,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             bool ok = (uint32_t)grp >= total || compute(nc, cur);
             for (uint32_t g = grp; ok && g < total; g += kConvGroups) {
                 const int s = g % kStages;
-                if (!mbar_wait(empty(s), ((g / kStages) & 1) ^ 1, a.err, 5)) break;
+                if (!mbar_wait(empty(fb(g)), fph(g) ^ 1, a.err, 5)) break;
                 if constexpr (PP::kTrans)
                     Dequant<KIND, FMT>::store_t(tg, cur, sA0 + s * kABytes);
                 else
@@ -859,7 +869,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                 if (nc.j < total) ok = compute(nc, nxt);
                 fence_proxy_async();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(full_a(s));
+                if (lane == 0) mbar_arrive(full_a(fb(g)));
 #pragma unroll
                 for (int c = 0; c < kEPT / 8; ++c) cur[c] = nxt[c];
             }

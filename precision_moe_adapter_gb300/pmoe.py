@@ -235,9 +235,7 @@ def dense_linear_backward(fmt, q, s, N, K, block, R, rows, X, dY, dX, dR, ws, st
 
 def moe_permute_noalloc(dm, idx, rt: Routing, stream=None):
     _check(lib().moe_permute_noalloc(dm, _ptr(idx), ctypes.byref(rt), _stream(stream)),
-           "moe_permute_noalloc",
-           "dense_linear_ws_bytes", "dense_linear_forward", "dense_linear_backward",
-           "moe_adapter_publish", "moe_chunked_forward_slots")
+           "moe_permute_noalloc")
 
 
 def moe_chunked_forward(dm, wts: Weights, adp, rt: Routing, X, chunk_C, mode, Y, ctx, ws,
