@@ -35,7 +35,7 @@ from precision_moe_adapter_gb300 import inputs as gi  # noqa: E402
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="kimi_k2", choices=sorted(gi.CONFIGS))
@@ -123,7 +123,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -132,7 +132,7 @@ class ClockSampler:
     def __exit__(self, *a):
         self.out = ""
         if self.proc:
-            time.sleep(0.25)
+            time.sleep(0.06)
             self.proc.terminate()
             try:
                 self.out, _ = self.proc.communicate(timeout=5)
