@@ -51,7 +51,7 @@ bool make_rows_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t cols
 }
 
 bool make_bytes_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t row_bytes,
-                     int box_bytes, int box_rows, int swizzle_bytes)
+                     int box_bytes, int box_rows, int swizzle_bytes, int l2_promote)
 {
     EncodeTiled enc = encoder();
     if (!enc) return false;
@@ -62,9 +62,12 @@ bool make_bytes_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t row
     const CUtensorMapSwizzle swz = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
                                    : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                                                          : CU_TENSOR_MAP_SWIZZLE_NONE;
+    const CUtensorMapL2promotion pro = l2_promote == 256  ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                       : l2_promote == 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                       : l2_promote == 64  ? CU_TENSOR_MAP_L2_PROMOTION_L2_64B
+                                                           : CU_TENSOR_MAP_L2_PROMOTION_NONE;
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, pro, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool make_slots_tmap(CUtensorMap *m, const void *base, int64_t slots, int64_t rows, int64_t cols,

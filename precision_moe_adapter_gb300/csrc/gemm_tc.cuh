@@ -298,6 +298,7 @@ struct TcArgs {
     const int32_t *chunk_tiles;
     int c0, c1;
     int slot_index;
+    int scale_tma;              // backward kinds: scales by TMA (tmS) instead of cp.async
     uint16_t *out;
     uint16_t *ctx;
     int I;
@@ -317,7 +318,11 @@ struct TcArgs {
 //                   swizzle; one 4-byte scale word per row
 //   backward kinds: 64 stored rows x 128 columns (kRowBytes each), 64- or
 //                   128-byte TMA swizzle (conflict-free converter reads);
-//                   two 4-byte scale words per row
+//                   per row the 16 aligned scale bytes around the tile's
+//                   columns, by one TMA box with the tile when the scale
+//                   rows are whole 16-byte units (no per-lane copies to
+//                   compete with the epilogue's loads), else the words the
+//                   lanes copy
 // BF16 scratch weights come by TMA straight into the swizzled A stage.
 template <int KIND, int FMT>
 struct Pipe {
@@ -343,7 +348,7 @@ struct Pipe {
     static constexpr int kRawRows = kTrans ? 64 : 128;
     static constexpr int kRowBytes = kTrans ? (kFp8 ? 128 : 64) : (kFp8 ? 64 : 32);
     static constexpr int kScaleOff = kRawRows * kRowBytes;   // scale words after the data
-    static constexpr int kRawTile = kTrans ? (kScaleOff + 64 * 8 + 1023) & ~1023 : kScaleOff + 128 * 4;
+    static constexpr int kRawTile = kTrans ? (kScaleOff + 64 * 16 + 1023) & ~1023 : kScaleOff + 128 * 4;
 #ifdef PMOE_RAW_STAGES
     static constexpr int kRawTma = kFp8 ? 8 : PMOE_RAW_STAGES;
 #else
@@ -545,12 +550,12 @@ struct Dequant {
             return;
         }
         const uint8_t *row = rawt + k * PP::kRowBytes;
-        const uint32_t *sw = (const uint32_t *)(rawt + PP::kScaleOff + 8 * k);
+        const uint8_t *sw = rawt + PP::kScaleOff + 16 * k;   // stored row k's 16 scale bytes
         if (FMT == PMOE_W_FP8_B128_F32) {
             // 128-byte rows, 128-byte swizzle: chunk c sits at c ^ (k & 7)
             const uint4 q0 = *(const uint4 *)(row + (((2 * mq) ^ (k & 7)) << 4));
             const uint4 q1 = *(const uint4 *)(row + (((2 * mq + 1) ^ (k & 7)) << 4));
-            const float sc = __uint_as_float(sw[0]);
+            const float sc = *(const float *)sw;
             out[0] = chunk8(make_uint2(q0.x, q0.y), sc);
             out[1] = chunk8(make_uint2(q0.z, q0.w), sc);
             out[2] = chunk8(make_uint2(q1.x, q1.y), sc);
@@ -558,13 +563,17 @@ struct Dequant {
         } else {
             // 64-byte rows, 64-byte swizzle: chunk c sits at c ^ ((k >> 1) & 3)
             const uint4 q = *(const uint4 *)(row + ((mq ^ ((k >> 1) & 3)) << 4));
+            // scale group f0/32 + mq: BF16 index (f0/32 & 7) + mq (INT4); byte
+            // (f0/32 & 15) + mq (MXFP4 by TMA), or ((row * Kst/32 + f0/32) & 3)
+            // + mq of the two aligned words the lanes copied
             uint32_t sb;
             if (FMT == PMOE_W_INT4_G32_BF16) {
-                sb = (sw[mq >> 1] >> (16 * (mq & 1))) & 0xFFFFu;
+                sb = *(const uint16_t *)(sw + 2 * (((f0 >> 5) & 7) + mq));
             } else {
                 const int64_t srow = (int64_t)ks * kBK + k;
-                const int byte = (int)((srow * (a.Kst >> 5)) & 3) + mq;
-                sb = (sw[byte >> 2] >> (8 * (byte & 3))) & 0xFFu;
+                const int byte = a.scale_tma ? ((f0 >> 5) & 15) + mq
+                                             : (int)((srow * (a.Kst >> 5) + (f0 >> 5)) & 3) + mq;
+                sb = sw[byte];
             }
             out[0] = chunk4(q.x, sb);
             out[1] = chunk4(q.y, sb);
@@ -590,6 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                                                          const __grid_constant__ CUtensorMap tmB64,
                                                          const __grid_constant__ CUtensorMap tmB32,
                                                          const __grid_constant__ CUtensorMap tmA,
+                                                         const __grid_constant__ CUtensorMap tmS,
                                                          const TcArgs a)
 {
     using PP = Pipe<KIND, FMT>;
@@ -674,18 +684,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                     if constexpr (PP::kTrans) {
                         // 64 stored rows ks*64 .. +63, columns f0 .. f0+127
                         if (lane == 0) {
-                            mbar_expect_tx(raw_full(r), 64 * PP::kRowBytes);
+                            mbar_expect_tx(raw_full(r), 64 * PP::kRowBytes + (a.scale_tma ? 64 * 16 : 0));
                             tma_load_2d(dst, &tmA, PP::kFp8 ? f0 : f0 >> 1,
                                         (int)(widx * a.Nst) + ks * kBK, raw_full(r));
+                            if (a.scale_tma) {
+                                // 16 aligned bytes of scale groups around f0/32, 64 stored rows
+                                const int x = FMT == PMOE_W_INT4_G32_BF16 ? ((f0 >> 5) & ~7) * 2 : (f0 >> 5) & ~15;
+                                tma_load_2d(dst + PP::kScaleOff, &tmS, x, (int)(widx * a.Nst) + ks * kBK,
+                                            raw_full(r));
+                            }
                         }
                         // columns past Mtot (a 64-wide last tile) get no scales
                         const bool full = f0 + 128 <= a.Mtot;
 #pragma unroll
                         for (int i = 0; i < 2; ++i) {
+                            if (a.scale_tma) break;
                             const int k = lane + 32 * i;
                             const int64_t row = (int64_t)ks * kBK + k;
                             const uint8_t *src = ws + Dequant<KIND, FMT>::scale_word_t(a, row, f0);
-                            const uint32_t sd = dst + PP::kScaleOff + 8 * k;
+                            // INT4: the 4 BF16 at index f0/32 & 7 of the row's 16 bytes
+                            const uint32_t sd = dst + PP::kScaleOff + 16 * k +
+                                                (FMT == PMOE_W_INT4_G32_BF16 ? 2 * ((f0 >> 5) & 7) : 0);
                             cpa4(sd, src);
                             const bool second = FMT == PMOE_W_INT4_G32_BF16 ? full
                                               : FMT == PMOE_W_MXFP4_G32_E8M0

@@ -13,7 +13,7 @@ bool make_rows_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t cols
 // uint8 [rows, row_bytes] tensor, box of box_rows x box_bytes, swizzle of
 // swizzle_bytes (0: none, 64 or 128; box_bytes must then equal it)
 bool make_bytes_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t row_bytes,
-                     int box_bytes, int box_rows, int swizzle_bytes);
+                     int box_bytes, int box_rows, int swizzle_bytes, int l2_promote = 256);
 // BF16 scratch slots [slots][rows][cols], box 64 cols x box_rows, 128-byte swizzle
 bool make_slots_tmap(CUtensorMap *m, const void *base, int64_t slots, int64_t rows, int64_t cols,
                      int64_t slot_bytes, int box_rows);
@@ -43,7 +43,20 @@ bool launch_kind(const CUtensorMap (&tmB)[4], const TcArgs &a, int64_t nmat, cud
                              KIND == GK_FWD_GU ? 16 : 128))
             return false;
     }
-    k_gemm_tc<KIND, FMT><<<num_sms(), kThreads, PP::kSmem, st>>>(tmB[0], tmB[1], tmB[2], tmB[3], tmA, a);
+    // Backward kinds: the scales by TMA where their rows are whole 16-byte
+    // units and one tensor spans every expert; FP8 (one word per block)
+    // and other shapes go by cp.async.
+    CUtensorMap tmS;
+    memset(&tmS, 0, sizeof tmS);
+    TcArgs b = a;
+    b.scale_tma = 0;
+    if constexpr (PP::kTrans && FMT != PMOE_W_FP8_B128_F32) {
+        const int64_t srb = FMT == PMOE_W_INT4_G32_BF16 ? (a.Kst >> 5) * 2 : a.Kst >> 5;
+        if (srb % 16 == 0 && ((uintptr_t)a.ws & 15) == 0 && a.ws_stride == a.Nst * srb &&
+            make_bytes_tmap(&tmS, a.ws, nmat * a.Nst, srb, 16, kBK, 0))
+            b.scale_tma = 1;
+    }
+    k_gemm_tc<KIND, FMT><<<num_sms(), kThreads, PP::kSmem, st>>>(tmB[0], tmB[1], tmB[2], tmB[3], tmA, tmS, b);
     note_launch();
     return true;
 }
