@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(128) k_cayley_warp(int nblk, const float *__re
 }
 
 // b = 64 with two warps per block matrix (32 rows each), so a lane keeps
-// 8 x 8 elements (about 100 registers instead of 255) and four times as
+// 8 x 8 elements (about 140 registers instead of 255) and three times as
 // many warps fit an SM.  Lane (row group rg = lane / 8, column group
 // cg = lane % 8) of warp half h keeps rows 32h + 8rg .. +7, columns
 // 8cg .. +7.  For pivot k the warp holding row k scales it and puts it in
@@ -185,6 +185,27 @@ __global__ void __launch_bounds__(128) k_cayley_pair64(int nblk, const float *__
             v[i][j + 3] = (row == col + 3 ? 1.f : 0.f) - sv.w;
         }
     }
+    // Software-pipelined over pivots: while pivot k is applied, row k+1 and
+    // column k+1 are finished first, so pivot k+1's multipliers (shuffles)
+    // and scaled row (shared memory) are on their way while the other 49
+    // updates of pivot k issue.  Each element still takes the same operations
+    // in the same order.
+    float f[8];
+    {   // pivot 0: multipliers and scaled row
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = __shfl_sync(0xffffffffu, v[i][0], lane & ~7);
+        if (half == 0) {
+            const float piv = __shfl_sync(0xffffffffu, v[0][0], 0);
+            const float p = 1.f / piv;
+            if (rg == 0) {
+                float *pr = prow[mloc][0];
+                *(float4 *)(pr + 8 * cg) = make_float4(v[0][0] * p, v[0][1] * p, v[0][2] * p, v[0][3] * p);
+                *(float4 *)(pr + 8 * cg + 4) = make_float4(v[0][4] * p, v[0][5] * p, v[0][6] * p, v[0][7] * p);
+                if (cg == 0) pr[B] = p;
+            }
+        }
+        asm volatile("bar.sync %0, 64;" ::"r"(1 + mloc) : "memory");
+    }
     for (int kb = 0; kb < 8; ++kb) {       // pivots k = 8 kb .. 8 kb + 7
         const int owner = kb >> 2, g = kb & 3;
         const bool in_g = half == owner && rg == g;
@@ -192,39 +213,64 @@ __global__ void __launch_bounds__(128) k_cayley_pair64(int nblk, const float *__
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
             const int k = 8 * kb + jj;
-            float *pr = prow[mloc][k & 1];
-            float f[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) f[i] = __shfl_sync(0xffffffffu, v[i][jj], (lane & ~7) | kb);
-            if (half == owner) {
-                const float piv = __shfl_sync(0xffffffffu, v[jj][jj], (g << 3) | kb);
-                const float p = 1.f / piv;
-                if (rg == g) {
-                    *(float4 *)(pr + 8 * cg) =
-                        make_float4(v[jj][0] * p, v[jj][1] * p, v[jj][2] * p, v[jj][3] * p);
-                    *(float4 *)(pr + 8 * cg + 4) =
-                        make_float4(v[jj][4] * p, v[jj][5] * p, v[jj][6] * p, v[jj][7] * p);
-                    if (cg == kb) pr[B] = p;
-                }
-            }
-            asm volatile("bar.sync %0, 64;" ::"r"(1 + mloc) : "memory");
+            const int j1 = (jj + 1) & 7;                      // local index of pivot k+1
+            const int kb1 = kb + (jj == 7);
+            const float *pr = prow[mloc][k & 1];
             const float4 q0 = *(const float4 *)(pr + 8 * cg), q1 = *(const float4 *)(pr + 8 * cg + 4);
             const float p = pr[B];
             const float ps[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
             if (in_g) f[jj] = 0.f;   // the pivot row is only rescaled
+            // 1. row j1 and column j1 of pivot k's result
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j1][j] = fmaf(-f[j1], ps[j], v[j1][j]);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
+                if (i != j1) v[i][j1] = fmaf(-f[i], ps[j1], v[i][j1]);
+            if (in_g) v[jj][j1] = ps[j1];
+            if (in_h) v[j1][jj] = fmaf(-f[j1], p, 0.f);
+            // 2. pivot k+1: multipliers, and the owner's scaled row
+            float fn[8];
+            if (kb1 < 8) {
+                const int owner1 = kb1 >> 2, g1 = kb1 & 3;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) v[i][j] = fmaf(-f[i], ps[j], v[i][j]);
+                for (int i = 0; i < 8; ++i) fn[i] = __shfl_sync(0xffffffffu, v[i][j1], (lane & ~7) | kb1);
+                if (half == owner1) {
+                    const float piv = __shfl_sync(0xffffffffu, v[j1][j1], (g1 << 3) | kb1);
+                    const float p1 = 1.f / piv;
+                    if (rg == g1) {
+                        float *pn = prow[mloc][(k + 1) & 1];
+                        *(float4 *)(pn + 8 * cg) =
+                            make_float4(v[j1][0] * p1, v[j1][1] * p1, v[j1][2] * p1, v[j1][3] * p1);
+                        *(float4 *)(pn + 8 * cg + 4) =
+                            make_float4(v[j1][4] * p1, v[j1][5] * p1, v[j1][6] * p1, v[j1][7] * p1);
+                        if (cg == kb1) pn[B] = p1;
+                    }
+                }
+            }
+            // 3. the rest of pivot k
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (i == j1) continue;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j != j1) v[i][j] = fmaf(-f[i], ps[j], v[i][j]);
+            }
             if (in_g) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) v[jj][j] = ps[j];
+                for (int j = 0; j < 8; ++j)
+                    if (j != j1) v[jj][j] = ps[j];
             }
             if (in_h) {   // column k becomes column k of the inverse
 #pragma unroll
-                for (int i = 0; i < 8; ++i) v[i][jj] = fmaf(-f[i], p, 0.f);
+                for (int i = 0; i < 8; ++i)
+                    if (i != j1) v[i][jj] = fmaf(-f[i], p, 0.f);
                 if (in_g) v[jj][jj] = p;
             }
+            if (kb1 < 8) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) f[i] = fn[i];
+            }
+            asm volatile("bar.sync %0, 64;" ::"r"(1 + mloc) : "memory");
         }
     }
     if (!live) return;
