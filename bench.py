@@ -51,8 +51,10 @@ def parse():
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch
 # of the GEMM classes, from one ncu capture of this kernel version on the
 # default workload (profiles/k_gemm_tc_kimi_k2_int4.md); None elsewhere.
-TRAFFIC_BYTES = {("kimi_k2", "fused", "gemm_gate_up"): 8.564e9,
-                 ("kimi_k2", "fused", "gemm_bwd_dx"): 7.800e9}
+TRAFFIC_BYTES = {("kimi_k2", "fused", "gemm_gate_up"): 8.589e9,
+                 ("kimi_k2", "fused", "gemm_down"): 4.359e9,
+                 ("kimi_k2", "fused", "gemm_bwd_g"): 5.325e9,
+                 ("kimi_k2", "fused", "gemm_bwd_dx"): 8.055e9}
 
 
 def max_over_ranks(x: float) -> float:
@@ -341,15 +343,16 @@ def main():
         torch.cuda.synchronize()
     launches = pmoe.pmoe_launch_count() - n0
     ms = ev0.elapsed_time(ev1)
+    # per-launch device times of the timed region only
+    kt = {name: pmoe.pmoe_kernel_time(i) for i, name in enumerate(
+        ("gemm_gate_up", "gemm_down", "gemm_bwd_g", "gemm_bwd_dx", "router"))}
+    pmoe.pmoe_kernel_timing(False)
     # one extra step with events between the calls: where the step's time goes
     phase_ev.clear()
     step(X, dY, timed=True)
     torch.cuda.synchronize()
     for (n_, e_), (_, f_) in zip(phase_ev[:-1], phase_ev[1:]):
         phase_ms[n_] += e_.elapsed_time(f_)
-    kt = {name: pmoe.pmoe_kernel_time(i) for i, name in enumerate(
-        ("gemm_gate_up", "gemm_down", "gemm_bwd_g", "gemm_bwd_dx", "router"))}
-    pmoe.pmoe_kernel_timing(False)
     ms = max_over_ranks(ms)
     ms_step = ms / args.steps
     tokens_per_s = whole_job_rate(cfg.T, args.steps, ms, world)
