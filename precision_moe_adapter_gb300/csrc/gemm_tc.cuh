@@ -874,23 +874,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                 if (lane == 0) mbar_arrive(raw_empty(r));
                 return true;
             };
-            uint4 cur[kEPT / 8], nxt[kEPT / 8];
+            uint4 bufa[kEPT / 8], bufb[kEPT / 8];
             Cur nc = at((uint32_t)grp);
-            bool ok = (uint32_t)grp >= total || compute(nc, cur);
-            for (uint32_t g = grp; ok && g < total; g += kConvGroups) {
+            bool ok = (uint32_t)grp >= total || compute(nc, bufa);
+            // one step of the group: store step g's chunks (cur), convert the
+            // group's next step into nxt, publish step g
+            auto body = [&](uint32_t g, const uint4 (&cur)[kEPT / 8], uint4 (&nxt)[kEPT / 8]) -> bool {
                 const int s = g % kStages;
-                if (!mbar_wait(empty(fb(g)), fph(g) ^ 1, a.err, 5)) break;
+                if (!mbar_wait(empty(fb(g)), fph(g) ^ 1, a.err, 5)) return false;
                 if constexpr (PP::kTrans)
                     Dequant<KIND, FMT>::store_t(tg, cur, sA0 + s * kABytes);
                 else
                     Dequant<KIND, FMT>::template store_tma<kEPT>(tg, cur, sA0 + s * kABytes);
                 advance(nc);
-                if (nc.j < total) ok = compute(nc, nxt);
+                // converting the next step before publishing this one lets
+                // the stores drain meanwhile (publishing first measured slower)
+                const bool okc = nc.j >= total || compute(nc, nxt);
                 fence_proxy_async();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(full_a(fb(g)));
-#pragma unroll
-                for (int c = 0; c < kEPT / 8; ++c) cur[c] = nxt[c];
+                return okc;
+            };
+            // unrolled by two so the converted chunks alternate between two
+            // buffers instead of being copied
+            for (uint32_t g = grp; ok && g < total; g += 2 * kConvGroups) {
+                ok = body(g, bufa, bufb);
+                if (!ok || g + kConvGroups >= total) break;
+                ok = body(g + kConvGroups, bufb, bufa);
             }
         }
     } else {
