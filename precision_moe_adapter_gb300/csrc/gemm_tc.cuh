@@ -163,24 +163,21 @@ __device__ __forceinline__ uint32_t idesc_bf16(int M, int N, bool a_mn = false)
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                     uint32_t accum)
+// Called by a whole converged warp, so the issue loop's operands stay
+// uniform: one K step of 64, i.e. four MMAs of K = 16 (descriptors a0..a3,
+// b0..b3) and the commit of `bar`, issued by one elected lane.
+__device__ __forceinline__ void umma_step_warp(uint32_t d_tmem, const uint64_t (&a)[4], const uint64_t (&b)[4],
+                                               uint32_t idesc, uint32_t accum, uint32_t bar)
 {
     asm volatile(
-        "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(
-            d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accum)
-        : "memory");
-}
-// The same two, called by a whole converged warp: one elected lane issues.
-// Keeping the warp converged lets the issue loop's operands stay uniform.
-__device__ __forceinline__ void umma_warp(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                          uint32_t accum)
-{
-    asm volatile(
-        "{ .reg .pred e, p; elect.sync _|e, 0xffffffff; setp.ne.b32 p, %4, 0;\n"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accum)
+        "{ .reg .pred e, p, t; elect.sync _|e, 0xffffffff; setp.ne.b32 p, %9, 0; setp.eq.b32 t, %9, %9;\n"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %10, p;\n"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %10, t;\n"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %10, t;\n"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %10, t;\n"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%11]; }" ::"r"(d_tmem),
+        "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]),
+        "r"(accum), "r"(idesc), "r"(bar)
         : "memory");
 }
 __device__ __forceinline__ void umma_commit_warp(uint32_t bar)
@@ -189,11 +186,6 @@ __device__ __forceinline__ void umma_commit_warp(uint32_t bar)
         "{ .reg .pred e; elect.sync _|e, 0xffffffff;\n"
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0]; }" ::"r"(bar)
         : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint32_t bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
 }
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
 {
@@ -820,11 +812,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                     // 8-row K groups (2 x 2048 B) of the MN-major tile
                     const uint64_t ad = adesc0 + (uint32_t)(s * (kABytes >> 4));
                     const uint64_t bd = bdesc0 + (uint32_t)((g % kStagesB) * (kBBytes >> 4));
-                    umma_warp(d, ad, bd, idesc, ks != 0);
-#pragma unroll
-                    for (int kk = 1; kk < kBK / 16; ++kk)
-                        umma_warp(d, ad + kk * kAStep, bd + kk * (32 >> 4), idesc, 1u);
-                    umma_commit_warp(empty(fb(g)));
+                    static_assert(kBK == 64, "four MMAs of K = 16 per step");
+                    const uint64_t av[4] = {ad, ad + kAStep, ad + 2 * kAStep, ad + 3 * kAStep};
+                    const uint64_t bv[4] = {bd, bd + 2, bd + 4, bd + 6};
+                    umma_step_warp(d, av, bv, idesc, ks != 0, empty(fb(g)));
                 }
                 if (ok) umma_commit_warp(tfull(acc));
             }
