@@ -447,12 +447,26 @@ struct Dequant {
             o.z = prmt(p[0], p[1], 0x7632);
             o.w = prmt(p[2], p[3], 0x7632);
         } else {
-            const float sc = e8m0_value(sbits);
+            // E2M1 by table: the BF16 pattern of |code| (0, 0.5, 1, 1.5, 2,
+            // 3, 4, 6) as two 8-entry byte tables (high and low byte) looked
+            // up by prmt with the 3 magnitude bits, the code's sign bit moved
+            // to bit 7 of the high byte, then one BF16 multiply by the E8M0
+            // scale 2^(u-127) (a power of two: a single rounding of the exact
+            // product)
+            const uint32_t sb = sbits == 0u ? 0x0040u : sbits == 255u ? 0x7FC0u : sbits << 7;
+            const uint32_t s2 = sb | (sb << 16);
+            const uint32_t ws = w << 4;   // bit 7 of byte k: sign of element 2k
             uint32_t r[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                r[j] = pack_bf2(__fmul_rn(e2m1_value((w >> (8 * j)) & 15u), sc),
-                                __fmul_rn(e2m1_value((w >> (8 * j + 4)) & 15u), sc));
+            for (int h = 0; h < 2; ++h) {   // elements 4h .. 4h+3
+                const uint32_t sel = (h ? w >> 16 : w) & 0x7777u;
+                const uint32_t hi = prmt(0x3F3F3F00u, 0x40404040u, sel);
+                const uint32_t lo = prmt(0xC0800000u, 0xC0804000u, sel);
+                const uint32_t sg = prmt(ws, w, h ? 0x7362u : 0x5140u);
+                const uint32_t hs = hi | (sg & 0x80808080u);
+                r[2 * h] = bf2_mul(prmt(lo, hs, 0x5140u), s2);
+                r[2 * h + 1] = bf2_mul(prmt(lo, hs, 0x7362u), s2);
+            }
             o = make_uint4(r[0], r[1], r[2], r[3]);
         }
         return o;
