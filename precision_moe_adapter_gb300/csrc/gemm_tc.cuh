@@ -960,18 +960,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                             hts[j] = (fl && j8 + j < ncol)
                                          ? a.ht[(int64_t)(tl.row0 + c0 + j8 + j) * a.Mtot + f]
                                          : 0;
+                        float part[8];   // G * h~ of the lane's feature, per column
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const int jj = j8 + j;
                             const float wr = __shfl_sync(0xffffffffu, w_lane, jj);
                             const int64_t r = tl.row0 + c0 + jj;
-                            float part = fl ? v[jj] * bf2f(hts[j]) : 0.f;
+                            part[j] = fl ? v[jj] * bf2f(hts[j]) : 0.f;
                             if (fl && jj < ncol) a.out[r * a.Mtot + f] = f2bf(wr * v[jj]);
-#pragma unroll
-                            for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-                            if (fl && lane == 0 && jj < ncol)
-                                a.dtw_part[r * (a.Mtot / 32) + (f0 + 32 * q) / 32] = part;
                         }
+                        // sum over the warp's 32 features for the 8 columns at once
+                        // (reduce-scatter over lane distances 16, 8, 4): lane l then
+                        // holds column (l >> 2) & 7 over the lanes sharing bits 2-4
+#pragma unroll
+                        for (int h = 4; h >= 1; h >>= 1) {
+                            const bool up = lane & (4 * h);
+#pragma unroll
+                            for (int i = 0; i < h; ++i) {
+                                const float send = up ? part[i] : part[i + h];
+                                const float keep = up ? part[i + h] : part[i];
+                                part[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4 * h);
+                            }
+                        }
+                        float sum = part[0] + __shfl_xor_sync(0xffffffffu, part[0], 1);
+                        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                        const int jj = j8 + ((lane >> 2) & 7);
+                        if ((lane & 3) == 0 && jj < ncol && f0 + 32 * q < a.Mtot)
+                            a.dtw_part[(int64_t)(tl.row0 + c0 + jj) * (a.Mtot / 32) + (f0 + 32 * q) / 32] = sum;
                     }
                 } else if (KIND == GK_ROUTER) {
                     const int f = f0 + 32 * q + lane;
