@@ -196,8 +196,9 @@ struct PermWs {
     DevErr *err;
     int32_t *hist;
     float *logits;
-    uint16_t *wr3;        // router weight split [E, 3d] bf16
-    Tile *rtiles;         // router token tiles
+    uint16_t *wr3;        // router weight split, [splits][E][3d / splits] bf16
+    float *rpart;         // router partials [splits][T][E] f32
+    Tile *rtiles;         // router token tiles of every split
     int32_t *rchunk;      // [2]
 };
 static PermWs carve_perm(void *ws, const pmoe_dims &d, size_t *bytes)
@@ -208,7 +209,8 @@ static PermWs carve_perm(void *ws, const pmoe_dims &d, size_t *bytes)
     w.hist = c.take<int32_t>(permute_ws_bytes(d.T * d.k, d.E) / sizeof(int32_t));
     w.logits = c.take<float>((int64_t)d.T * d.E);
     w.wr3 = c.take<uint16_t>((int64_t)d.E * 3 * d.d);
-    w.rtiles = c.take<Tile>(cdiv(d.T > 0 ? d.T : 1, 16));
+    w.rpart = c.take<float>((int64_t)router_splits(d.d) * d.T * d.E);
+    w.rtiles = c.take<Tile>(cdiv(d.T > 0 ? d.T : 1, 16) * router_splits(d.d));
     w.rchunk = c.take<int32_t>(2);
     if (bytes) *bytes = c.off;
     return w;
@@ -319,26 +321,32 @@ pmoe_status moe_route(pmoe_dims dims, const void *X, const float *Wr, const floa
     if (dims.T == 0) return PMOE_OK;
     {
         ScopedTimer tm(PMOE_KT_ROUTER, stream);
-        const int rows = router_tile_rows(dims.T, dims.E, gemm_num_sms());
+        // K splits (a function of d alone): every split is one matrix of
+        // [E, 3d / splits] and writes its own partial logits
+        const int splits = router_splits(dims.d);
+        const int ks = 3 * dims.d / splits;
+        const int rows = router_tile_rows(dims.T, dims.E, splits, gemm_num_sms());
         launch_router_prep(dims.T, dims.d, dims.E, Wr, pw.wr3, pw.rtiles, pw.rchunk, rows, stream);
         GemmArgs g{};
         g.kind = GK_ROUTER;
         g.fmt = kFmtBF16;
         g.wq = (const uint8_t *)pw.wr3;
-        g.wq_stride = (int64_t)dims.E * 3 * dims.d * 2;
+        g.wq_stride = (int64_t)dims.E * ks * 2;
         g.Nst = dims.E;
-        g.Kst = 3 * (int64_t)dims.d;
-        g.nmat = 1;
+        g.Kst = ks;
+        g.nmat = splits;
         g.A = (const uint16_t *)X;
-        g.K = 3 * dims.d;
+        g.K = ks;
         g.Kb = dims.d;
         g.Nout = dims.E;
         g.tiles = pw.rtiles;
         g.chunk_tiles = pw.rchunk;
         g.c0 = 0;
         g.c1 = 1;
-        g.outf = pw.logits;
+        g.outf = pw.rpart;
+        g.outf_split = (int64_t)dims.T * dims.E;
         if (!launch_gemm_tc(g, dims.T, pw.err, stream)) return PMOE_ERR_CUDA;
+        launch_router_reduce(dims.T, dims.E, splits, pw.rpart, pw.logits, stream);
     }
     launch_route_topk(dims.T, dims.E, dims.k, pw.logits, bias, idx, w, logits, stream);
     return launched(stream);

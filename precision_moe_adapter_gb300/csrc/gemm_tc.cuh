@@ -299,6 +299,7 @@ struct TcArgs {
     const uint16_t *ht;
     float *dtw_part;
     float *outf;
+    int64_t outf_split;         // router: elements between the partials of two K splits
     DevErr *err;
 };
 
@@ -777,7 +778,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                         const CUtensorMap *tm = left >= 256 ? &tmB256 : left >= 128 ? &tmB128
                                               : left >= 64 ? &tmB64 : &tmB32;
                         const int rows = left >= 256 ? 256 : left >= 128 ? 128 : left >= 64 ? 64 : 32;
-                        const int xb = KIND == GK_ROUTER ? (ks * kBK) % a.Kb : ks * kBK;
+                        // router: split widx covers K steps widx*nk .. of the
+                        // [X | X | X] operand of length 3d
+                        const int xb = KIND == GK_ROUTER ? (int)((((int64_t)widx * nk + ks) * kBK) % a.Kb) : ks * kBK;
                         tma_load_2d(sB0 + sb * kBBytes + r0 * kBK * 2, tm, xb, tl.row0 + r0, fbar);
                         r0 += rows;
                     }
@@ -997,7 +1000,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const int col = c0 + j;
-                            if (col < tl.nrows) a.outf[(int64_t)(tl.row0 + col) * a.Mtot + f] = v[j];
+                            if (col < tl.nrows)
+                                a.outf[(int64_t)tl.expert * a.outf_split + (int64_t)(tl.row0 + col) * a.Mtot + f] = v[j];
                         }
                     }
                 } else {

@@ -94,6 +94,7 @@ bool launch_fmt(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st)
     a.ht = g.ht;
     a.dtw_part = g.dtw_part;
     a.outf = g.outf;
+    a.outf_split = g.outf_split;
     a.err = err;
     switch (g.kind) {
     case GK_FWD_GU: return launch_kind<GK_FWD_GU, FMT>(tm, a, g.nmat, st);

@@ -15,9 +15,14 @@ bool dims_ok(const pmoe_dims &d);
 // route_permute.cu
 // Wr [d, E] f32 -> WrT3 [E, 3d] bf16 with WrT3[e][s*d + c] the s-th term of
 // the exact three-term BF16 split of Wr[c][e]; and the router's token tiles.
+// Router K splits: the length-3d contraction runs as router_splits(d) parts
+// of 3d / router_splits(d) columns each (a function of d alone, so a token's
+// logits do not depend on the batch); their partials are summed in order.
+int router_splits(int d);
+void launch_router_reduce(int T, int E, int splits, const float *part, float *logits, cudaStream_t st);
 void launch_router_prep(int T, int d, int E, const float *Wr, uint16_t *WrT3, Tile *tiles,
                         int32_t *chunk_tiles, int tile_rows, cudaStream_t st);
-int router_tile_rows(int T, int E, int num_sms);
+int router_tile_rows(int T, int E, int splits, int num_sms);
 void launch_route_topk(int T, int E, int k, const float *logits, const float *bias, int32_t *idx,
                        float *w, float *logits_out, cudaStream_t st);
 size_t permute_ws_bytes(int P, int E);
@@ -72,7 +77,8 @@ struct GemmArgs {
     const int32_t *perm;
     const uint16_t *ht;      // BWD_G: h~ [P, I]
     float *dtw_part;         // BWD_G: [P, I/32]
-    float *outf;             // ROUTER: [P, Nout] f32
+    float *outf;             // ROUTER: [splits][P, Nout] f32 partials
+    int64_t outf_split;      // ROUTER: P * Nout (elements between two splits' partials)
 };
 // tcgen05 grouped GEMM (returns false if the request cannot be
 // launched, e.g. the TMA descriptor could not be encoded)

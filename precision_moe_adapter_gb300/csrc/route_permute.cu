@@ -343,12 +343,15 @@ void launch_offsets_to_active(int E, int rows, const int32_t *offsets, int32_t *
 // FP32, and the three terms hold all 24 bits of the FP32 value).  The
 // logits X Wr = [X | X | X] [hi; mid; lo] are then one BF16 contraction of
 // length 3d whose products are exact and whose sums are FP32.
-__global__ void __launch_bounds__(256) k_router_split(int d, int E, const float *__restrict__ Wr,
-                                                      uint16_t *__restrict__ WrT3)
+// The split terms are stored split-major: K split s of the length-3d row of
+// expert e is row e of matrix s, [splits][E][3d / splits].
+__global__ void __launch_bounds__(256) k_router_split(int d, int E, int splits, const float *__restrict__ Wr,
+                                                      uint16_t *__restrict__ WrS)
 {
     __shared__ float t[32][33];
     const int c0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int ks = 3 * d / splits;
     for (int i = ty; i < 32; i += 8) {
         const int c = c0 + i, e = e0 + tx;
         t[i][tx] = (c < d && e < E) ? Wr[(int64_t)c * E + e] : 0.f;
@@ -362,48 +365,72 @@ __global__ void __launch_bounds__(256) k_router_split(int d, int E, const float 
         const float r1 = w - bf2f(hi);
         const uint16_t mid = f2bf(r1);
         const uint16_t lo = f2bf(r1 - bf2f(mid));
-        uint16_t *row = WrT3 + (int64_t)e * 3 * d;
-        row[c] = hi;
-        row[d + c] = mid;
-        row[2 * d + c] = lo;
+        const uint16_t term[3] = {hi, mid, lo};
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+            const int kk = q * d + c;   // column of the length-3d row
+            WrS[((int64_t)(kk / ks) * E + e) * ks + kk % ks] = term[q];
+        }
     }
 }
-
-__global__ void k_router_tiles(int T, int rows, Tile *__restrict__ tiles, int32_t *__restrict__ chunk_tiles)
+// token tiles of every K split: tile i is split i / n, token rows (i % n) * rows ..
+__global__ void k_router_tiles(int T, int rows, int splits, Tile *__restrict__ tiles,
+                               int32_t *__restrict__ chunk_tiles)
 {
     const int n = (T + rows - 1) / rows;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    for (int i = threadIdx.x; i < n * splits; i += blockDim.x) {
         Tile tl;
-        tl.expert = 0;
-        tl.row0 = i * rows;
-        tl.nrows = min(rows, T - i * rows);
+        tl.expert = i / n;
+        tl.row0 = (i % n) * rows;
+        tl.nrows = min(rows, T - (i % n) * rows);
         tl.chunk = 0;
         tiles[i] = tl;
     }
     if (threadIdx.x == 0) {
         chunk_tiles[0] = 0;
-        chunk_tiles[1] = n;
+        chunk_tiles[1] = n * splits;
     }
 }
-
-// Token rows per tile: enough tiles to give every SM one work item (three
-// 128-expert feature tiles at E = 384), multiples of 16, at most 256.
-int router_tile_rows(int T, int E, int num_sms)
+// logits = the splits' partials summed in split order
+__global__ void __launch_bounds__(256) k_router_reduce(int64_t n, int splits, const float *__restrict__ part,
+                                                       float *__restrict__ logits)
+{
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        float s = part[i];
+        for (int q = 1; q < splits; ++q) s += part[q * n + i];
+        logits[i] = s;
+    }
+}
+int router_splits(int d)
+{
+    const int steps = d / 64;   // K steps of one term
+    return 3 * (steps % 4 == 0 ? 4 : steps % 2 == 0 ? 2 : 1);
+}
+// Token rows per tile: enough work items to give every SM one (feature
+// tiles of 128 experts times the K splits), multiples of 16, at most 256.
+int router_tile_rows(int T, int E, int splits, int num_sms)
 {
     const int64_t nft = cdiv(E, 128);
-    int64_t r = cdiv((int64_t)T * nft, num_sms > 0 ? num_sms : 1);
+    int64_t r = cdiv((int64_t)T * nft * splits, num_sms > 0 ? num_sms : 1);
     r = (r + 15) & ~(int64_t)15;
     return (int)std::min<int64_t>(256, std::max<int64_t>(16, r));
 }
-
-void launch_router_prep(int T, int d, int E, const float *Wr, uint16_t *WrT3, Tile *tiles,
-                        int32_t *chunk_tiles, int tile_rows, cudaStream_t st)
+void launch_router_reduce(int T, int E, int splits, const float *part, float *logits, cudaStream_t st)
 {
-    dim3 grid((unsigned)cdiv(d, 32), (unsigned)cdiv(E, 32));
-    k_router_split<<<grid, 256, 0, st>>>(d, E, Wr, WrT3);
-    note_launch();
-    k_router_tiles<<<1, 256, 0, st>>>(T, tile_rows, tiles, chunk_tiles);
+    const int64_t n = (int64_t)T * E;
+    if (n <= 0) return;
+    const int grid = (int)std::min<int64_t>(cdiv(n, 256), 152 * 8);
+    k_router_reduce<<<grid, 256, 0, st>>>(n, splits, part, logits);
     note_launch();
 }
-
+void launch_router_prep(int T, int d, int E, const float *Wr, uint16_t *WrS, Tile *tiles,
+                        int32_t *chunk_tiles, int tile_rows, cudaStream_t st)
+{
+    const int splits = router_splits(d);
+    dim3 grid((unsigned)cdiv(d, 32), (unsigned)cdiv(E, 32));
+    k_router_split<<<grid, 256, 0, st>>>(d, E, splits, Wr, WrS);
+    note_launch();
+    k_router_tiles<<<1, 256, 0, st>>>(T, tile_rows, splits, tiles, chunk_tiles);
+    note_launch();
+}
 }  // namespace pmoe
