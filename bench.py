@@ -51,10 +51,10 @@ def parse():
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch
 # of the GEMM classes, from one ncu capture of this kernel version on the
 # default workload (profiles/k_gemm_tc_kimi_k2_int4.md); None elsewhere.
-TRAFFIC_BYTES = {("kimi_k2", "fused", "gemm_gate_up"): 8.584e9,
+TRAFFIC_BYTES = {("kimi_k2", "fused", "gemm_gate_up"): 8.653e9,
                  ("kimi_k2", "fused", "gemm_down"): 4.360e9,
-                 ("kimi_k2", "fused", "gemm_bwd_g"): 4.741e9,
-                 ("kimi_k2", "fused", "gemm_bwd_dx"): 7.910e9}
+                 ("kimi_k2", "fused", "gemm_bwd_g"): 4.757e9,
+                 ("kimi_k2", "fused", "gemm_bwd_dx"): 7.891e9}
 
 
 def max_over_ranks(x: float) -> float:
