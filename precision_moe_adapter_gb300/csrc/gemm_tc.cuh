@@ -9,19 +9,23 @@
 //
 //   D[f, t] = sum_k W~[f, k] * B[t, k]      (FP32 in TMEM: lanes = f, columns = t)
 //
-// Roles (704 threads, one CTA per SM, persistent over the work list):
+// Roles (800 threads, one CTA per SM, persistent over the work list):
 //   warps 0-3   epilogue: TMEM -> registers -> fused epilogue -> global
-//   warp  4     TMA producer of the packed weight tiles (with their scale
-//               words) and of the activation tiles B (128B swizzle)
-//   warp  5     TMEM allocator and MMA issuer (one elected thread)
-//   warps 6-21  converters: packed weights -> BF16 A tiles, 128B-swizzled.
-//               Forward kinds contract over the stored matrix's columns and
-//               write A K-major; backward kinds contract over its rows and
-//               write A MN-major (each stored row segment lands as one
-//               swizzle row, and the MMA reads the tile transposed).
-// Pipeline: kStages shared-memory stages (A 16 KB + B 32 KB) with full/empty
-// mbarriers; two TMEM accumulators of 256 columns so the epilogue of one
-// tile overlaps the main loop of the next.  Every wait is bounded.
+//   warps 4, 7  TMA producers of the packed weight tiles and their scales,
+//               taking alternate K steps (raw ring)
+//   warp  5     TMEM allocator and MMA issuer (one elected lane per K step)
+//   warps 6, 8  TMA producers of the token tiles B (128B swizzle), alternate
+//               K steps; BF16 weights (scratch mode, router) come the same way
+//   warps 9-24  converters in two groups taking alternate K steps: packed
+//               weights -> BF16 A tiles, 128B-swizzled.  Forward kinds
+//               contract over the stored matrix's columns and write A
+//               K-major; backward kinds contract over its rows and write A
+//               MN-major (each stored row segment lands as one swizzle row,
+//               and the MMA reads the tile transposed).
+// Pipeline: a raw ring of packed tiles, an A ring of converted tiles (16 KB)
+// and a B ring of token tiles (up to 32 KB), with full/empty mbarriers; two
+// TMEM accumulators of 256 columns so the epilogue of one tile overlaps the
+// main loop of the next.  Every wait is bounded.
 #pragma once
 
 #include <cuda.h>
