@@ -22,17 +22,16 @@
  *  - Page 1 (Kimi-K2.6 / DeepSeek V4 Flash sections): INT4 base and FP4 base
  *    with a BF16 adapter.
  *
- * Everything accumulates in double precision.  The method is a BF16
- * training step: every tensor that passes from one operation to the next is
- * a BF16 tensor, and only the sums inside an operation are wider.  The
- * rounding points are therefore, in the forward, the rotated activations
- * x~, the saved gate and up projections g and u, the SwiGLU output h, the
- * rotated h~, each pair's expert output o and the layer output Y; in the
- * backward, dh~ = w G, the SwiGLU input gradients dg and du, the expert
- * input gradient dx~, the rotated dx of each pair and the layer's dX.  They
- * are applied with a round-to-nearest-even conversion written out below;
- * the flag OR_NO_ROUND turns them off so that finite differences can check
- * the backward against the forward.
+ * Everything accumulates in double precision.  The BF16 rounding points are
+ * the tensors the method itself stores in BF16: the rotated activations x~
+ * (input of the gate/up projection), the SwiGLU output h and the rotated h~
+ * (input of the down projection), the layer output Y and the input gradient
+ * dX.  Every other quantity -- the projections g and u, each pair's expert
+ * output o and all the backward intermediates (G, dh~, dh, dg, du, dx~, the
+ * rotated dx of each pair) -- keeps the full precision of the sum that
+ * produced it.  The rounding is a round-to-nearest-even conversion written
+ * out below; the flag OR_NO_ROUND turns it off so that finite differences
+ * can check the backward against the forward.
  *
  * Where the pages are silent the plainest reading is taken (layouts,
  * rotation side, tie-breaking); each is stated beside the code that uses it.
@@ -552,9 +551,8 @@ static double sigm(double g) { return 1.0 / (1.0 + exp(-g)); }
 
 /* One (token, expert) pair through the expert, straight from the
  * definition: x~ = bf16(x R_up); g, u = x~ W_gate^T, x~ W_up^T;
- * h = bf16(silu(g) u); h~ = bf16(h R_down); o = bf16(h~ W_down^T).
- * g and u are kept unrounded here (h is formed from the sums); the
- * backward reads them as the BF16 tensors the forward saves. */
+ * h = bf16(silu(g) u); h~ = bf16(h R_down); o = h~ W_down^T.  g, u and o
+ * keep the precision of their sums. */
 static void expert_forward(const or_layer *L, int e, const uint16_t *xrow, const double *xrow64,
                            int flags, pair_buf *pb)
 {
@@ -595,7 +593,7 @@ static void expert_forward(const or_layer *L, int e, const uint16_t *xrow, const
         double acc = 0.0;
         for (int n = 0; n < I; ++n)
             acc += pb->ht[n] * dequant_elem(L->fmt, q2, s2, I, c, n);
-        pb->o[c] = rbf(acc, flags);
+        pb->o[c] = acc;
     }
 }
 
@@ -656,13 +654,13 @@ void or_forward(const or_layer *L, const uint16_t *X, const double *X64, const i
 /*
  * Backward-data of the layer (routing and w held fixed; no gradient for
  * the frozen base weights).  For each listed token t and slot j, e = idx,
- * with g and u the saved BF16 projections:
+ * with g and u the forward's unrounded projections:
  *   G = dY_t W_down                      d_topk_w[t,j] = G . h~
- *   dh~ = bf16(w_tj G)                   dR_down[e] += h_blk^T dh~_blk
+ *   dh~ = w_tj G                         dR_down[e] += h_blk^T dh~_blk
  *   dh = dh~ R_down^T
- *   dg = bf16(dh u sigma(g)(1 + g(1 - sigma(g))))   du = bf16(dh silu(g))
- *   dx~ = bf16(dg W_gate + du W_up)      dR_up[e] += x_blk^T dx~_blk
- *   dx_pair = bf16(dx~ R_up^T)           dX_t = bf16(sum_j dx_pair)
+ *   dg = dh u sigma(g)(1 + g(1 - sigma(g)))     du = dh silu(g)
+ *   dx~ = dg W_gate + du W_up            dR_up[e] += x_blk^T dx~_blk
+ *   dx_pair = dx~ R_up^T                 dX_t = bf16(sum_j dx_pair)
  * The adapter gradients accumulate over the listed tokens only, in token
  * then slot order; when the adapter is shared (stride 0) everything
  * accumulates into block set 0.  dX, d_topk_w, dR_up, dR_down nullable.
@@ -706,7 +704,7 @@ void or_backward(const or_layer *L, const uint16_t *X, const double *X64, const 
                 d_topk_w[(int64_t)t * k + j] = (float)dw;
             double *dht = dhts + p * I;
             for (int n = 0; n < I; ++n)
-                dht[n] = rbf(wt * G[n], flags);
+                dht[n] = wt * G[n];
             memcpy(hs + p * I, pb.h, sizeof(double) * (size_t)I);
             if (L->R_down) {
                 int64_t o = (int64_t)e * L->stride_down;
@@ -715,9 +713,9 @@ void or_backward(const or_layer *L, const uint16_t *X, const double *X64, const 
                 memcpy(dh, dht, sizeof(double) * (size_t)I);
             }
             for (int n = 0; n < I; ++n) {
-                double g = rbf(pb.g[n], flags), u = rbf(pb.u[n], flags), sg = sigm(g);
-                dg[n] = rbf(dh[n] * u * sg * (1.0 + g * (1.0 - sg)), flags);
-                du[n] = rbf(dh[n] * silu(g), flags);
+                double g = pb.g[n], u = pb.u[n], sg = sigm(g);
+                dg[n] = dh[n] * u * sg * (1.0 + g * (1.0 - sg));
+                du[n] = dh[n] * silu(g);
             }
             const uint8_t *q13 = wq(L, 13, e);
             const void *s13 = ws(L, 13, e);
@@ -726,15 +724,13 @@ void or_backward(const or_layer *L, const uint16_t *X, const double *X64, const 
                 for (int n = 0; n < I; ++n)
                     a += dg[n] * dequant_elem(L->fmt, q13, s13, d, n, c)
                        + du[n] * dequant_elem(L->fmt, q13, s13, d, I + n, c);
-                dxt[c] = rbf(a, flags);
+                dxt[c] = a;
             }
             memcpy(dxts + p * d, dxt, sizeof(double) * (size_t)d);
             memcpy(xs + p * d, pb.x, sizeof(double) * (size_t)d);
             if (L->R_up) {
                 int64_t o = (int64_t)e * L->stride_up;
                 rotate_row_t64(dxt, L->R_up + o, L->R_up64 ? L->R_up64 + o : NULL, d, b, dxp);
-                for (int c = 0; c < d; ++c)
-                    dxp[c] = rbf(dxp[c], flags);
             } else {
                 memcpy(dxp, dxt, sizeof(double) * (size_t)d);
             }
@@ -808,10 +804,10 @@ void or_backward(const or_layer *L, const uint16_t *X, const double *X64, const 
  * activations).  W is [N, K] in the packed format fmt, R (nullable) is one
  * block-diagonal rotation [K/b, b, b] (BF16 bits, or doubles in R64).
  *   forward:  x~ = bf16(x R);  y = x~ W^T;  Y = bf16(y)
- *   backward: G = dY W;  dx~ = bf16(G);  dR = sum_rows x_blk^T dx~_blk;
- *             dX = bf16(dx~ R^T)        (without R: dX = bf16(G))
- * Rounding points as in the layer (OR_NO_ROUND removes them); X64 replaces
- * the BF16 input for finite differences.
+ *   backward: dx~ = dY W;  dR = sum_rows x_blk^T dx~_blk;  dX = bf16(dx~ R^T)
+ *             (without R: dX = bf16(dY W))
+ * Rounding points as in the layer: x~, Y and dX (OR_NO_ROUND removes them);
+ * X64 replaces the BF16 input for finite differences.
  */
 void or_dense_forward(int rows, int N, int K, int b, int fmt, const uint8_t *q, const void *s,
                       const uint16_t *R, const double *R64, const uint16_t *X, const double *X64,
@@ -854,7 +850,7 @@ void or_dense_backward(int rows, int N, int K, int b, int fmt, const uint8_t *q,
             double a = 0.0;
             for (int n = 0; n < N; ++n)
                 a += or_bf16_to_double(dY[(int64_t)i * N + n]) * dequant_elem(fmt, q, s, K, n, c);
-            dxt[c] = has_r ? rbf(a, flags) : a;
+            dxt[c] = a;
         }
         if (has_r)
             rotate_row_t64(dxt, R, R64, K, b, dx);

@@ -81,7 +81,8 @@ def test_backward_finite_differences():
 
 
 def test_rounding_points_against_torch():
-    """x~, dx~ and the outputs are BF16 tensors (torch's conversion)."""
+    """x~ and the outputs are BF16 tensors (torch's conversion); the
+    backward's dx~ = dY W keeps its precision."""
     import torch
     q, s, X, dY, W = _case(rows=4)
     N, K, b = 128, 128, 32
@@ -93,7 +94,8 @@ def test_rounding_points_against_torch():
     Y, Y64 = oracle.dense_forward(gi.INT4, q, s, N, K, b, Rb, X)
     assert np.allclose(Y64, xt @ W.T, rtol=1e-12, atol=1e-12)
     g = oracle.dense_backward(gi.INT4, q, s, N, K, b, Rb, X, dY)
-    dxt = r(bf(dY) @ W)
+    dxt = bf(dY) @ W
     assert np.allclose(g["dX64"], dxt @ BD.T, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(bf(g["dX"]), r(dxt @ BD.T))
     nb = lambda a: a.reshape(a.shape[0], -1, b)
     assert np.allclose(g["dR"], np.einsum("tbr,tbc->brc", nb(bf(X)), nb(dxt)), rtol=1e-12, atol=1e-12)
