@@ -43,18 +43,49 @@ def parse():
     ap.add_argument("--chunk", type=int, default=0, help="experts per chunk (0: the config's C)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (0: the config's T)")
     ap.add_argument("--experts", type=int, default=0, help="override E (0: the config's E)")
+    ap.add_argument("--sweep-chunks", default="",
+                    help="comma-separated chunk sizes (0: all active experts): after the main "
+                         "line, one line per C with the step time in --mode and its dequant "
+                         "scratch bytes")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch
-# of the GEMM classes, from one ncu capture of this kernel version on the
-# default workload (profiles/k_gemm_tc_kimi_k2_int4.md); None elsewhere.
-TRAFFIC_BYTES = {("kimi_k2", "fused", "gemm_gate_up"): 8.653e9,
-                 ("kimi_k2", "fused", "gemm_down"): 4.360e9,
-                 ("kimi_k2", "fused", "gemm_bwd_g"): 4.757e9,
-                 ("kimi_k2", "fused", "gemm_bwd_dx"): 7.891e9}
+# of the GEMM classes on the default workload, from one ncu capture, keyed
+# by the digest of the GEMM sources it was taken with: once those sources
+# change the figure no longer describes the kernel and is reported as null.
+TRAFFIC = {"digest": "", "bytes": {}}
+
+
+def gemm_digest() -> str:
+    """SHA-256 (first 16 hex digits) of the grouped GEMM's sources."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "precision_moe_adapter_gb300", "csrc")
+    for f in ("gemm_tc.cuh", "gemm_tc_host.cuh", "gemm_tc.cu"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_of(cfg_name: str, mode: str, kernel: str, default_load: bool):
+    if not default_load or TRAFFIC["digest"] != gemm_digest():
+        return None
+    return TRAFFIC["bytes"].get((cfg_name, mode, kernel))
+
+
+def pick_peak(pk, clocks):
+    """The dense BF16 denominator: the measured burst figure when the timed
+    region ran at the maximum SM clock with no power cap, else the measured
+    sustained (power-capped) one."""
+    capped = "sw_power_cap" in (clocks.get("reasons") or [])
+    sm, smax = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    at_max = sm is not None and smax is not None and sm >= 0.97 * smax
+    if at_max and not capped:
+        return pk["bf16"], f"{pk['src']} bf16 burst (timed region at {sm:.0f} MHz, no power cap)"
+    return pk["bf16_sus"], f"{pk['src']} bf16 sustained (timed region at {sm} MHz, reasons {clocks.get('reasons')})"
 
 
 def max_over_ranks(x: float) -> float:
@@ -106,7 +137,7 @@ def bytes_of(cfg, counts):
         wq = 3 * d * I // 2 + 3 * d * (I // 32) * (2 if cfg.fmt == gi.INT4 else 1)
     adp = (d + I) * b * 2 if cfg.adapter == "per_expert" else 0
     act_f = cfg.T * d * 2 * 2 + d * cfg.E * 4          # X, Y, Wr
-    act_b = cfg.T * d * 2 * 3 + cfg.P * 3 * I * 2      # X, dY, dX, ctx
+    act_b = cfg.T * d * 2 * 3 + cfg.P * I * 10         # X, dY, dX, ctx (g, u f32; h bf16)
     return na * (wq + adp) * 2 + act_f + act_b
 
 
@@ -281,7 +312,7 @@ def main():
     rt = L.new_routing()
     Y = torch.empty_like(X)
     dX = torch.empty_like(X)
-    ctx = torch.empty((cfg.P, 3 * cfg.I), dtype=torch.int16, device=dev)
+    ctx = L.new_ctx()
     dtw = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
     dRu, dRd = L.grads()
     dSu = None if L.S_up is None else torch.empty_like(L.S_up)
@@ -298,9 +329,10 @@ def main():
             e.record()
             phase_ev.append((name, e))
 
-    def step(Xs, dYs, timed=False, Yo=None, dXo=None):
+    def step(Xs, dYs, timed=False, Yo=None, dXo=None, C=None):
         Yo = Y if Yo is None else Yo
         dXo = dX if dXo is None else dXo
+        C = C or cfg.C
         mark("cayley", timed)
         if L.S_up is not None:   # R = Cayley(S) for the adapter of this step
             pmoe.adapter_cayley(L.S_up.numel() // (b * b), b, L.S_up, L.R_up, L.Rf_up)
@@ -310,9 +342,9 @@ def main():
         mark("permute", timed)
         L.permute(rt)
         mark("forward", timed)
-        L.forward(Xs, rt, Yo, C=cfg.C, mode=mode, ctx=ctx)
+        L.forward(Xs, rt, Yo, C=C, mode=mode, ctx=ctx)
         mark("backward", timed)
-        L.backward(Xs, dYs, ctx, rt, dXo, dtw, dRu, dRd, C=cfg.C)
+        L.backward(Xs, dYs, ctx, rt, dXo, dtw, dRu, dRd, C=C)
         mark("cayley_grad", timed)
         if L.S_up is not None:
             pmoe.adapter_cayley_grad(L.S_up.numel() // (b * b), b, L.S_up, L.Rf_up, dRu, dSu)
@@ -361,7 +393,9 @@ def main():
     pk = peaks()
     tflops = (f_fwd + f_bwd) / (ms_step / 1e3) / 1e12
     B = bytes_of(cfg, counts)
-    t_roof = max((f_fwd + f_bwd) / (pk["bf16_sus"] * 1e12), B / (pk["hbm"] * 1e9))
+    clocks = clk.summary()
+    peak_tf, peak_src = pick_peak(pk, clocks)
+    t_roof = max((f_fwd + f_bwd) / (peak_tf * 1e12), B / (pk["hbm"] * 1e9))
 
     # dominant kernel: the timed class with the largest share of device time
     dom = max(kt, key=lambda k_: kt[k_][0])
@@ -372,10 +406,11 @@ def main():
     dom_avg_ms = dom_ms / max(dom_n, 1)
     dom_tf = dom_flops / (dom_avg_ms / 1e3) / 1e12
     default_load = not (args.tokens or args.experts or args.chunk)
-    traffic = TRAFFIC_BYTES.get((cfg.name, args.mode, dom)) if default_load else None
+    traffic = traffic_of(cfg.name, args.mode, dom, default_load)
     roofline = {"kernel": dom, "bound": "tensor", "achieved": round(dom_tf, 3),
-                "peak": pk["bf16_sus"], "unit": "TFLOP/s", "frac": round(dom_tf / pk["bf16_sus"], 5),
-                "traffic": traffic, "peak_source": f"{pk['src']} bf16 sustained",
+                "peak": peak_tf, "unit": "TFLOP/s", "frac": round(dom_tf / peak_tf, 5),
+                "traffic": traffic, "peak_source": peak_src,
+                "frac_of_sustained": round(dom_tf / pk["bf16_sus"], 5),
                 "launch_ms": round(dom_avg_ms, 4), "launches": dom_n,
                 "algorithmic_flops_per_launch": dom_flops}
 
@@ -446,6 +481,32 @@ def main():
                "sample": f"first {n_tok} of {cfg.T} tokens (router + forward + backward-data), "
                          f"{dt:.1f} s"}
 
+    sweep = []
+    if args.sweep_chunks:
+        for c_ in [int(v) for v in args.sweep_chunks.split(",")]:
+            C_ = c_ if c_ > 0 else cfg.E
+            for _ in range(args.warmup):
+                step(X, dY, C=C_)
+            torch.cuda.synchronize()
+            f0 = torch.cuda.mem_get_info()[0]
+            ev0.record(stream)
+            for _ in range(args.steps):
+                step(X, dY, C=C_)
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            sms = ev0.elapsed_time(ev1) / args.steps
+            sweep.append({"sweep": "chunk", "mode": args.mode, "C": C_,
+                          "active_experts": int((counts > 0).sum()),
+                          "chunks": int(np.ceil((counts > 0).sum() / C_)),
+                          "ms_per_step": sms, "tokens_per_s": cfg.T / (sms / 1e3),
+                          "scratch_bytes_per_chunk": pmoe.moe_scratch_bytes(L.dims, C_, mode),
+                          "workspace_bytes_forward": pmoe.moe_workspace_bytes(
+                              L.dims, pmoe.OP_FORWARD, C_, mode),
+                          "device_bytes_in_use": torch.cuda.mem_get_info()[1] - f0})
+        st = L.status()
+        if st != pmoe.PMOE_OK:
+            raise RuntimeError(f"device error in the sweep: {pmoe.status_string(st)}")
+
     if rank == 0:
         line = {"metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -454,13 +515,16 @@ def main():
                 "tflops": tflops, "step_roofline": {
                     "time_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms_step,
                     "flops": f_fwd + f_bwd, "bytes": B,
-                    "peaks": f"{pk['src']}: bf16 {pk['bf16_sus']} TF/s sustained, HBM {pk['hbm']} GB/s"},
+                    "peaks": f"{peak_src}: {peak_tf} TF/s; HBM {pk['hbm']} GB/s ({pk['src']})",
+                    "note": "the layer-level fraction the >= 0.6 target is judged on"},
                 "roofline": roofline, "kernel_ms_per_step": {k_: v[0] / args.steps for k_, v in kt.items()},
                 "phase_ms": {k_: round(v, 3) for k_, v in phase_ms.items()},
-                "clocks": clk.summary(), "e2e": e2e, "gpu_launches": launches,
+                "clocks": clocks, "e2e": e2e, "gpu_launches": launches,
                 "cpu_baseline": cpu,
                 "scratch_bytes_per_chunk": pmoe.moe_scratch_bytes(L.dims, cfg.C, mode)}
         print(json.dumps(line), flush=True)
+        for sl in sweep:
+            print(json.dumps(sl), flush=True)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()

@@ -5,9 +5,10 @@
  *
  * The operation follows the "Active-expert-chunked dequantization" and
  * "bypass-base-weight-grad GEMM backward" passages of the Orbit
- * announcement (page 1, section 技艺细节), the OFT adapter of the Orbit
- * analysis (page 2, sections 机制拆解 and 术语), and the block-scaled FP8
- * weight format of the NeMo RL FP8 blog (page 3, Table 1).
+ * announcement (section 技艺细节), the OFT adapter of the Orbit analysis
+ * "Orbit：把万亿模型 RL 后训练改写成部署一致性问题" (sections 机制拆解 and
+ * 术语和概念边界), and the block-scaled FP8 weight format of the NeMo RL FP8
+ * article (section "RL 中线性层的 FP8", Table 1).
  *
  * Conventions for every entry point:
  *  - Ownership: the caller allocates every buffer.  The library never
@@ -54,8 +55,9 @@ typedef enum {
     PMOE_ERR_TIMEOUT = 6        /* device: a bounded wait gave up */
 } pmoe_status;
 
-/* Frozen-base weight formats ("INT4 base", "FP4 base" on page 1; FP8 E4M3
- * with [128,128] FP32 block scales, page 3 Table 1).  Every weight matrix
+/* Frozen-base weight formats (the INT4 and FP4 bases of the Orbit
+ * announcement; FP8 E4M3 with [128,128] FP32 block scales, NeMo RL FP8
+ * article, Table 1).  Every weight matrix
  * is stored in the linear convention [N_out, K_in]:
  *   INT4  : q u8 [N, K/2] (element 2i = low nibble of byte i, two's
  *           complement in [-8, 7]); s bf16 [N, K/32].  W = bf16(q*s).
@@ -115,14 +117,16 @@ enum {
 
 /* Router modes. */
 enum {
-    PMOE_ROUTE_FAST = 0    /* FP32 logits from an exact 3-term BF16 split of Wr on tensor cores */
+    PMOE_ROUTE_FAST = 0,   /* FP32 logits from an exact 3-term BF16 split of Wr on tensor cores */
+    PMOE_ROUTE_EXACT = 1   /* FP32 logits on the CUDA cores in one fixed summation order */
 };
 
 /* Ops for moe_workspace_bytes. */
 enum { PMOE_OP_PERMUTE = 0, PMOE_OP_FORWARD = 1, PMOE_OP_BACKWARD = 2 };
 
 /*
- * moe_route -- router top-k (page 1, 技艺细节: "router 选中的 experts").
+ * moe_route -- router top-k (Orbit announcement, 技艺细节: the experts the
+ * router selects).
  * logits = fp32(X Wr) + bias; the k experts with the largest logits are
  * selected (ties to the lower expert id), slots in descending logit order;
  * w = softmax over the k selected logits (FP32).
@@ -132,13 +136,27 @@ enum { PMOE_OP_PERMUTE = 0, PMOE_OP_FORWARD = 1, PMOE_OP_BACKWARD = 2 };
  *   ws     workspace of moe_workspace_bytes(dims, PMOE_OP_PERMUTE, 0, 0)
  *          bytes or more (holds the split router weights and the error word)
  * Requires E <= 4096 and k <= 32.
+ * Modes (the logits before the bias; the bias is then one FP32 addition):
+ *   PMOE_ROUTE_FAST  the tensor-core contraction in fixed K splits whose
+ *                    FP32 partials are summed in order: within the FP32
+ *                    summation error of the exact logits, and per token
+ *                    independent of the batch.
+ *   PMOE_ROUTE_EXACT the canonical order, reproducible bit for bit by a
+ *                    plain CPU program: 32 partial sums, partial i the
+ *                    fmaf chain over columns i, i+32, i+64, ... from 0;
+ *                    then s[i] = s[i] + s[i+h] for i < h, h = 16, 8, 4, 2,
+ *                    1; the logit is s[0] (+ bias).  Slower (CUDA cores).
+ * The selection and the softmax are the same for both: the order (logit
+ * descending, id ascending) over the FP32 logits, and w_j = exp(l_j - l_0)
+ * / sum_i exp(l_i - l_0) in FP32.
  */
 pmoe_status moe_route(pmoe_dims dims, const void *X, const float *Wr, const float *bias,
                       float *logits, int32_t *idx, float *w, int mode,
                       void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
- * moe_permute -- groups the (token, slot) pairs by expert (page 1, 技艺细节:
+ * moe_permute -- groups the (token, slot) pairs by expert (Orbit
+ * announcement, 技艺细节:
  * the selected experts are gathered into batches): histogram of idx,
  * exclusive-scan offsets and a stable scatter.  Bit-exact and
  * deterministic: perm lists pair ids by (expert, pair id).
@@ -182,7 +200,8 @@ pmoe_status moe_permute_noalloc(pmoe_dims dims, const int32_t *idx, const pmoe_r
                                 cudaStream_t stream);
 
 /*
- * moe_chunked_forward -- the layer (page 1, 技艺细节): active experts are
+ * moe_chunked_forward -- the layer (Orbit announcement, 技艺细节): active
+ * experts are
  * taken C at a time in ascending id order; each chunk's experts are
  * dequantized to BF16 (FUSED: tile by tile in shared memory, no global
  * scratch; SCRATCH: into a C-expert global BF16 buffer that the next chunk
@@ -190,11 +209,14 @@ pmoe_status moe_permute_noalloc(pmoe_dims dims, const int32_t *idx, const pmoe_r
  *   x~ = bf16(x blockdiag(R_up[e]))             (adapter on the activations)
  *   g, u = x~ W_gate[e]^T, x~ W_up[e]^T          (FP32 accumulate)
  *   h  = bf16(silu(g) u);  h~ = bf16(h blockdiag(R_down[e]))
- *   o  = h~ W_down[e]^T
- * and finally Y_t = bf16(sum_j w[t,j] o_(t,j)), slots summed in order.
+ *   o  = h~ W_down[e]^T                          (kept in FP32)
+ * and finally Y_t = bf16(sum_j w[t,j] o_(t,j)), slots summed in order in
+ * FP32.
  *   X   bf16 [T, d] (in)         Y bf16 [T, d] (out)
- *   ctx bf16 [P, 3I] or NULL: when given, receives [g | u | h] per pair in
- *       expert-sorted order (row i = pair perm[i]) for moe_backward_data
+ *   ctx NULL, or moe_ctx_bytes(dims) bytes: when given, receives what
+ *       moe_backward_data needs, per pair in expert-sorted order (row i =
+ *       pair perm[i]): first g | u as f32 [P, 2I] (g in columns 0..I-1,
+ *       u in I..2I-1), then h as bf16 [P, I]
  *   chunk_C >= 1 experts per chunk (>= E means one chunk)
  *   ws  >= moe_workspace_bytes(dims, PMOE_OP_FORWARD, chunk_C, mode)
  * The result does not depend on chunk_C or mode (bit-identical).
@@ -203,6 +225,8 @@ pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const p
                                 const pmoe_routing *rt, const void *X, int32_t chunk_C, int mode,
                                 void *Y, void *ctx, void *ws, size_t ws_bytes,
                                 cudaStream_t stream);
+/* Bytes of the forward's saved context: P * I * (8 + 2); 0 for invalid dims. */
+size_t moe_ctx_bytes(pmoe_dims dims);
 
 /*
  * Adapter slots for rollout while training publishes (the Orbit analysis:
@@ -237,15 +261,24 @@ pmoe_status moe_chunked_forward_slots(pmoe_dims dims, const pmoe_weights *wts,
 
 /*
  * moe_backward_data -- backward through the frozen experts with no base
- * weight gradient (page 1, 技艺细节: bypass-base-weight-grad GEMM backward;
- * page 2, 机制拆解: the base takes no backward update cost).  Routing and
+ * weight gradient (Orbit announcement, 技艺细节: bypass-base-weight-grad GEMM
+ * backward; the Orbit analysis, 机制拆解: the base takes no backward update
+ * cost).  Routing and
  * w are held fixed.  Per pair (t, j), e = idx[t, j]:
  *   G = dY_t W_down[e]          d_topk_w[t,j] = G . h~
  *   dh~ = w[t,j] G              dR_down[e] += h_blk^T dh~_blk
  *   dh = dh~ R_down^T;  dg = dh u s(g)(1 + g(1 - s(g)));  du = dh silu(g)
  *   dx~ = dg W_gate + du W_up   dR_up[e] += x_blk^T dx~_blk
  *   dx_pair = dx~ R_up^T        dX_t = bf16(sum_j dx_pair), slots in order
- *   X, dY   bf16 [T, d] (in)    ctx bf16 [P, 3I] from the forward (in)
+ * with h~ = bf16(h blockdiag(R_down[e])) recomputed from the saved h.  Every
+ * intermediate is FP32 (g, u from ctx; G, dh~, dh, dg, du, dx~, dx_pair),
+ * except at the tensor cores: dh~ and dx~ enter the rotations and adapter
+ * gradients as two BF16 parts hi = bf16(v), lo = bf16(v - hi), which carry
+ * v to 2^-16; [dg | du] enters the dx~ GEMM in FP16 (11 significant bits),
+ * with the weights' BF16 values in FP16 encoding (exact for weights in the
+ * FP16 normal range [2^-14, 65504] and zero).  The only BF16 roundings are
+ * h~ and dX.
+ *   X, dY   bf16 [T, d] (in)    ctx from the forward (in, moe_ctx_bytes)
  *   dX      bf16 [T, d] (out)
  *   d_topk_w f32 [T, k] or NULL (out)
  *   dR_up   f32 shaped like R_up, dR_down f32 shaped like R_down (out,
@@ -261,8 +294,8 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
                               cudaStream_t stream);
 
 /*
- * moe_dequant -- the dequantization step alone (page 1, 技艺细节:
- * "临时反量化"): one [N, K] weight matrix in `fmt` to BF16 [N, K].
+ * moe_dequant -- the dequantization step alone (Orbit announcement,
+ * 技艺细节: temporary dequantization of the selected experts): one [N, K] weight matrix in `fmt` to BF16 [N, K].
  * Bit-exact with the format definitions above.  N >= 0, K % 32 == 0
  * (INT4 / MXFP4) or N % 128 == 0 and K % 128 == 0 (FP8).
  */
@@ -270,7 +303,7 @@ pmoe_status moe_dequant(pmoe_wfmt fmt, const void *q, const void *s, int64_t N, 
                         void *out, cudaStream_t stream);
 
 /*
- * moe_grouped_gemm -- the grouped GEMM step alone (page 1, 技艺细节:
+ * moe_grouped_gemm -- the grouped GEMM step alone (Orbit announcement, 技艺细节:
  * "grouped GEMM" over the dequantized experts), on the tensor cores with
  * the weights dequantized tile by tile in shared memory.  Rows
  * offsets[e] .. offsets[e+1]-1 of A belong to expert e.
@@ -289,7 +322,7 @@ pmoe_status moe_grouped_gemm(pmoe_wfmt fmt, const void *q, const void *s, int32_
 size_t moe_grouped_gemm_ws_bytes(int32_t E, int32_t rows);
 
 /*
- * adapter_apply -- Xr = bf16(X blockdiag(R)) (page 2, 机制拆解: the OFT
+ * adapter_apply -- Xr = bf16(X blockdiag(R)) (the Orbit analysis, 机制拆解: the OFT
  * adapter as a local orthogonal transform).  X bf16 [rows, dim], R bf16
  * [dim/b, b, b], Xr bf16 [rows, dim] (must not alias X).  dim % b == 0,
  * b in {16, 32, 64, 128}.
@@ -394,6 +427,23 @@ pmoe_status pmoe_kernel_timing(int enable);
 /* Total device time (ms) and number of launches of kernel class `which`
  * recorded since timing was enabled; waits for the recorded events. */
 pmoe_status pmoe_kernel_time(int which, double *ms_total, int *launches);
+
+/*
+ * pmoe_debug_expire_gemm_wait -- test hook for the bounded waits (no
+ * counterpart in the pages).  Every wait inside the grouped-GEMM kernel is
+ * bounded; this makes one of them run out without any fault: the NEXT
+ * grouped-GEMM launch in the process (whichever entry point makes it) uses
+ * wait_ns as the limit of its waits, and its MMA issuer withholds the
+ * accumulator-full signal of CTA 0's first work item.  CTA 0's epilogue
+ * then gives up after wait_ns, records PMOE_ERR_TIMEOUT in the call's error
+ * word, and every role of that CTA leaves its loop after its own bounded
+ * wait and frees its tensor memory; the call's outputs are incomplete.
+ * One-shot: the launch consumes the hook.  wait_ns in [1e5, 2e9] (the
+ * bound keeps every issued copy and MMA long finished before a role gives
+ * up), else PMOE_ERR_INVALID_ARG.  Process-wide state: not for use while
+ * other threads launch layer work.
+ */
+pmoe_status pmoe_debug_expire_gemm_wait(uint64_t wait_ns);
 
 #ifdef __cplusplus
 }

@@ -10,13 +10,15 @@ accumulation, OpenMP only across independent tokens / blocks).  This module
 compiles it with gcc on first use and exposes one numpy-level function per
 step of the method:
 
-  dequant        -- "Active-expert-chunked dequantization" (page 1, 技艺细节):
+  dequant        -- active-expert-chunked dequantization (Orbit announcement, 技艺细节):
                     INT4 group-32 / MXFP4 / FP8 [128,128] weights -> BF16
   route          -- router top-k + softmax over the selected experts
+  topk           -- the selection and softmax alone, on given logits
+  route_canonical -- router logits in one fixed FP32 summation order
   permute        -- grouping of (token, slot) pairs by expert
   forward        -- per-token definition of the layer (no chunks)
   backward       -- backward-data: dX, d_topk_w, adapter gradients; no base
-                    weight gradient ("bypass-base-weight-grad", page 1)
+                    weight gradient (bypass-base-weight-grad backward, Orbit announcement)
   adapter_apply / adapter_grad -- block-diagonal orthogonal (OFT) rotation
   cayley / cayley_grad         -- R = (I+S)(I-S)^-1 per block
 
@@ -93,6 +95,10 @@ def _declare(L):
     L.or_e4m3_value.restype = ctypes.c_double
     L.or_dequant.argtypes = [_i, _p, _p, _i64, _i64, _p]
     L.or_route.argtypes = [_i, _i, _i, _i, _p, _p, _p, _p, _i, _p, _p, _p]
+    L.or_topk.argtypes = [_i, _i, _p, _p, _i, _p, _p]
+    L.or_topk.restype = None
+    L.or_route_canonical.argtypes = [_i, _i, _p, _p, _p, _p, _i, _p]
+    L.or_route_canonical.restype = None
     L.or_permute.argtypes = [_i, _i, _p, _p, _p, _p, _p, _p, _p]
     L.or_adapter_apply.argtypes = [_i, _i, _i, _p, _p, _p]
     L.or_adapter_grad.argtypes = [_i, _i, _i, _p, _p, _p, _p, _p]
@@ -168,6 +174,37 @@ def route(X: np.ndarray, Wr: np.ndarray, bias, k: int, toks=None):
     _L().or_route(T, d, E, k, _ptr(X), _ptr(Wr), _ptr(bias), _ptr(toks_a), n,
                   _ptr(logits), _ptr(idx), _ptr(w))
     return logits, idx, w
+
+
+def topk(logits: np.ndarray, k: int, toks=None):
+    """Selection and weights from given FP32 logits [T, E] (bias included):
+    top-k by (logit desc, id asc), softmax over the k selected in double
+    rounded to FP32.  Returns (idx i32 [T,k], w f32 [T,k]); rows not in
+    ``toks`` are left zero."""
+    logits = _c(logits, np.float32)
+    T, E = logits.shape
+    toks_a = _c(toks, np.int32)
+    n = T if toks is None else len(toks_a)
+    idx = np.zeros((T, k), np.int32)
+    w = np.zeros((T, k), np.float32)
+    _L().or_topk(E, k, _ptr(logits), _ptr(toks_a), n, _ptr(idx), _ptr(w))
+    return idx, w
+
+
+def route_canonical(X: np.ndarray, Wr: np.ndarray, bias, toks=None) -> np.ndarray:
+    """The router logits in the library's canonical FP32 summation order
+    (32 lane-strided fmaf chains, then a pairwise tree, then + bias):
+    f32 [T, E]; rows not in ``toks`` are left zero."""
+    X = _c(X, np.uint16)
+    Wr = _c(Wr, np.float32)
+    bias = _c(bias, np.float32)
+    T, d = X.shape
+    E = Wr.shape[1]
+    toks_a = _c(toks, np.int32)
+    n = T if toks is None else len(toks_a)
+    logits = np.zeros((T, E), np.float32)
+    _L().or_route_canonical(d, E, _ptr(X), _ptr(Wr), _ptr(bias), _ptr(toks_a), n, _ptr(logits))
+    return logits
 
 
 def permute(idx: np.ndarray, E: int):

@@ -19,7 +19,7 @@
  *    policy): disabling the adapter recovers the frozen base.
  *  - NeMo RL FP8 blog, Table 1: FP8 E4M3 weights with an FP32 scale per
  *    [128,128] block.
- *  - Page 1 (Kimi-K2.6 / DeepSeek V4 Flash sections): INT4 base and FP4 base
+ *  - Orbit announcement (Kimi-K2.6 / DeepSeek V4 Flash sections): INT4 base and FP4 base
  *    with a BF16 adapter.
  *
  * Everything accumulates in double precision.  The BF16 rounding points are
@@ -136,7 +136,7 @@ double or_e4m3_value(unsigned c)
 }
 
 /* ------------------------------------------------------------------ */
-/* Weight dequantization (the "临时反量化" step)                        */
+/* Weight dequantization (the temporary dequantization step)         */
 /* ------------------------------------------------------------------ */
 /*
  * A weight matrix is stored in the linear convention [N_out, K_in].
@@ -201,13 +201,43 @@ static int64_t s_bytes(int fmt, int64_t N, int64_t K)
 /* Router (top-k over the experts, softmax over the selected)          */
 /* ------------------------------------------------------------------ */
 /*
+ * Selection and weights from given FP32 logits (bias already added): the k
+ * largest by (logit descending, expert id ascending) fill the slots in that
+ * order; w[t, j] = exp(l_j - l_0) / sum_i exp(l_i - l_0) over the k
+ * selected, in double, rounded to FP32.  Only the tokens in `toks` (n_toks
+ * of them; NULL: 0 .. n_toks-1) are handled, at their own rows.
+ */
+void or_topk(int E, int k, const float *logits, const int32_t *toks, int n_toks, int32_t *idx,
+             float *w)
+{
+#pragma omp parallel for schedule(static)
+    for (int it = 0; it < n_toks; ++it) {
+        int t = toks ? toks[it] : it;
+        const float *l = logits + (int64_t)t * E;
+        /* k passes of "best remaining", ties to the lower id */
+        char *taken = calloc((size_t)E, 1);
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || l[e] > l[best]) best = e;
+            }
+            taken[best] = 1;
+            idx[(int64_t)t * k + j] = best;
+        }
+        free(taken);
+        double lmax = l[idx[(int64_t)t * k]], den = 0.0;
+        for (int j = 0; j < k; ++j)
+            den += exp((double)l[idx[(int64_t)t * k + j]] - lmax);
+        for (int j = 0; j < k; ++j)
+            w[(int64_t)t * k + j] = (float)(exp((double)l[idx[(int64_t)t * k + j]] - lmax) / den);
+    }
+}
+
+/*
  * logits[t, e] = fp32( sum_c x[t,c] * Wr[c,e] + bias[e] ), the sum in
- * double.  The selection is made on these FP32 values, ordered by
- * (logit descending, expert id ascending); slots hold the selected experts
- * in that order.  w[t, j] = exp(l_j - l_0) / sum_i exp(l_i - l_0) over the
- * k selected logits, in double, rounded to FP32.
- * Only the tokens in `toks` (n_toks of them) are computed; outputs are
- * written at the token's own row.
+ * double, then or_topk.  Only the tokens in `toks` are computed; outputs
+ * are written at the token's own row.
  */
 void or_route(int T, int d, int E, int k, const uint16_t *X, const float *Wr,
               const float *bias, const int32_t *toks, int n_toks,
@@ -226,23 +256,41 @@ void or_route(int T, int d, int E, int k, const uint16_t *X, const float *Wr,
                 acc += (double)bias[e];
             l[e] = (float)acc;
         }
-        /* selection: k passes of "best remaining", ties to the lower id */
-        char *taken = calloc((size_t)E, 1);
-        for (int j = 0; j < k; ++j) {
-            int best = -1;
-            for (int e = 0; e < E; ++e) {
-                if (taken[e]) continue;
-                if (best < 0 || l[e] > l[best]) best = e;
+    }
+    or_topk(E, k, logits, toks, n_toks, idx, w);
+}
+
+/*
+ * The router logits in one fixed FP32 summation order (the library's
+ * canonical router mode, so that its logits can be compared bit for bit):
+ * 32 partial sums, partial i = fmaf chain over the columns c = i, i + 32,
+ * i + 64, ... in ascending order starting from 0; then the pairwise tree
+ * s[i] = s[i] + s[i + h] for i < h, h = 16, 8, 4, 2, 1; the logit is
+ * s[0] + bias[e] (one FP32 addition; no bias: s[0]).  d % 32 == 0.
+ */
+void or_route_canonical(int d, int E, const uint16_t *X, const float *Wr, const float *bias,
+                        const int32_t *toks, int n_toks, float *logits)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int it = 0; it < n_toks; ++it) {
+        int t = toks ? toks[it] : it;
+        for (int e = 0; e < E; ++e) {
+            float s[32];
+            for (int i = 0; i < 32; ++i) {
+                float acc = 0.0f;
+                for (int c = i; c < d; c += 32) {
+                    uint32_t u = (uint32_t)X[(int64_t)t * d + c] << 16;
+                    float x;
+                    memcpy(&x, &u, sizeof x);
+                    acc = fmaf(x, Wr[(int64_t)c * E + e], acc);
+                }
+                s[i] = acc;
             }
-            taken[best] = 1;
-            idx[(int64_t)t * k + j] = best;
+            for (int h = 16; h >= 1; h >>= 1)
+                for (int i = 0; i < h; ++i)
+                    s[i] = s[i] + s[i + h];
+            logits[(int64_t)t * E + e] = bias ? s[0] + bias[e] : s[0];
         }
-        free(taken);
-        double lmax = l[idx[(int64_t)t * k]], den = 0.0;
-        for (int j = 0; j < k; ++j)
-            den += exp((double)l[idx[(int64_t)t * k + j]] - lmax);
-        for (int j = 0; j < k; ++j)
-            w[(int64_t)t * k + j] = (float)(exp((double)l[idx[(int64_t)t * k + j]] - lmax) / den);
     }
 }
 

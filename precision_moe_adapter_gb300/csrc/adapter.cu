@@ -1,5 +1,5 @@
 // adapter.cu -- the Cayley parameterisation of the orthogonal adapter
-// blocks, R = (I + S)(I - S)^{-1}, and its gradient (page 2, 机制拆解: the
+// blocks, R = (I + S)(I - S)^{-1}, and its gradient ("Orbit：把万亿模型 RL 后训练改写成部署一致性问题", 机制拆解: the
 // adapter is a local orthogonal transform; S skew-symmetric makes each
 // block orthogonal).
 #include "common.cuh"

@@ -148,7 +148,8 @@ static void build_lists(const Lists &l, const pmoe_dims &d, int C, const pmoe_ro
 struct FwdWs {
     DevErr *err;
     Lists l;
-    uint16_t *xt, *h, *ht, *o, *scratch;
+    uint16_t *xt, *h, *ht, *scratch;
+    float *o;         // each pair's expert output, FP32 [P, d]
     uint64_t *snap;   // adapter-slot snapshot of this forward
 };
 static FwdWs carve_fwd(void *ws, const pmoe_dims &d, int C, int mode, size_t *bytes)
@@ -161,7 +162,7 @@ static FwdWs carve_fwd(void *ws, const pmoe_dims &d, int C, int mode, size_t *by
     w.xt = c.take<uint16_t>(P * d.d);
     w.h = c.take<uint16_t>(P * d.inter);
     w.ht = c.take<uint16_t>(P * d.inter);
-    w.o = c.take<uint16_t>(P * d.d);
+    w.o = c.take<float>(P * d.d);
     int64_t slots = mode == PMOE_MODE_SCRATCH ? std::min(C, d.E) : 0;
     w.scratch = c.take<uint16_t>(slots * 3 * (int64_t)d.inter * d.d);
     w.snap = c.take<uint64_t>(2);
@@ -172,7 +173,9 @@ static FwdWs carve_fwd(void *ws, const pmoe_dims &d, int C, int mode, size_t *by
 struct BwdWs {
     DevErr *err;
     Lists l;
-    uint16_t *dyp, *ht, *dht, *dgu, *dxt;
+    uint16_t *dyp, *ht;
+    uint16_t *dgu;          // [dg | du], FP16 [P, 2I]
+    float *dht, *dxt, *dxp; // dh~ [P, I], dx~ [P, d], rotated dx [P, d], FP32
     float *dtw_part;
 };
 static BwdWs carve_bwd(void *ws, const pmoe_dims &d, int C, size_t *bytes)
@@ -182,11 +185,12 @@ static BwdWs carve_bwd(void *ws, const pmoe_dims &d, int C, size_t *bytes)
     int64_t P = (int64_t)d.T * d.k;
     w.err = c.take<DevErr>(kHdrBytes / sizeof(DevErr));
     w.l = carve_lists(c, d, C);
-    w.dyp = c.take<uint16_t>(P * d.d);      // gathered dY rows; later the rotated dx rows
+    w.dyp = c.take<uint16_t>(P * d.d);      // gathered dY rows
     w.ht = c.take<uint16_t>(P * d.inter);
-    w.dht = c.take<uint16_t>(P * d.inter);
+    w.dht = c.take<float>(P * d.inter);
     w.dgu = c.take<uint16_t>(P * 2 * d.inter);
-    w.dxt = c.take<uint16_t>(P * d.d);
+    w.dxt = c.take<float>(P * d.d);
+    w.dxp = c.take<float>(P * d.d);
     w.dtw_part = c.take<float>(P * (d.inter / 32));
     if (bytes) *bytes = c.off;
     return w;
@@ -283,6 +287,12 @@ size_t moe_workspace_bytes(pmoe_dims dims, int op, int32_t chunk_C, int mode)
     return b;
 }
 
+size_t moe_ctx_bytes(pmoe_dims dims)
+{
+    if (!dims_ok(dims)) return 0;
+    return (size_t)dims.T * dims.k * dims.inter * (4 * 2 + 2);
+}
+
 size_t moe_scratch_bytes(pmoe_dims dims, int32_t chunk_C, int mode)
 {
     if (!dims_ok(dims) || mode != PMOE_MODE_SCRATCH || chunk_C < 1) return 0;
@@ -310,7 +320,8 @@ pmoe_status moe_route(pmoe_dims dims, const void *X, const float *Wr, const floa
                       float *logits, int32_t *idx, float *w, int mode, void *ws, size_t ws_bytes,
                       cudaStream_t stream)
 {
-    if (!dims_ok(dims) || mode != PMOE_ROUTE_FAST) return PMOE_ERR_INVALID_ARG;
+    if (!dims_ok(dims) || (mode != PMOE_ROUTE_FAST && mode != PMOE_ROUTE_EXACT))
+        return PMOE_ERR_INVALID_ARG;
     if (dims.T > 0 && (!X || !Wr || !idx || !w)) return PMOE_ERR_INVALID_ARG;
     if (!aligned16(X) || !aligned16(Wr) || !aligned16(idx) || !aligned16(w) || !aligned16(bias) ||
         !aligned16(logits))
@@ -319,7 +330,10 @@ pmoe_status moe_route(pmoe_dims dims, const void *X, const float *Wr, const floa
     PermWs pw = carve_perm(ws, dims, &need);
     if (!ws || ws_bytes < need || !aligned16(ws)) return PMOE_ERR_WORKSPACE;
     if (dims.T == 0) return PMOE_OK;
-    {
+    if (mode == PMOE_ROUTE_EXACT) {
+        ScopedTimer tm(PMOE_KT_ROUTER, stream);
+        launch_router_exact(dims.T, dims.d, dims.E, (const uint16_t *)X, Wr, pw.logits, stream);
+    } else {
         ScopedTimer tm(PMOE_KT_ROUTER, stream);
         // K splits (a function of d alone): every split is one matrix of
         // [E, 3d / splits] and writes its own partial logits
@@ -391,6 +405,32 @@ static bool adapter_ok(const pmoe_adapter *ad)
 }
 
 namespace pmoe {
+// Plain rotation of BF16 rows (x R, or x R^T with trans) over a work list.
+static RotCall rot_rows(int b, bool trans, const void *src, int64_t src_ld, const int32_t *gather_perm,
+                        int k, const uint16_t *R, int64_t stride, int dim, void *out, int64_t out_ld,
+                        const Tile *tiles, const int32_t *tbeg, const int32_t *tend, int max_tiles,
+                        int nrows)
+{
+    RotCall c{};
+    c.b = b;
+    c.trans = trans;
+    c.src = src;
+    c.src_ld = src_ld;
+    c.perm = gather_perm;
+    c.k = k;
+    c.R = R;
+    c.stride = stride;
+    c.dim = dim;
+    c.out = out;
+    c.out_ld = out_ld;
+    c.tiles = tiles;
+    c.tbeg = tbeg;
+    c.tend = tend;
+    c.max_tiles = max_tiles;
+    c.nrows = nrows;
+    return c;
+}
+
 // The forward for one adapter, or for two adapter slots picked on the device
 // by a snapshot of the slot control word (slots: R_*_alt is slot 1).
 static pmoe_status forward_impl(pmoe_dims dims, const pmoe_weights *wts, const uint16_t *R_up,
@@ -414,14 +454,21 @@ static pmoe_status forward_impl(pmoe_dims dims, const pmoe_weights *wts, const u
         launch_adapter_snapshot(ctrl, w.snap, version_out, stream);
         sel = w.snap;
     }
+    // the saved context: g | u rows (FP32, [P, 2I]) then h rows (BF16, [P, I])
+    float *ctx_gu = (float *)ctx;
+    uint16_t *h = ctx ? (uint16_t *)(ctx_gu + (int64_t)P * 2 * I) : w.h;
     const int nch = nchunks_of(dims, C);
     const int maxrt = max_rot_tiles_of(dims);
     const Lists &L = w.l;
     build_lists(L, dims, C, rt, stream);
     // x~ = bf16(x R_up[e]) for every pair, gathered into expert-sorted order
-    launch_rotate_tc(b, false, false, (const uint16_t *)X, d, true, rt->perm, k, rt->idx, R_up, su,
-                     d, w.xt, d, L.rtiles, L.chunk_rtiles, L.chunk_rtiles + nch, maxrt, 0, nullptr,
-                     stream, R_up_alt, sel);
+    {
+        RotCall c = rot_rows(b, false, X, d, rt->perm, k, R_up, su, d, w.xt, d, L.rtiles,
+                             L.chunk_rtiles, L.chunk_rtiles + nch, maxrt, 0);
+        c.R_alt = R_up_alt;
+        c.sel = sel;
+        launch_rotate_tc(c, stream);
+    }
 
     GemmArgs gu{};
     gu.kind = GK_FWD_GU;
@@ -432,23 +479,30 @@ static pmoe_status forward_impl(pmoe_dims dims, const pmoe_weights *wts, const u
     gu.Kst = d;
     gu.tiles = L.tiles;
     gu.chunk_tiles = L.chunk_tiles;
-    gu.out = w.h;
-    gu.ctx = (uint16_t *)ctx;
+    gu.out = h;
+    gu.ctxf = ctx_gu;
     gu.I = I;
     gu.nmat = dims.E;
     GemmArgs dn{};
     dn.kind = GK_FWD_DOWN;
-    dn.A = R_dn ? w.ht : w.h;
+    dn.A = R_dn ? w.ht : h;
     dn.K = I;
     dn.Nout = d;
     dn.Nst = d;
     dn.Kst = I;
     dn.tiles = L.tiles;
     dn.chunk_tiles = L.chunk_tiles;
-    dn.out = w.o;
+    dn.outf = w.o;
     dn.I = I;
     dn.nmat = dims.E;
     pmoe_status gs;
+    auto rot_down = [&](const int32_t *tb, const int32_t *te) {
+        RotCall c = rot_rows(b, false, h, I, nullptr, k, R_dn, sd, I, w.ht, I, L.rtiles, tb, te,
+                             maxrt, 0);
+        c.R_alt = R_dn_alt;
+        c.sel = sel;
+        launch_rotate_tc(c, stream);
+    };
 
     if (mode == PMOE_MODE_FUSED) {
         gu.fmt = dn.fmt = fmt;
@@ -466,10 +520,7 @@ static pmoe_status forward_impl(pmoe_dims dims, const pmoe_weights *wts, const u
             ScopedTimer tm(PMOE_KT_GEMM_GATE_UP, stream);
             if ((gs = run_gemm(gu, P, w.err, stream)) != PMOE_OK) return gs;
         }
-        if (R_dn)
-            launch_rotate_tc(b, false, false, w.h, I, false, rt->perm, k, rt->idx, R_dn, sd, I, w.ht,
-                             I, L.rtiles, L.chunk_rtiles, L.chunk_rtiles + nch, maxrt, 0, nullptr,
-                             stream, R_dn_alt, sel);
+        if (R_dn) rot_down(L.chunk_rtiles, L.chunk_rtiles + nch);
         {
             ScopedTimer tm(PMOE_KT_GEMM_DOWN, stream);
             if ((gs = run_gemm(dn, P, w.err, stream)) != PMOE_OK) return gs;
@@ -495,10 +546,7 @@ static pmoe_status forward_impl(pmoe_dims dims, const pmoe_weights *wts, const u
                 ScopedTimer tm(PMOE_KT_GEMM_GATE_UP, stream);
                 if ((gs = run_gemm(gu, P, w.err, stream)) != PMOE_OK) return gs;
             }
-            if (R_dn)
-                launch_rotate_tc(b, false, false, w.h, I, false, rt->perm, k, rt->idx, R_dn, sd, I,
-                                 w.ht, I, L.rtiles, L.chunk_rtiles + c, L.chunk_rtiles + c + 1,
-                                 maxrt, 0, nullptr, stream, R_dn_alt, sel);
+            if (R_dn) rot_down(L.chunk_rtiles + c, L.chunk_rtiles + c + 1);
             {
                 ScopedTimer tm(PMOE_KT_GEMM_DOWN, stream);
                 if ((gs = run_gemm(dn, P, w.err, stream)) != PMOE_OK) return gs;
@@ -601,16 +649,19 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
         return PMOE_OK;
     }
     const Lists &L = w.l;
-    const uint16_t *cx = (const uint16_t *)ctx;
-    const uint16_t *h = cx + 2 * I;   // saved h rows (stride 3I)
+    // the forward's saved context: g | u rows (FP32, [P, 2I]) then h rows (BF16, [P, I])
+    const float *ctx_gu = (const float *)ctx;
+    const uint16_t *h = (const uint16_t *)(ctx_gu + (int64_t)P * 2 * I);
+    const int32_t *rtb = L.chunk_rtiles, *rte = L.chunk_rtiles + nch;
     build_lists(L, dims, C, rt, stream);
     // dY rows per pair (expert-sorted) and h~ = bf16(h R_down) from the saved h
-    launch_rotate_tc(b, false, false, (const uint16_t *)dY, d, true, rt->perm, k, rt->idx, nullptr,
-                     0, d, w.dyp, d, L.rtiles, L.chunk_rtiles, L.chunk_rtiles + nch, maxrt, 0,
-                     nullptr, stream);
-    launch_rotate_tc(b, false, false, h, 3 * (int64_t)I, false, rt->perm, k, rt->idx, R_dn, sd, I,
-                     w.ht, I, L.rtiles, L.chunk_rtiles, L.chunk_rtiles + nch, maxrt, 0, nullptr,
+    launch_rotate_tc(rot_rows(b, false, dY, d, rt->perm, k, nullptr, 0, d, w.dyp, d, L.rtiles, rtb,
+                              rte, maxrt, 0),
                      stream);
+    if (R_dn)
+        launch_rotate_tc(rot_rows(b, false, h, I, nullptr, k, R_dn, sd, I, w.ht, I, L.rtiles, rtb,
+                                  rte, maxrt, 0),
+                         stream);
     pmoe_status gs;
     GemmArgs g{};
     g.kind = GK_BWD_G;
@@ -628,28 +679,35 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
     g.chunk_tiles = L.chunk_tiles;
     g.c0 = 0;
     g.c1 = nch;
-    g.out = w.dht;
+    g.outf = w.dht;   // dh~ = w G in FP32
     g.I = I;
     g.w = rt->w;
     g.perm = rt->perm;
-    g.ht = w.ht;
+    g.ht = R_dn ? w.ht : h;
     g.dtw_part = w.dtw_part;
     g.nmat = E;
     {
         ScopedTimer tm(PMOE_KT_GEMM_BWD_G, stream);
         if ((gs = run_gemm(g, P, w.err, stream)) != PMOE_OK) return gs;
     }
-    if (d_topk_w) launch_dtw_reduce(P, I / 32, w.dtw_part, rt->perm, d_topk_w, stream);
-    // dh = dh~ R_down^T, then the SwiGLU backward into [dg | du]
-    launch_rotate_tc(b, true, true, w.dht, I, false, rt->perm, k, rt->idx, R_dn, sd, I, w.dgu,
-                     2 * (int64_t)I, L.rtiles, L.chunk_rtiles, L.chunk_rtiles + nch, maxrt, 0, cx,
-                     stream);
+    if (d_topk_w) launch_dtw_reduce(P, I / 32, w.dtw_part, rt->inv_perm, d_topk_w, stream);
+    // dh = dh~ R_down^T (FP32 dh~ split into two BF16 parts), then the SwiGLU
+    // backward from the saved FP32 g, u into FP16 [dg | du]
+    {
+        RotCall c = rot_rows(b, true, w.dht, I, nullptr, k, R_dn, sd, I, w.dgu, 2 * (int64_t)I,
+                             L.rtiles, rtb, rte, maxrt, 0);
+        c.src_f32 = true;
+        c.swiglu_bwd = true;
+        c.ctxf = ctx_gu;
+        launch_rotate_tc(c, stream);
+    }
     if (R_dn)
-        launch_outer_tc(nsets_dn, P, I, b, h, 3 * (int64_t)I, false, rt->perm, k, w.dht, I,
+        launch_outer_tc(nsets_dn, P, I, b, h, I, false, rt->perm, k, w.dht, true, I,
                         sd ? rt->offsets : nullptr, dR_down, stream);
 
+    // dx~ = [dg | du] W13 on FP16 operands (dg, du to 11 significant bits)
     GemmArgs x{};
-    x.kind = GK_BWD_DX;
+    x.kind = GK_BWD_DX_F16;
     x.fmt = fmt;
     x.wq = (const uint8_t *)wts->w13;
     x.ws = (const uint8_t *)wts->s13;
@@ -664,7 +722,7 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
     x.chunk_tiles = L.chunk_tiles;
     x.c0 = 0;
     x.c1 = nch;
-    x.out = w.dxt;
+    x.outf = w.dxt;
     x.I = I;
     x.nmat = E;
     {
@@ -672,17 +730,18 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
         if ((gs = run_gemm(x, P, w.err, stream)) != PMOE_OK) return gs;
     }
     if (R_up)
-        launch_outer_tc(nsets_up, P, d, b, (const uint16_t *)X, d, true, rt->perm, k, w.dxt, d,
+        launch_outer_tc(nsets_up, P, d, b, (const uint16_t *)X, d, true, rt->perm, k, w.dxt, true, d,
                         su ? rt->offsets : nullptr, dR_up, stream);
-    // dx_pair = dx~ R_up^T (into the dY buffer), then the slot sum per token
-    const uint16_t *dxp = w.dxt;
-    if (R_up) {
-        launch_rotate_tc(b, true, false, w.dxt, d, false, rt->perm, k, rt->idx, R_up, su, d, w.dyp,
-                         d, L.rtiles, L.chunk_rtiles, L.chunk_rtiles + nch, maxrt, 0, nullptr,
-                         stream);
-        dxp = w.dyp;
+    // dx_pair = dx~ R_up^T (FP32; without an adapter the same pass as the
+    // identity, so that R = I and no adapter agree bit for bit), then the
+    // slot sum per token
+    {
+        RotCall c = rot_rows(b, true, w.dxt, d, nullptr, k, R_up, su, d, w.dxp, d, L.rtiles, rtb, rte,
+                             maxrt, 0);
+        c.src_f32 = c.out_f32 = true;
+        launch_rotate_tc(c, stream);
     }
-    launch_combine(dims.T, d, k, dxp, rt->inv_perm, nullptr, (uint16_t *)dX, stream);
+    launch_combine(dims.T, d, k, w.dxp, rt->inv_perm, nullptr, (uint16_t *)dX, stream);
     return launched(stream);
 }
 
@@ -786,9 +845,9 @@ pmoe_status adapter_apply(int32_t rows, int32_t dim, int32_t b, const void *X, c
     if (rows == 0) return PMOE_OK;
     if (!X || !R || !Xr || X == Xr || !aligned16(X) || !aligned16(R) || !aligned16(Xr))
         return PMOE_ERR_INVALID_ARG;
-    launch_rotate_tc(b, false, false, (const uint16_t *)X, dim, false, nullptr, 1, nullptr,
-                     (const uint16_t *)R, 0, dim, (uint16_t *)Xr, dim, nullptr, nullptr, nullptr,
-                     0, rows, nullptr, stream);
+    launch_rotate_tc(rot_rows(b, false, X, dim, nullptr, 1, (const uint16_t *)R, 0, dim, Xr, dim,
+                              nullptr, nullptr, nullptr, 0, rows),
+                     stream);
     return launched(stream);
 }
 
@@ -801,11 +860,11 @@ pmoe_status adapter_grad(int32_t rows, int32_t dim, int32_t b, const void *X, co
     if (!aligned16(X) || !aligned16(dXr) || !aligned16(R) || !aligned16(dX) || !aligned16(dR))
         return PMOE_ERR_INVALID_ARG;
     if (dX && rows > 0)
-        launch_rotate_tc(b, true, false, (const uint16_t *)dXr, dim, false, nullptr, 1, nullptr,
-                         (const uint16_t *)R, 0, dim, (uint16_t *)dX, dim, nullptr, nullptr, nullptr,
-                         0, rows, nullptr, stream);
-    launch_outer_tc(1, rows, dim, b, (const uint16_t *)X, dim, false, nullptr, 1,
-                    (const uint16_t *)dXr, dim, nullptr, dR, stream);
+        launch_rotate_tc(rot_rows(b, true, dXr, dim, nullptr, 1, (const uint16_t *)R, 0, dim, dX, dim,
+                                  nullptr, nullptr, nullptr, 0, rows),
+                         stream);
+    launch_outer_tc(1, rows, dim, b, (const uint16_t *)X, dim, false, nullptr, 1, dXr, false, dim,
+                    nullptr, dR, stream);
     return launched(stream);
 }
 
@@ -814,7 +873,7 @@ namespace pmoe {
 struct DenseWs {
     GgWs g;
     int32_t *offsets;
-    uint16_t *buf;   // x~ (forward) or dx~ (backward), [rows, K] bf16
+    void *buf;   // x~ (forward, BF16) or dx~ (backward, FP32), [rows, K]
 };
 static DenseWs carve_dense(void *ws, int rows, int K, size_t *bytes)
 {
@@ -824,7 +883,7 @@ static DenseWs carve_dense(void *ws, int rows, int K, size_t *bytes)
     Carver c(ws);
     c.off = gb;
     w.offsets = c.take<int32_t>(2);
-    w.buf = c.take<uint16_t>((int64_t)(rows > 0 ? rows : 1) * K);
+    w.buf = c.take<float>((int64_t)(rows > 0 ? rows : 1) * K);
     if (bytes) *bytes = c.off;
     return w;
 }
@@ -838,7 +897,8 @@ static bool dense_shape_ok(pmoe_wfmt fmt, int N, int K, int b, int rows)
 }
 // One frozen [N, K] matrix as a single-expert grouped GEMM over rows 0..rows-1.
 static pmoe_status dense_gemm(pmoe_wfmt fmt, const void *q, const void *s, int N, int K, bool trans,
-                              const void *A, int rows, void *out, DenseWs &w, cudaStream_t st)
+                              const void *A, int rows, void *out, bool out_f32, DenseWs &w,
+                              cudaStream_t st)
 {
     launch_set_offsets(w.offsets, rows, st);
     launch_offsets_to_active(1, rows, w.offsets, w.g.counts, w.g.active, w.g.num_active, w.g.err, st);
@@ -860,7 +920,8 @@ static pmoe_status dense_gemm(pmoe_wfmt fmt, const void *q, const void *s, int N
     g.chunk_tiles = w.g.chunk_tiles;
     g.c0 = 0;
     g.c1 = 1;
-    g.out = (uint16_t *)out;
+    if (out_f32) g.outf = (float *)out;
+    else g.out = (uint16_t *)out;
     g.I = N;
     g.nmat = 1;
     return run_gemm(g, rows, w.g.err, st);
@@ -890,12 +951,12 @@ pmoe_status dense_linear_forward(pmoe_wfmt fmt, const void *q, const void *s, in
     if (rows == 0) return PMOE_OK;
     const void *A = X;
     if (R) {   // x~ = bf16(x blockdiag(R))
-        launch_rotate_tc(block, false, false, (const uint16_t *)X, K, false, nullptr, 1, nullptr,
-                         (const uint16_t *)R, 0, K, w.buf, K, nullptr, nullptr, nullptr, 0, rows,
-                         nullptr, stream);
+        launch_rotate_tc(rot_rows(block, false, X, K, nullptr, 1, (const uint16_t *)R, 0, K, w.buf, K,
+                                  nullptr, nullptr, nullptr, 0, rows),
+                         stream);
         A = w.buf;
     }
-    pmoe_status st = dense_gemm(fmt, q, s, N, K, false, A, rows, Y, w, stream);
+    pmoe_status st = dense_gemm(fmt, q, s, N, K, false, A, rows, Y, false, w, stream);
     if (st != PMOE_OK) return st;
     return launched(stream);
 }
@@ -919,16 +980,19 @@ pmoe_status dense_linear_backward(pmoe_wfmt fmt, const void *q, const void *s, i
             return PMOE_ERR_CUDA;
         return PMOE_OK;
     }
-    // G = dY W (contraction over the stored rows); with an adapter it is
-    // the BF16 tensor dx~, then dX = bf16(dx~ R^T) and dR = sum x^T dx~
-    pmoe_status st = dense_gemm(fmt, q, s, N, K, true, dY, rows, R ? (void *)w.buf : dX, w, stream);
+    // dx~ = dY W (contraction over the stored rows); with an adapter dx~ is
+    // kept in FP32, then dX = bf16(dx~ R^T) and dR = sum x^T dx~ (dx~ split
+    // into two BF16 parts for the MMAs)
+    pmoe_status st = dense_gemm(fmt, q, s, N, K, true, dY, rows, R ? w.buf : dX, R != nullptr, w,
+                                stream);
     if (st != PMOE_OK) return st;
     if (R) {
-        launch_outer_tc(1, rows, K, block, (const uint16_t *)X, K, false, nullptr, 1, w.buf, K,
+        launch_outer_tc(1, rows, K, block, (const uint16_t *)X, K, false, nullptr, 1, w.buf, true, K,
                         nullptr, dR, stream);
-        launch_rotate_tc(block, true, false, w.buf, K, false, nullptr, 1, nullptr,
-                         (const uint16_t *)R, 0, K, (uint16_t *)dX, K, nullptr, nullptr, nullptr, 0,
-                         rows, nullptr, stream);
+        RotCall c = rot_rows(block, true, w.buf, K, nullptr, 1, (const uint16_t *)R, 0, K, dX, K,
+                             nullptr, nullptr, nullptr, 0, rows);
+        c.src_f32 = true;
+        launch_rotate_tc(c, stream);
     }
     return launched(stream);
 }

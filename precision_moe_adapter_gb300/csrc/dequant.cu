@@ -1,4 +1,4 @@
-// dequant.cu -- the "临时反量化" step (page 1, 技艺细节): frozen INT4 /
+// dequant.cu -- the temporary dequantization step (Orbit announcement, 技艺细节): frozen INT4 /
 // MXFP4 / FP8 weights to BF16, for one matrix or for the experts of one
 // chunk into the bounded global scratch that the next chunk reuses.
 #include "common.cuh"

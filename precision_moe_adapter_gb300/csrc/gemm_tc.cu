@@ -2,6 +2,7 @@
 // descriptors (cuTensorMapEncodeTiled reached through the runtime's driver
 // entry point, so the library does not link libcuda) and the dispatch by
 // weight format.
+#include <atomic>
 #include <mutex>
 
 #include "gemm_tc_host.cuh"
@@ -35,17 +36,18 @@ static EncodeTiled encoder()
     return fn;
 }
 
-// 2-D BF16 row-major [rows, cols] tensor, box of box_rows rows x 64 columns
-// (128 bytes: one swizzle row), 128-byte swizzle, zero fill out of bounds.
+// 16-bit row-major [rows][cols] tensor (BF16, or FP16: TMA copies the bits)
+// as a 3-D map with one plane, box of box_rows rows x 64 columns (128 bytes:
+// one swizzle row), 128-byte swizzle, zero fill out of bounds.
 bool make_rows_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int box_rows)
 {
     EncodeTiled enc = encoder();
     if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, 1};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)(rows > 0 ? rows : 1) * cols * 2};
+    cuuint32_t box[3] = {(cuuint32_t)kBK, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -84,6 +86,24 @@ bool make_slots_tmap(CUtensorMap *m, const void *base, int64_t slots, int64_t ro
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// One-shot test hook (pmoe_debug_expire_gemm_wait): the wait limit of the
+// next grouped-GEMM launch, 0 when none is armed.
+static std::atomic<uint64_t> g_expire_wait_ns{0};
+
+void take_wait_hook(uint64_t &wait_ns, int &skip_item)
+{
+    const uint64_t v = g_expire_wait_ns.exchange(0);
+    wait_ns = v ? v : kWaitNs;
+    skip_item = v ? 0 : -1;
+}
+
+bool arm_wait_hook(uint64_t wait_ns)
+{
+    if (wait_ns < 100000ull || wait_ns > kWaitNs) return false;
+    g_expire_wait_ns.store(wait_ns);
+    return true;
+}
+
 int num_sms()
 {
     static int n = 0;
@@ -112,3 +132,8 @@ bool launch_gemm_tc(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st)
 }
 
 }  // namespace pmoe
+
+extern "C" pmoe_status pmoe_debug_expire_gemm_wait(uint64_t wait_ns)
+{
+    return pmoe::tc::arm_wait_hook(wait_ns) ? PMOE_OK : PMOE_ERR_INVALID_ARG;
+}

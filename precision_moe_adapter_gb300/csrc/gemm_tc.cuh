@@ -1,6 +1,7 @@
 // gemm_tc.cuh -- grouped GEMM of the layer on the 5th-generation tensor
 // cores (tcgen05 + TMEM + TMA), with the frozen weights dequantized tile by
-// tile into shared memory ("临时反量化后实行 grouped GEMM", page 1, 技艺细节).
+// tile into shared memory (Orbit announcement, 技艺细节: the active experts'
+// weights are dequantized to BF16 only while their grouped GEMM runs).
 //
 // Orientation: the weights are the MMA's M operand (128 output features per
 // tile) and the tokens of one expert are the N operand (16..256 rows per
@@ -65,7 +66,7 @@ constexpr int kDqWarps = PMOE_DQ_WARPS;
 constexpr int kConvGroups = PMOE_CONV_GROUPS;   // converter groups taking alternate stages
 constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;
 constexpr int kTmemCols = 512;
-constexpr unsigned long long kWaitNs = 2000000000ull;   // bounded waits: 2 s
+constexpr unsigned long long kWaitNs = 2000000000ull;   // bounded waits: 2 s (default)
 
 // ------------------------------------------------------------------ PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -101,16 +102,17 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
         : "memory");
     return ok != 0;
 }
-// Bounded wait: gives up after kWaitNs, records PMOE_ERR_TIMEOUT with the
+// Bounded wait: gives up after limit_ns, records PMOE_ERR_TIMEOUT with the
 // waiting role and returns false (the caller then leaves its loop).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, DevErr *err, int where)
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, DevErr *err, int where,
+                                          uint64_t limit_ns)
 {
     if (mbar_try(bar, parity)) return true;
     uint64_t t0 = globaltimer();
     while (true) {
         for (int i = 0; i < 64; ++i)
             if (mbar_try(bar, parity)) return true;
-        if (globaltimer() - t0 > kWaitNs) {
+        if (globaltimer() - t0 > limit_ns) {
             record_error(err, PMOE_ERR_TIMEOUT, where, (int)blockIdx.x);
             return false;
         }
@@ -160,12 +162,22 @@ __device__ __forceinline__ uint64_t sdesc_mn(uint32_t saddr)
     d |= (uint64_t)2 << 61;
     return d;
 }
-// Instruction descriptor, kind::f16: BF16 A and B, FP32 D, M x N; B K-major,
-// A K-major or (a_mn) MN-major.
-__device__ __forceinline__ uint32_t idesc_bf16(int M, int N, bool a_mn = false)
+// Instruction descriptor, kind::f16: BF16 (or, f16, FP16) A and B, FP32 D,
+// M x N; B K-major, A K-major or (a_mn) MN-major.
+__device__ __forceinline__ uint32_t idesc_bf16(int M, int N, bool a_mn = false, bool f16 = false)
 {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) |
+    const uint32_t ab = f16 ? 0u : 1u;   // operand format: 0 FP16, 1 BF16
+    return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)a_mn << 15) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// A BF16 pair re-encoded as an FP16 pair (exact for values in the FP16
+// normal range and zero)
+__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t p)
+{
+    uint32_t h;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(__uint_as_float(p & 0xFFFF0000u)),
+        "f"(__uint_as_float(p << 16)));
+    return h;
 }
 // Called by a whole converged warp, so the issue loop's operands stay
 // uniform: one K step of 64, i.e. four MMAs of K = 16 (descriptors a0..a3,
@@ -219,6 +231,34 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+// total += partial over one warp's 32 TMEM lanes, columns [0, ncols): 16
+// columns of each buffer per step, FP32 additions (round to nearest)
+__device__ __forceinline__ void tmem_drain(uint32_t part, uint32_t total, int ncols)
+{
+    for (int c0 = 0; c0 < ncols; c0 += 16) {
+        uint32_t p[16], t[16];
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n"
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n"
+            "tcgen05.wait::ld.sync.aligned;"
+            : "=r"(p[0]), "=r"(p[1]), "=r"(p[2]), "=r"(p[3]), "=r"(p[4]), "=r"(p[5]), "=r"(p[6]),
+              "=r"(p[7]), "=r"(p[8]), "=r"(p[9]), "=r"(p[10]), "=r"(p[11]), "=r"(p[12]), "=r"(p[13]),
+              "=r"(p[14]), "=r"(p[15]), "=r"(t[0]), "=r"(t[1]), "=r"(t[2]), "=r"(t[3]), "=r"(t[4]),
+              "=r"(t[5]), "=r"(t[6]), "=r"(t[7]), "=r"(t[8]), "=r"(t[9]), "=r"(t[10]), "=r"(t[11]),
+              "=r"(t[12]), "=r"(t[13]), "=r"(t[14]), "=r"(t[15])
+            : "r"(part + c0), "r"(total + c0)
+            : "memory");
+#pragma unroll
+        for (int i = 0; i < 16; ++i) t[i] = __float_as_uint(__fadd_rn(__uint_as_float(t[i]), __uint_as_float(p[i])));
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+                total + c0),
+            "r"(t[0]), "r"(t[1]), "r"(t[2]), "r"(t[3]), "r"(t[4]), "r"(t[5]), "r"(t[6]), "r"(t[7]),
+            "r"(t[8]), "r"(t[9]), "r"(t[10]), "r"(t[11]), "r"(t[12]), "r"(t[13]), "r"(t[14]), "r"(t[15])
+            : "memory");
+    }
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v)
 {
@@ -295,18 +335,24 @@ struct TcArgs {
     int c0, c1;
     int slot_index;
     int scale_tma;              // backward kinds: scales by TMA (tmS) instead of cp.async
-    uint16_t *out;
-    uint16_t *ctx;
+    uint16_t *out;              // BF16 output (when outf is NULL)
+    float *ctxf;                // GU: saved g | u rows [P, 2I] f32 (or NULL)
     int I;
     const float *w;
     const int32_t *perm;
     const uint16_t *ht;
     float *dtw_part;
-    float *outf;
+    float *outf;                // FP32 output: router partials, o, dh~ or dx~
     int64_t outf_split;         // router: elements between the partials of two K splits
     DevErr *err;
+    uint64_t wait_ns;           // limit of every bounded wait
+    int skip_commit_item;       // test hook: work item whose accumulator-full signal the
+                                // MMA issuer withholds (-1: none)
 };
 
+#ifndef PMOE_GU_CHUNK
+#define PMOE_GU_CHUNK 8
+#endif
 // ------------------------------------------------------------------ pipeline sizes
 // Per kind and weight format.  Packed weight tiles come by TMA into a raw
 // ring of kRawTma stages, each followed by the tile's scale words, which the
@@ -324,7 +370,18 @@ struct TcArgs {
 template <int KIND, int FMT>
 struct Pipe {
     // backward kinds: the contraction runs over the stored matrix's rows
-    static constexpr bool kTrans = KIND == GK_BWD_G || KIND == GK_BWD_DX;
+    static constexpr bool kTrans = KIND == GK_BWD_G || KIND == GK_BWD_DX || KIND == GK_BWD_DX_F16;
+    // FP16 operands: the converters write the weights' BF16 values in FP16
+    // encoding and the token operand is FP16 (11 significant bits)
+    static constexpr bool kF16 = KIND == GK_BWD_DX_F16;
+    static constexpr int kBStage = kBBytes;
+    // Chunked accumulation (gate/up, whose sums are rounded to BF16 in h):
+    // the tensor cores' FP32 accumulation loses about one bit per 16-long K
+    // step, so over thousands of steps g and u drift far beyond FP32 rounding
+    // and flip the BF16 rounding of h.  Each run of kChunk K steps is summed
+    // in its own TMEM buffer and added into the tile's total by the epilogue
+    // warps in FP32, which bounds the drift by the chunk length.
+    static constexpr int kChunk = KIND == GK_FWD_GU ? PMOE_GU_CHUNK : 1 << 30;
     static constexpr bool kBf16 = FMT == kFmtBF16;
     static constexpr bool kTmaRaw = !kBf16;
     static constexpr bool kFp8 = FMT == PMOE_W_FP8_B128_F32;
@@ -360,7 +417,7 @@ struct Pipe {
     // transaction barrier while the tile is in use).
     static_assert(kRawTma % kProd == 0, "raw ring size must be a multiple of the producer warps");
     static constexpr int kNumBars = 2 * kStagesA + 4 + 2 * kRawTma;
-    static constexpr int kBarOff = kStagesA * kABytes + kStagesB * kBBytes;
+    static constexpr int kBarOff = kStagesA * kABytes + kStagesB * kBStage;
     static constexpr int kBarBytes = 8 * kNumBars + 16;
     static constexpr int kRawOff = (kBarOff + kBarBytes + 1023) & ~1023;
     static constexpr size_t kSmem = (size_t)kRawOff + kRawBytes + 1024;
@@ -597,7 +654,12 @@ struct Dequant {
         const int r = tg & 7, mq = (tg >> 3) & 3, kg = tg >> 5;
         const uint32_t base = sA + kg * 2048 + (mq >> 1) * 1024 + r * 128;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) st_shared_v4(base + (((4 * (mq & 1) + j) ^ r) << 4), out[j]);
+        for (int j = 0; j < 4; ++j) {
+            uint4 v = out[j];
+            if (KIND == GK_BWD_DX_F16)   // the same values in FP16 encoding
+                v = make_uint4(bf2_to_h2(v.x), bf2_to_h2(v.y), bf2_to_h2(v.z), bf2_to_h2(v.w));
+            st_shared_v4(base + (((4 * (mq & 1) + j) ^ r) << 4), v);
+        }
     }
 };
 
@@ -623,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const uint32_t sA0 = smem_u32(smem);
     const uint32_t sB0 = sA0 + kStages * kABytes;
-    const uint32_t bar0 = sB0 + kStagesB * kBBytes;
+    const uint32_t bar0 = sB0 + kStagesB * PP::kBStage;
     uint32_t *tmem_slot = (uint32_t *)(smem + PP::kBarOff + 8 * PP::kNumBars);
     // full_a(s): step g's A and B are in place (s = g % kStages); empty(s):
     // the MMAs of the step that last used A slot s have completed
@@ -692,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                 for (int ks = 0; ks < nk; ++ks, ++g) {
                     if (kProd > 1 && g % kProd != prod_part) continue;
                     const int r = g % PP::kRawTma;
-                    if (!(ok = mbar_wait(raw_empty(r), ((g / PP::kRawTma) & 1) ^ 1, a.err, 7))) break;
+                    if (!(ok = mbar_wait(raw_empty(r), ((g / PP::kRawTma) & 1) ^ 1, a.err, 7, a.wait_ns))) break;
                     const uint32_t dst = raw0 + r * PP::kRawTile;
                     const uint8_t *ws = a.ws + widx * a.ws_stride;
                     if constexpr (PP::kTrans) {
@@ -772,7 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                 // MMAs (which also frees A slot s for the BF16 weight tiles)
                 if (g >= (uint32_t)kStagesB) {
                     const uint32_t gp = g - kStagesB;
-                    if (!(ok = mbar_wait(empty(fb(gp)), fph(gp), a.err, 1))) break;
+                    if (!(ok = mbar_wait(empty(fb(gp)), fph(gp), a.err, 1, a.wait_ns))) break;
                 }
                 const uint32_t fbar = full_a(fb(g));
                 if (lane == 0) {
@@ -785,7 +847,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                         // router: split widx covers K steps widx*nk .. of the
                         // [X | X | X] operand of length 3d
                         const int xb = KIND == GK_ROUTER ? (int)((((int64_t)widx * nk + ks) * kBK) % a.Kb) : ks * kBK;
-                        tma_load_2d(sB0 + sb * kBBytes + r0 * kBK * 2, tm, xb, tl.row0 + r0, fbar);
+                        tma_load_3d(sB0 + sb * PP::kBStage + r0 * kBK * 2, tm, xb, tl.row0 + r0, 0, fbar);
                         r0 += rows;
                     }
                     if constexpr (PP::kBf16) {
@@ -817,31 +879,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             const uint64_t adesc0 = PP::kTrans ? sdesc_mn(sA0) : sdesc(sA0);
             const uint64_t bdesc0 = sdesc(sB0);
             constexpr uint32_t kAStep = PP::kTrans ? 4096 >> 4 : 32 >> 4;   // per K step of 16
+            // The two 256-column TMEM buffers: item li sums into buffer li & 1
+            // (its total) and, when its K loop is chunked, runs every chunk
+            // after the first in the other buffer (a partial the epilogue adds
+            // into the total).  fills0/1 count each buffer's fills; a fill
+            // waits until the epilogue has consumed the previous one.
+            uint32_t fills0 = 0u, fills1 = 0u;   // (scalars: no local-memory array)
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++li) {
                 const Tile tl = a.tiles[tbeg + item / nft];
                 const int N = (tl.nrows + 15) & ~15;
-                const uint32_t idesc = idesc_bf16(kM, N, PP::kTrans);
-                const int acc = li & 1;
-                // every lane waits; the outcome is made warp-uniform so that the
-                // lanes stay converged for the elected issue
-                if (!(ok = __all_sync(0xffffffffu, mbar_wait(tempty(acc), ((li >> 1) & 1) ^ 1, a.err, 2))))
-                    break;
-                tc_fence_after();
-                const uint32_t d = tmem + acc * (kTmemCols / 2);
+                const uint32_t idesc = idesc_bf16(kM, N, PP::kTrans, PP::kF16);
+                const int tot = li & 1, par = tot ^ 1;
                 for (int ks = 0; ks < nk; ++ks, ++g) {
                     const int s = g % kStages;
-                    if (!(ok = __all_sync(0xffffffffu, mbar_wait(full_a(fb(g)), fph(g), a.err, 3)))) break;
+                    const bool first = ks % PP::kChunk == 0;
+                    const int buf = ks < PP::kChunk ? tot : par;
+                    if (first) {
+                        // every lane waits; the outcome is made warp-uniform so
+                        // that the lanes stay converged for the elected issue
+                        const uint32_t u = buf ? fills1++ : fills0++;
+                        if (!(ok = __all_sync(0xffffffffu, mbar_wait(tempty(buf), (u & 1) ^ 1, a.err, 2, a.wait_ns))))
+                            break;
+                        tc_fence_after();
+                    }
+                    if (!(ok = __all_sync(0xffffffffu, mbar_wait(full_a(fb(g)), fph(g), a.err, 3, a.wait_ns)))) break;
                     tc_fence_after();
                     // K step of 16: +32 B inside the K-major swizzle row, or two
                     // 8-row K groups (2 x 2048 B) of the MN-major tile
                     const uint64_t ad = adesc0 + (uint32_t)(s * (kABytes >> 4));
-                    const uint64_t bd = bdesc0 + (uint32_t)((g % kStagesB) * (kBBytes >> 4));
+                    const uint64_t bd = bdesc0 + (uint32_t)((g % kStagesB) * (PP::kBStage >> 4));
                     static_assert(kBK == 64, "four MMAs of K = 16 per step");
                     const uint64_t av[4] = {ad, ad + kAStep, ad + 2 * kAStep, ad + 3 * kAStep};
                     const uint64_t bv[4] = {bd, bd + 2, bd + 4, bd + 6};
-                    umma_step_warp(d, av, bv, idesc, ks != 0, empty(fb(g)));
+                    umma_step_warp(tmem + buf * (kTmemCols / 2), av, bv, idesc, !first, empty(fb(g)));
+                    // a partial chunk is complete: hand it to the epilogue
+                    if (buf == par && ((ks + 1) % PP::kChunk == 0 || ks + 1 == nk)) umma_commit_warp(tfull(par));
                 }
-                if (ok) umma_commit_warp(tfull(acc));
+                // (the test hook withholds one accumulator-full signal: the
+                // epilogue's bounded wait for it then runs out)
+                if (ok && item != a.skip_commit_item) umma_commit_warp(tfull(tot));
             }
         }
     } else if (warp >= kDqWarp0) {
@@ -879,7 +955,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             };
             auto compute = [&](const Cur &c, uint4 (&o)[kEPT / 8]) -> bool {
                 const int r = c.j % PP::kRawTma;
-                if (!mbar_wait(raw_full(r), (c.j / PP::kRawTma) & 1, a.err, 8)) return false;
+                if (!mbar_wait(raw_full(r), (c.j / PP::kRawTma) & 1, a.err, 8, a.wait_ns)) return false;
                 const uint8_t *rawt = smem + PP::kRawOff + r * PP::kRawTile;
                 if constexpr (PP::kTrans)
                     Dequant<KIND, FMT>::compute_t(a, c.f0, c.ks, tg, rawt, o);
@@ -896,7 +972,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             // group's next step into nxt, publish step g
             auto body = [&](uint32_t g, const uint4 (&cur)[kEPT / 8], uint4 (&nxt)[kEPT / 8]) -> bool {
                 const int s = g % kStages;
-                if (!mbar_wait(empty(fb(g)), fph(g) ^ 1, a.err, 5)) return false;
+                if (!mbar_wait(empty(fb(g)), fph(g) ^ 1, a.err, 5, a.wait_ns)) return false;
                 if constexpr (PP::kTrans)
                     Dequant<KIND, FMT>::store_t(tg, cur, sA0 + s * kABytes);
                 else
@@ -922,14 +998,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
         // ---------------- epilogue (warps 0-3: TMEM lanes 32*warp .. +31)
         uint32_t li = 0;
         const int q = warp;
+        uint32_t cons0 = 0u, cons1 = 0u;   // fills of each TMEM buffer consumed so far
+        const int nchunks = (nk + PP::kChunk - 1) / PP::kChunk;
+        const uint32_t lanes = (uint32_t)(32 * q) << 16;
         for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++li) {
             const Tile tl = a.tiles[tbeg + item / nft];
             const int f0 = (item % nft) * a.m_tile;
-            const int acc = li & 1;
-            if (!mbar_wait(tfull(acc), (li >> 1) & 1, a.err, 6)) break;
-            tc_fence_after();
-            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + acc * (kTmemCols / 2);
+            const int tot = li & 1, par = tot ^ 1;
             const int ncols = (tl.nrows + 15) & ~15;
+            // chunked K loop: add each partial into the total (the MMA warp
+            // fills the partial buffer again once it is released)
+            bool ok = true;
+            for (int j = 1; j < nchunks && ok; ++j) {
+                const uint32_t u = par ? cons1++ : cons0++;
+                if (!(ok = mbar_wait(tfull(par), u & 1, a.err, 9, a.wait_ns))) break;
+                tc_fence_after();
+                tmem_drain(tmem + lanes + par * (kTmemCols / 2), tmem + lanes + tot * (kTmemCols / 2), ncols);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty(par));
+            }
+            if (!ok) break;
+            const uint32_t ut = tot ? cons1++ : cons0++;
+            if (!mbar_wait(tfull(tot), ut & 1, a.err, 6, a.wait_ns)) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem + lanes + tot * (kTmemCols / 2);
             for (int c0 = 0; c0 < ncols; c0 += 16) {
                 float v[16];
                 tmem_ld16(taddr + c0, v);
@@ -948,11 +1041,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                             const int64_t r = tl.row0 + col;
                             const uint16_t h = f2bf(silu_f(g) * u);
                             a.out[r * a.I + f] = h;
-                            if (a.ctx) {   // saved for the backward: [g | u | h]
-                                uint16_t *c = a.ctx + r * 3 * a.I + f;
-                                c[0] = f2bf(g);
-                                c[a.I] = f2bf(u);
-                                c[2 * a.I] = h;
+                            if (a.ctxf) {   // saved for the backward: g, u in FP32
+                                a.ctxf[r * 2 * a.I + f] = g;
+                                a.ctxf[r * 2 * a.I + a.I + f] = u;
                             }
                         }
                     }
@@ -977,7 +1068,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                             const float wr = __shfl_sync(0xffffffffu, w_lane, jj);
                             const int64_t r = tl.row0 + c0 + jj;
                             part[j] = fl ? v[jj] * bf2f(hts[j]) : 0.f;
-                            if (fl && jj < ncol) a.out[r * a.Mtot + f] = f2bf(wr * v[jj]);
+                            if (fl && jj < ncol) a.outf[r * a.Mtot + f] = wr * v[jj];   // dh~ = w G, FP32
                         }
                         // sum over the warp's 32 features for the 8 columns at once
                         // (reduce-scatter over lane distances 16, 8, 4): lane l then
@@ -1009,19 +1100,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                         }
                     }
                 } else {
+                    // FP32 store (the layer's o and dx~: a warp writes 128 contiguous
+                    // bytes per column), or BF16
                     const int f = f0 + 32 * q + lane;
                     if (f < a.Mtot) {
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const int col = c0 + j;
-                            if (col < tl.nrows) a.out[(int64_t)(tl.row0 + col) * a.Mtot + f] = f2bf(v[j]);
+                            if (col >= tl.nrows) continue;
+                            const int64_t o = (int64_t)(tl.row0 + col) * a.Mtot + f;
+                            if (a.outf) a.outf[o] = v[j];
+                            else a.out[o] = f2bf(v[j]);
                         }
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty(acc));
+            if (lane == 0) mbar_arrive(tempty(tot));
         }
     }
     tc_fence_before();

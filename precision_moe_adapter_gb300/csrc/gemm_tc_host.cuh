@@ -9,6 +9,8 @@
 namespace pmoe {
 namespace tc {
 
+// 16-bit token operand [rows][cols] (as one plane of a 3-D map), box of
+// box_rows x 64 columns, 128-byte swizzle
 bool make_rows_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int box_rows);
 // uint8 [rows, row_bytes] tensor, box of box_rows x box_bytes, swizzle of
 // swizzle_bytes (0: none, 64 or 128; box_bytes must then equal it)
@@ -18,6 +20,9 @@ bool make_bytes_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t row
 bool make_slots_tmap(CUtensorMap *m, const void *base, int64_t slots, int64_t rows, int64_t cols,
                      int64_t slot_bytes, int box_rows);
 int num_sms();
+// The bounded-wait limit and withheld item of the next launch: the armed test
+// hook (once), else the default limit and none.
+void take_wait_hook(uint64_t &wait_ns, int &skip_item);
 
 template <int KIND, int FMT>
 bool launch_kind(const CUtensorMap (&tmB)[4], const TcArgs &a, int64_t nmat, cudaStream_t st)
@@ -87,7 +92,7 @@ bool launch_fmt(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st)
     a.c1 = g.c1;
     a.slot_index = g.slot_index;
     a.out = g.out;
-    a.ctx = g.ctx;
+    a.ctxf = g.ctxf;
     a.I = g.I;
     a.w = g.w;
     a.perm = g.perm;
@@ -96,6 +101,7 @@ bool launch_fmt(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st)
     a.outf = g.outf;
     a.outf_split = g.outf_split;
     a.err = err;
+    take_wait_hook(a.wait_ns, a.skip_commit_item);
     switch (g.kind) {
     case GK_FWD_GU: return launch_kind<GK_FWD_GU, FMT>(tm, a, g.nmat, st);
     case GK_FWD_DOWN: return launch_kind<GK_FWD_DOWN, FMT>(tm, a, g.nmat, st);
@@ -104,6 +110,9 @@ bool launch_fmt(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st)
         return false;
     case GK_BWD_DX:
         if constexpr (FMT != kFmtBF16) return launch_kind<GK_BWD_DX, FMT>(tm, a, g.nmat, st);
+        return false;
+    case GK_BWD_DX_F16:
+        if constexpr (FMT != kFmtBF16) return launch_kind<GK_BWD_DX_F16, FMT>(tm, a, g.nmat, st);
         return false;
     case GK_ROUTER:
         if constexpr (FMT == kFmtBF16) return launch_kind<GK_ROUTER, FMT>(tm, a, g.nmat, st);

@@ -23,6 +23,10 @@ void launch_router_reduce(int T, int E, int splits, const float *part, float *lo
 void launch_router_prep(int T, int d, int E, const float *Wr, uint16_t *WrT3, Tile *tiles,
                         int32_t *chunk_tiles, int tile_rows, cudaStream_t st);
 int router_tile_rows(int T, int E, int splits, int num_sms);
+// Canonical router mode: FP32 logits (without bias) in one fixed summation
+// order (32 lane-strided fmaf chains, then a pairwise tree); d % 64 == 0.
+void launch_router_exact(int T, int d, int E, const uint16_t *X, const float *Wr, float *logits,
+                         cudaStream_t st);
 void launch_route_topk(int T, int E, int k, const float *logits, const float *bias, int32_t *idx,
                        float *w, float *logits_out, cudaStream_t st);
 size_t permute_ws_bytes(int P, int E);
@@ -51,7 +55,10 @@ void launch_cayley_grad(int nblk, int b, const float *S, const float *Rf, const 
 // grouped GEMM (gemm_tc*.cu)
 // GK_ROUTER: FP32 logits X Wr with Wr split into three BF16 terms stacked
 // along K (A = [E, 3d]); the token operand X [T, d] is read three times.
-enum GemmKind { GK_FWD_GU = 0, GK_FWD_DOWN = 1, GK_BWD_G = 2, GK_BWD_DX = 3, GK_ROUTER = 4 };
+// GK_BWD_DX_F16: GK_BWD_DX with FP16 operands (the token operand A is FP16;
+// the weights' BF16 values are used in FP16 encoding).
+enum GemmKind { GK_FWD_GU = 0, GK_FWD_DOWN = 1, GK_BWD_G = 2, GK_BWD_DX = 3, GK_ROUTER = 4,
+                GK_BWD_DX_F16 = 5 };
 constexpr int kFmtBF16 = 3;  // weights already dequantized (scratch mode)
 struct GemmArgs {
     int kind;
@@ -70,14 +77,15 @@ struct GemmArgs {
     const int32_t *chunk_tiles;  // tile range [chunk_tiles[c0], chunk_tiles[c1])
     int c0, c1;
     bool slot_index;         // weights indexed by chunk slot (scratch) instead of expert
-    uint16_t *out;           // [P, Nout] bf16
-    uint16_t *ctx;           // FWD_GU: [P, 3I] g|u|h or NULL
+    uint16_t *out;           // [P, Nout] bf16 (when outf is NULL)
+    float *ctxf;             // FWD_GU: saved g | u [P, 2I] f32, or NULL
     int I;
     const float *w;          // BWD_G: routing weights by pair id
     const int32_t *perm;
     const uint16_t *ht;      // BWD_G: h~ [P, I]
     float *dtw_part;         // BWD_G: [P, I/32]
-    float *outf;             // ROUTER: [splits][P, Nout] f32 partials
+    float *outf;             // ROUTER: [splits][P, Nout] f32 partials; DOWN, BWD_G,
+                             // BWD_DX*: [P, Nout] f32 output in place of out
     int64_t outf_split;      // ROUTER: P * Nout (elements between two splits' partials)
 };
 // tcgen05 grouped GEMM (returns false if the request cannot be
@@ -88,24 +96,43 @@ int gemm_num_sms();   // SMs of the current device (cached)
 void launch_offsets_to_active(int E, int rows, const int32_t *offsets, int32_t *counts,
                               int32_t *active, int32_t *num_active, DevErr *err, cudaStream_t st);
 
-// rotate_tc.cu: block-diagonal rotation on mma.sync.  Tiles: 64-row tiles
+// rotate_tc.cu: block-diagonal rotation on mma.sync.  Tiles: 128-row tiles
 // of one expert (indices *tbeg .. *tend-1), or NULL for rows 0..nrows-1 of
-// one shared rotation.  trans: R^T.  swiglu_bwd: the output is [dg | du]
-// (out_ld = 2*dim) from the saved [g | u | h] rows of ctx.
-void launch_rotate_tc(int b, bool trans, bool swiglu_bwd, const uint16_t *src, int64_t src_ld,
-                      bool gather, const int32_t *perm, int k, const int32_t *idx_flat,
-                      const uint16_t *R, int64_t stride, int dim, uint16_t *out, int64_t out_ld,
-                      const Tile *tiles, const int32_t *tbeg, const int32_t *tend, int max_tiles,
-                      int nrows, const uint16_t *ctx, cudaStream_t st,
-                      const uint16_t *R_alt = nullptr, const uint64_t *sel = nullptr);
-// dR[s][beta] = sum over rows of set s of a_blk^T g_blk on mma.sync
+// one shared rotation.
+struct RotCall {
+    int b;
+    bool trans;               // R^T
+    bool swiglu_bwd;          // out = FP16 [dg | du] (out_ld = 2*dim) from ctxf
+    const void *src;          // BF16 rows, or FP32 rows (src_f32)
+    bool src_f32;
+    int64_t src_ld;
+    const int32_t *perm;      // gather source row perm[r] / k (NULL: row r)
+    int k;
+    const uint16_t *R;        // NULL: identity
+    int64_t stride;
+    int dim;
+    void *out;                // BF16 rows, or FP32 rows (out_f32)
+    bool out_f32;
+    int64_t out_ld;
+    const Tile *tiles;
+    const int32_t *tbeg, *tend;
+    int max_tiles;
+    int nrows;
+    const float *ctxf;        // swiglu_bwd: saved [g | u] rows, FP32
+    const uint16_t *R_alt;
+    const uint64_t *sel;
+};
+void launch_rotate_tc(const RotCall &c, cudaStream_t st);
+// dR[s][beta] = sum over rows of set s of a_blk^T g_blk on mma.sync (g BF16,
+// or FP32 when g_f32)
 void launch_outer_tc(int nsets, int nrows, int dim, int b, const uint16_t *a, int64_t a_ld,
-                     bool gather, const int32_t *perm, int k, const uint16_t *g, int64_t g_ld,
+                     bool gather, const int32_t *perm, int k, const void *g, bool g_f32, int64_t g_ld,
                      const int32_t *offsets, float *dR, cudaStream_t st);
-constexpr int kRotTileRows = 64;
+constexpr int kRotTileRows = 128;
 
 // layer.cu
-void launch_combine(int T, int d, int k, const uint16_t *o, const int32_t *inv_perm,
+// Y[t] = bf16(sum_j w[t, j] o[inv_perm[t*k + j]]) over FP32 pair rows o
+void launch_combine(int T, int d, int k, const float *o, const int32_t *inv_perm,
                     const float *w, uint16_t *Y, cudaStream_t st);
 // adapter slots: snap = *ctrl (one atomic 64-bit read), *version_out =
 // snap >> 32 when given; publish: *ctrl = version << 32 | slot (atomic)
@@ -116,6 +143,8 @@ void launch_adapter_publish(uint64_t *ctrl, uint32_t slot, uint32_t version, cud
 void launch_set_offsets(int32_t *offsets, int rows, cudaStream_t st);
 void launch_gather_rows(int P, int d, int k, const uint16_t *src, const int32_t *perm,
                         uint16_t *out, cudaStream_t st);
-void launch_dtw_reduce(int P, int nparts, const float *part, const int32_t *perm, float *dtw,
+// d_topk_w[p] = sum of pair p's partials (row inv_perm[p]); 0 for a pair
+// left out of the grouping
+void launch_dtw_reduce(int P, int nparts, const float *part, const int32_t *inv_perm, float *dtw,
                        cudaStream_t st);
 }  // namespace pmoe

@@ -6,9 +6,9 @@
 
 namespace pmoe {
 
-// Y[t] = bf16(sum_j w[t,j] o[inv_perm[t*k + j]]), slots in order (w NULL:
-// unit weights, the slot sum of the backward).
-__global__ void __launch_bounds__(256) k_combine(int T, int d, int k, const uint16_t *__restrict__ o,
+// Y[t] = bf16(sum_j w[t,j] o[inv_perm[t*k + j]]), slots in order, over the
+// FP32 pair outputs o (w NULL: unit weights, the slot sum of the backward).
+__global__ void __launch_bounds__(256) k_combine(int T, int d, int k, const float *__restrict__ o,
                                                  const int32_t *__restrict__ inv_perm,
                                                  const float *__restrict__ w,
                                                  uint16_t *__restrict__ Y)
@@ -20,10 +20,11 @@ __global__ void __launch_bounds__(256) k_combine(int T, int d, int k, const uint
             int r = inv_perm[(int64_t)t * k + j];
             if (r < 0) continue;
             float wj = w ? w[(int64_t)t * k + j] : 1.f;
-            uint4 v = *(const uint4 *)(o + (int64_t)r * d + c);
-            const uint16_t *hv = (const uint16_t *)&v;
+            const float4 v0 = *(const float4 *)(o + (int64_t)r * d + c);
+            const float4 v1 = *(const float4 *)(o + (int64_t)r * d + c + 4);
+            const float hv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, bf2f(hv[i]), acc[i]);
+            for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, hv[i], acc[i]);
         }
         uint4 out;
         out.x = pack_bf2(acc[0], acc[1]);
@@ -34,7 +35,7 @@ __global__ void __launch_bounds__(256) k_combine(int T, int d, int k, const uint
     }
 }
 
-void launch_combine(int T, int d, int k, const uint16_t *o, const int32_t *inv_perm,
+void launch_combine(int T, int d, int k, const float *o, const int32_t *inv_perm,
                     const float *w, uint16_t *Y, cudaStream_t st)
 {
     if (T <= 0) return;
@@ -59,21 +60,26 @@ void launch_gather_rows(int P, int d, int k, const uint16_t *src, const int32_t 
     note_launch();
 }
 
+// d_topk_w[p] = sum of the I/32 partials of pair p's expert-sorted row, in
+// order; a pair left out of the grouping (inv_perm[p] < 0: an expert id out
+// of range) gets 0.  One thread per pair, so every write stays in [0, P).
 __global__ void k_dtw_reduce(int P, int nparts, const float *__restrict__ part,
-                             const int32_t *__restrict__ perm, float *__restrict__ dtw)
+                             const int32_t *__restrict__ inv_perm, float *__restrict__ dtw)
 {
-    int r = blockIdx.x * blockDim.x + threadIdx.x;
-    if (r >= P) return;
+    int p = blockIdx.x * blockDim.x + threadIdx.x;
+    if (p >= P) return;
+    const int r = inv_perm[p];
     float s = 0.f;
-    for (int q = 0; q < nparts; ++q) s += part[(int64_t)r * nparts + q];
-    dtw[perm[r]] = s;
+    if (r >= 0)
+        for (int q = 0; q < nparts; ++q) s += part[(int64_t)r * nparts + q];
+    dtw[p] = s;
 }
 
-void launch_dtw_reduce(int P, int nparts, const float *part, const int32_t *perm, float *dtw,
+void launch_dtw_reduce(int P, int nparts, const float *part, const int32_t *inv_perm, float *dtw,
                        cudaStream_t st)
 {
     if (P <= 0) return;
-    k_dtw_reduce<<<(int)cdiv(P, 256), 256, 0, st>>>(P, nparts, part, perm, dtw);
+    k_dtw_reduce<<<(int)cdiv(P, 256), 256, 0, st>>>(P, nparts, part, inv_perm, dtw);
     note_launch();
 }
 

@@ -46,9 +46,13 @@ int32_t *scratch_on_current_device()
 }
 }  // namespace
 
+// Bytes of the per-block histogram for P pairs and E experts, in 64-bit
+// arithmetic (the same layout as permute_ws_bytes, whose int argument the
+// caller's T*k is never narrowed into before this check).
 size_t permute_noalloc_need_bytes(int64_t P, int E)
 {
-    return permute_ws_bytes((int)P, E);
+    const int64_t blocks = P > 0 ? (P + 1023) / 1024 : 1;
+    return (size_t)blocks * (size_t)(E > 0 ? E : 0) * sizeof(int32_t);
 }
 
 }  // namespace pmoe
@@ -61,13 +65,14 @@ extern "C" pmoe_status moe_permute_noalloc(pmoe_dims dims, const int32_t *idx,
     if ((dims.T > 0 && (!idx || !out->perm || !out->inv_perm)) || !out->counts ||
         !out->offsets || !out->active || !out->num_active)
         return PMOE_ERR_INVALID_ARG;
-    // the per-block histogram must fit the fixed buffer
-    if (permute_noalloc_need_bytes((int64_t)dims.T * dims.k, dims.E) > kNoAllocScratchBytes)
+    // the per-block histogram must fit the fixed buffer (and T*k an int)
+    const int64_t P = (int64_t)dims.T * dims.k;
+    if (P > INT32_MAX || permute_noalloc_need_bytes(P, dims.E) > kNoAllocScratchBytes)
         return PMOE_ERR_WORKSPACE;
     int32_t *hist = scratch_on_current_device();
     if (!hist) return PMOE_ERR_CUDA;
     // no error word: an expert id outside [0, E) shows only in the outputs
-    launch_permute(dims.T * dims.k, dims.E, idx, out->counts, out->offsets, out->perm,
+    launch_permute((int)P, dims.E, idx, out->counts, out->offsets, out->perm,
                    out->inv_perm, out->active, out->num_active, hist, nullptr, stream);
     return cudaPeekAtLastError() == cudaSuccess ? PMOE_OK : PMOE_ERR_CUDA;
 }

@@ -1,27 +1,39 @@
 // rotate_tc.cu -- the block-diagonal orthogonal adapter on the tensor cores
-// (page 2, 机制拆解: OFT, a local orthogonal transform of the activations).
+// ("Orbit：把万亿模型 RL 后训练改写成部署一致性问题", 机制拆解: the OFT
+// adapter is a local orthogonal transform of the activations).
 //
-//   out[r, beta] = bf16( src[row(r), beta] R_e[beta] )      (or R_e[beta]^T)
+//   out[r, beta] = src[row(r), beta] R_e[beta]      (or R_e[beta]^T)
 //
 // for expert-sorted pair rows r of one expert e per tile, each b-wide
 // block beta separately.  The rotation is a dense contraction of b
-// multiply-adds per element (b = 64: 32 FLOP per byte moved), so it runs
-// on mma.sync m16n8k16 (BF16 in, FP32 accumulate); the kernel is bound by
-// moving the rows.  One CTA = 4 warps x 16 rows = a 64-row tile of one
-// expert; work items are (tile, group of blocks).
+// multiply-adds per element (b = 64: 32 FLOP per BF16 byte moved), so it
+// runs on mma.sync m16n8k16 (BF16 in, FP32 accumulate); the kernel is bound
+// by moving the rows.  One CTA = 8 warps x 16 rows = a 128-row tile of one
+// expert; a work item is (tile, group of blocks), and the next block's rows
+// and rotation block are fetched by cp.async while the current one is
+// multiplied (two stages).
 //
-// Epilogues: plain BF16 store, or the SwiGLU backward (dh = dh~ R^T, then
-// dg = dh u s(g)(1 + g(1 - s(g))), du = dh silu(g) from the saved g, u).
+// Sources are BF16, or FP32: an FP32 row is split into hi = bf16(x) and
+// lo = bf16(x - hi) (together within 2^-16 of x) and both parts go through
+// the MMA, so an FP32 tensor is rotated at FP32 accuracy.
+// Outputs: BF16 or FP32 rows, or the SwiGLU backward (dh = dh~ R^T, then
+// dg = dh u s(g)(1 + g(1 - s(g))), du = dh silu(g) from the saved FP32 g,
+// u) written as FP16 [dg | du] (11 significant bits: the operand of the
+// FP16 dx~ GEMM).
 //
 // Also: the per-block adapter gradient dR[e][beta] = sum_r a_blk^T g_blk
-// over the rows of expert e, in a fixed order (deterministic).
+// over the rows of expert e, in a fixed order (deterministic), with g BF16
+// or FP32 (split the same way).
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "launch.h"
 
 namespace pmoe {
 
-constexpr int kRotRows = 64;      // rows per tile
-constexpr int kRotBlocks = 8;     // b-blocks per work item
+constexpr int kRotRows = kRotTileRows;   // rows per tile (8 warps x 16)
+constexpr int kRotBlocks = 8;            // b-blocks per work item
+constexpr int kRotThreads = 256;
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &a, uint32_t &b, uint32_t &c,
                                         uint32_t &d)
@@ -52,57 +64,71 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool p
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(sz)
                  : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 __device__ __forceinline__ void cp_async_wait_all()
 {
     asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
 }
 
+// hi = bf16(x), lo = bf16(x - hi) for two FP32 values (one BF16 pair each)
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo)
+{
+    hi = pack_bf2(x0, x1);
+    lo = pack_bf2(x0 - bf2f(hi & 0xFFFFu), x1 - bf2f(hi >> 16));
+}
+
 enum RotEpi { ROT_STORE = 0, ROT_SWIGLU_BWD = 1 };
 
 struct RotArgs {
-    const uint16_t *src;       // source rows
+    const void *src;           // source rows, BF16 or FP32
     int64_t src_ld;            // elements between source rows
     int gather;                // source row = perm[r] / k (else r)
     const int32_t *perm;
     int k;
-    const int32_t *idx_flat;   // expert of pair p (per-expert R)
     const uint16_t *R;         // rotation blocks [dim/b, b, b] of expert 0, or NULL (identity)
     int64_t stride;            // elements between experts' block sets (0 = shared)
     int dim;
-    uint16_t *out;             // [P, out_ld] bf16
+    void *out;                 // rows [*, out_ld], BF16 or FP32; SWIGLU: FP16 [dg | du]
     int64_t out_ld;
-    const Tile *tiles;         // 64-row tiles of one expert, or NULL: rows 64i.. of one set
+    const Tile *tiles;         // 128-row tiles of one expert, or NULL: rows 128i.. of one set
     const int32_t *tbeg, *tend;   // device range of tiles to process
     int nrows;                 // rows when tiles == NULL
-    const uint16_t *ctx;       // ROT_SWIGLU_BWD: [g | u | h] rows of 3*dim
+    const float *ctxf;         // SWIGLU: saved [g | u] rows of 2*dim FP32
     const uint16_t *R_alt;     // second adapter slot (NULL: none)
     const uint64_t *sel;       // adapter snapshot: low bit of the low word picks R_alt
 };
 
-// smem row pitch (elements): b + 8 keeps ldmatrix rows on distinct banks
-template <int B>
+// Shared memory of one stage: the source tile (BF16 rows of b + 8
+// elements for conflict-free ldmatrix, or FP32 rows of b + 8 floats for
+// conflict-free float2 fragment loads) and the rotation block.
+template <int B, bool F32IN>
 struct RotSmem {
-    static constexpr int kPitch = B + 8;
-    static constexpr int kX = kRotRows * kPitch;   // x tile
-    static constexpr int kR = (B > kRotRows ? B : kRotRows) * kPitch;   // rotation block / du tile
-    static constexpr int kBytes = (kX + kR) * 2;
+    static constexpr int kPitchX = B + 8;                   // elements per source row
+    static constexpr int kXBytes = kRotRows * kPitchX * (F32IN ? 4 : 2);
+    static constexpr int kPitchR = B + 8;
+    static constexpr int kRBytes = B * kPitchR * 2;
+    static constexpr int kStage = kXBytes + kRBytes;
+    static constexpr int kBytes = 2 * kStage;
 };
 
-template <int B, bool TRANS, int EPI>
-__global__ void __launch_bounds__(128) k_rotate_mma(RotArgs a)
+template <int B, bool TRANS, int EPI, bool F32IN, bool F32OUT>
+__global__ void __launch_bounds__(kRotThreads, 2) k_rotate_mma(RotArgs a)
 {
-    using S = RotSmem<B>;
-    extern __shared__ __align__(16) uint16_t rsm[];
-    uint16_t *xs = rsm, *rs = rsm + S::kX;
-    const uint32_t xs_a = (uint32_t)__cvta_generic_to_shared(xs);
-    const uint32_t rs_a = (uint32_t)__cvta_generic_to_shared(rs);
+    using S = RotSmem<B, F32IN>;
+    extern __shared__ __align__(16) uint8_t rsm[];
+    const uint32_t sm0 = (uint32_t)__cvta_generic_to_shared(rsm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nblk = a.dim / B;
     const int ngroups = (nblk + kRotBlocks - 1) / kRotBlocks;
     const int t0 = a.tiles ? *a.tbeg : 0;
     const int nt = a.tiles ? *a.tend - t0 : (a.nrows + kRotRows - 1) / kRotRows;
     const int64_t items = (int64_t)nt * ngroups;
-    constexpr int CPR = B / 8;   // 16-byte chunks per block row
+    constexpr int kEsz = F32IN ? 4 : 2;
+    constexpr int CPR = B * kEsz / 16;   // 16-byte chunks per source block row
+    constexpr int CPRR = B / 8;          // 16-byte chunks per rotation block row
+    const int g = lane >> 2, t = lane & 3;
 
     for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
         Tile tl;
@@ -116,25 +142,40 @@ __global__ void __launch_bounds__(128) k_rotate_mma(RotArgs a)
         const int bg = (int)(it % ngroups);
         const uint16_t *Re = (a.sel && (*a.sel & 1u)) ? a.R_alt : a.R;
         if (Re && a.stride) Re += (int64_t)tl.expert * a.stride;
-        for (int beta = bg * kRotBlocks; beta < min(nblk, (bg + 1) * kRotBlocks); ++beta) {
-            __syncthreads();
-            // stage the x tile (64 rows x B) and the rotation block (B x B)
-            for (int i = threadIdx.x; i < kRotRows * CPR; i += 128) {
+        const int b0 = bg * kRotBlocks, b1 = min(nblk, b0 + kRotBlocks);
+
+        // stage block beta (source tile and rotation block) into buffer buf
+        auto stage = [&](int beta, int buf) {
+            const uint32_t xs = sm0 + buf * S::kStage, rs = xs + S::kXBytes;
+            for (int i = threadIdx.x; i < kRotRows * CPR; i += kRotThreads) {
                 const int rr = i / CPR, c = i % CPR;
                 const bool live = rr < tl.nrows;
                 const int r = tl.row0 + (live ? rr : 0);
                 const int64_t srow = a.gather ? (int64_t)(a.perm[r] / a.k) : r;
-                cp_async16(xs_a + (rr * S::kPitch + c * 8) * 2,
-                           a.src + srow * a.src_ld + beta * B + c * 8, live);
+                const uint8_t *src = (const uint8_t *)a.src + (srow * a.src_ld + (int64_t)beta * B) * kEsz + c * 16;
+                cp_async16(xs + rr * S::kPitchX * kEsz + c * 16, src, live);
             }
             if (Re)
-                for (int i = threadIdx.x; i < B * CPR; i += 128) {
-                    const int rr = i / CPR, c = i % CPR;
-                    cp_async16(rs_a + (rr * S::kPitch + c * 8) * 2,
+                for (int i = threadIdx.x; i < B * CPRR; i += kRotThreads) {
+                    const int rr = i / CPRR, c = i % CPRR;
+                    cp_async16(rs + (rr * S::kPitchR + c * 8) * 2,
                                Re + (int64_t)beta * B * B + rr * B + c * 8, true);
                 }
-            cp_async_wait_all();
+            cp_async_commit();
+        };
+
+        stage(b0, 0);
+        for (int beta = b0; beta < b1; ++beta) {
+            const int buf = (beta - b0) & 1;
+            if (beta + 1 < b1) {
+                stage(beta + 1, buf ^ 1);
+                cp_async_wait<1>();
+            } else {
+                cp_async_wait<0>();
+            }
             __syncthreads();
+            const uint32_t xs_a = sm0 + buf * S::kStage, rs_a = xs_a + S::kXBytes;
+            const uint8_t *xs_p = rsm + buf * S::kStage;
 
             // warp w: rows 16w .. 16w+15, all B output columns
             float acc[B / 8][4];
@@ -143,153 +184,159 @@ __global__ void __launch_bounds__(128) k_rotate_mma(RotArgs a)
             if (Re) {
 #pragma unroll
                 for (int kk = 0; kk < B / 16; ++kk) {
-                    uint32_t a0, a1, a2, a3;
-                    {
+                    uint32_t a0, a1, a2, a3, l0 = 0, l1 = 0, l2 = 0, l3 = 0;
+                    if constexpr (F32IN) {
+                        const float *x0 = (const float *)xs_p + (16 * warp + g) * S::kPitchX + kk * 16 + 2 * t;
+                        const float *x1 = x0 + 8 * S::kPitchX;
+                        const float2 v00 = *(const float2 *)x0, v02 = *(const float2 *)(x0 + 8);
+                        const float2 v10 = *(const float2 *)x1, v12 = *(const float2 *)(x1 + 8);
+                        split2(v00.x, v00.y, a0, l0);
+                        split2(v10.x, v10.y, a1, l1);
+                        split2(v02.x, v02.y, a2, l2);
+                        split2(v12.x, v12.y, a3, l3);
+                    } else {
                         const int row = 16 * warp + (lane & 15);
                         const int col = kk * 16 + (lane >> 4) * 8;
-                        ldsm_x4(xs_a + (row * S::kPitch + col) * 2, a0, a1, a2, a3);
+                        ldsm_x4(xs_a + (row * S::kPitchX + col) * 2, a0, a1, a2, a3);
                     }
 #pragma unroll
                     for (int n = 0; n < B / 8; n += 2) {
-                        uint32_t b0, b1, b2, b3;
+                        uint32_t b0r, b1r, b2r, b3r;
                         if (!TRANS) {
                             // B(k, n) = R[k][n], row-major [k][n]: transposed 8x8 loads
                             const int krow = kk * 16 + (lane & 15);
                             const int ncol = n * 8 + (lane >> 4) * 8;
-                            ldsm_x4_t(rs_a + (krow * S::kPitch + ncol) * 2, b0, b1, b2, b3);
-                            mma16816(acc[n], a0, a1, a2, a3, b0, b1);
-                            mma16816(acc[n + 1], a0, a1, a2, a3, b2, b3);
+                            ldsm_x4_t(rs_a + (krow * S::kPitchR + ncol) * 2, b0r, b1r, b2r, b3r);
                         } else {
                             // B(k, n) = R[n][k]: row-major [n][k] is the col layout
                             const int nrow = n * 8 + (lane & 7) + ((lane >> 4) << 3);
                             const int kcol = kk * 16 + ((lane >> 3) & 1) * 8;
-                            ldsm_x4(rs_a + (nrow * S::kPitch + kcol) * 2, b0, b1, b2, b3);
-                            mma16816(acc[n], a0, a1, a2, a3, b0, b1);
-                            mma16816(acc[n + 1], a0, a1, a2, a3, b2, b3);
+                            ldsm_x4(rs_a + (nrow * S::kPitchR + kcol) * 2, b0r, b1r, b2r, b3r);
+                        }
+                        mma16816(acc[n], a0, a1, a2, a3, b0r, b1r);
+                        mma16816(acc[n + 1], a0, a1, a2, a3, b2r, b3r);
+                        if constexpr (F32IN) {
+                            mma16816(acc[n], l0, l1, l2, l3, b0r, b1r);
+                            mma16816(acc[n + 1], l0, l1, l2, l3, b2r, b3r);
                         }
                     }
                 }
             } else {
-                // identity: C = A
-                const int g = lane >> 2, t = lane & 3;
+                // identity: C = A.  An FP32 source passes as hi + lo, exactly
+                // what the two MMAs give with R = I (hi + lo is exact in
+                // FP32), so a unit rotation and no rotation agree bit for bit
 #pragma unroll
                 for (int n = 0; n < B / 8; ++n)
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int row = 16 * warp + g + 8 * h;
-                        const uint32_t v = *(const uint32_t *)(xs + row * S::kPitch + n * 8 + 2 * t);
-                        acc[n][2 * h] = bf2f(v & 0xFFFFu);
-                        acc[n][2 * h + 1] = bf2f(v >> 16);
-                    }
-            }
-            __syncthreads();   // x tile reads done: reuse it for the output tile
-            {
-                const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-                for (int n = 0; n < B / 8; ++n)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int rl = 16 * warp + g + 8 * h;
-                        const int col = n * 8 + 2 * t;
-                        float v0 = acc[n][2 * h], v1 = acc[n][2 * h + 1];
-                        uint32_t packed;
-                        if (EPI == ROT_SWIGLU_BWD) {
-                            packed = 0;
-                            if (rl < tl.nrows) {
-                                const int64_t r = tl.row0 + rl;
-                                const uint16_t *c = a.ctx + r * 3 * a.dim + beta * B + col;
-                                const uint32_t gg = *(const uint32_t *)c;
-                                const uint32_t uu = *(const uint32_t *)(c + a.dim);
-                                const float g0 = bf2f(gg & 0xFFFFu), g1 = bf2f(gg >> 16);
-                                const float u0 = bf2f(uu & 0xFFFFu), u1 = bf2f(uu >> 16);
-                                const float s0 = 1.f / (1.f + expf(-g0)), s1 = 1.f / (1.f + expf(-g1));
-                                // dg into the x tile, du into the rotation block region
-                                const uint32_t dg = pack_bf2(v0 * u0 * s0 * (1.f + g0 * (1.f - s0)),
-                                                             v1 * u1 * s1 * (1.f + g1 * (1.f - s1)));
-                                const uint32_t du = pack_bf2(v0 * g0 * s0, v1 * g1 * s1);
-                                *(uint32_t *)(rs + rl * S::kPitch + col) = du;
-                                packed = dg;
-                            }
+                        if constexpr (F32IN) {
+                            const float2 v = *(const float2 *)((const float *)xs_p + row * S::kPitchX + n * 8 + 2 * t);
+                            uint32_t hi, lo;
+                            split2(v.x, v.y, hi, lo);
+                            acc[n][2 * h] = bf2f(hi & 0xFFFFu) + bf2f(lo & 0xFFFFu);
+                            acc[n][2 * h + 1] = bf2f(hi >> 16) + bf2f(lo >> 16);
                         } else {
-                            packed = pack_bf2(v0, v1);
+                            const uint32_t v = *(const uint32_t *)((const uint16_t *)xs_p + row * S::kPitchX + n * 8 + 2 * t);
+                            acc[n][2 * h] = bf2f(v & 0xFFFFu);
+                            acc[n][2 * h + 1] = bf2f(v >> 16);
                         }
-                        *(uint32_t *)(xs + rl * S::kPitch + col) = packed;
                     }
             }
-            __syncthreads();
-            for (int i = threadIdx.x; i < kRotRows * CPR; i += 128) {
-                const int rr = i / CPR, c = i % CPR;
-                if (rr >= tl.nrows) continue;
-                const int64_t r = tl.row0 + rr;
-                const uint4 v = *(const uint4 *)(xs + rr * S::kPitch + c * 8);
-                *(uint4 *)(a.out + r * a.out_ld + beta * B + c * 8) = v;
-                if (EPI == ROT_SWIGLU_BWD) {
-                    const uint4 du = *(const uint4 *)(rs + rr * S::kPitch + c * 8);
-                    *(uint4 *)(a.out + r * a.out_ld + a.dim + beta * B + c * 8) = du;
+            // epilogue straight from the fragments: each quad of lanes writes
+            // 2 consecutive columns of one row
+#pragma unroll
+            for (int n = 0; n < B / 8; ++n)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int rl = 16 * warp + g + 8 * h;
+                    if (rl >= tl.nrows) continue;
+                    const int64_t r = tl.row0 + rl;
+                    const int col = beta * B + n * 8 + 2 * t;
+                    const float v0 = acc[n][2 * h], v1 = acc[n][2 * h + 1];
+                    if constexpr (EPI == ROT_SWIGLU_BWD) {
+                        const float *c = a.ctxf + r * 2 * a.dim + col;
+                        const float2 gg = *(const float2 *)c;
+                        const float2 uu = *(const float2 *)(c + a.dim);
+                        const float s0 = 1.f / (1.f + expf(-gg.x)), s1 = 1.f / (1.f + expf(-gg.y));
+                        const float dg0 = v0 * uu.x * s0 * (1.f + gg.x * (1.f - s0));
+                        const float dg1 = v1 * uu.y * s1 * (1.f + gg.y * (1.f - s1));
+                        const float du0 = v0 * (gg.x * s0), du1 = v1 * (gg.y * s1);
+                        __half2 *o = (__half2 *)((uint16_t *)a.out + r * a.out_ld + col);
+                        o[0] = __floats2half2_rn(dg0, dg1);
+                        o[a.dim / 2] = __floats2half2_rn(du0, du1);
+                    } else if constexpr (F32OUT) {
+                        *(float2 *)((float *)a.out + r * a.out_ld + col) = make_float2(v0, v1);
+                    } else {
+                        *(uint32_t *)((uint16_t *)a.out + r * a.out_ld + col) = pack_bf2(v0, v1);
+                    }
                 }
-            }
+            __syncthreads();   // buffer `buf` is restaged two blocks later
         }
     }
 }
 
-template <int B, bool TRANS, int EPI>
+template <int B, bool TRANS, int EPI, bool F32IN, bool F32OUT>
 static void rot_launch(const RotArgs &a, int max_tiles, cudaStream_t st)
 {
-    using S = RotSmem<B>;
-    const int ngroups = (a.dim / B + kRotBlocks - 1) / kRotBlocks;
-    int64_t items = (int64_t)max_tiles * ngroups;
-    int grid = (int)std::min<int64_t>(items, 152 * 8);
-    if (grid <= 0) return;
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_rotate_mma<B, TRANS, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             S::kBytes);
-        attr = true;
+    using S = RotSmem<B, F32IN>;
+    auto kern = k_rotate_mma<B, TRANS, EPI, F32IN, F32OUT>;
+    static int per_sm = 0;
+    if (!per_sm) {
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRotThreads, S::kBytes);
+        if (per_sm <= 0) per_sm = 1;
     }
-    k_rotate_mma<B, TRANS, EPI><<<grid, 128, S::kBytes, st>>>(a);
+    const int ngroups = (a.dim / B + kRotBlocks - 1) / kRotBlocks;
+    const int64_t items = (int64_t)max_tiles * ngroups;
+    const int grid = (int)std::min<int64_t>(items, (int64_t)gemm_num_sms() * per_sm);
+    if (grid <= 0) return;
+    kern<<<grid, kRotThreads, S::kBytes, st>>>(a);
     note_launch();
 }
 
-template <bool TRANS, int EPI>
+template <bool TRANS, int EPI, bool F32IN, bool F32OUT>
 static void rot_dispatch(int b, const RotArgs &a, int max_tiles, cudaStream_t st)
 {
     switch (b) {
-    case 16: rot_launch<16, TRANS, EPI>(a, max_tiles, st); break;
-    case 32: rot_launch<32, TRANS, EPI>(a, max_tiles, st); break;
-    case 64: rot_launch<64, TRANS, EPI>(a, max_tiles, st); break;
-    default: rot_launch<128, TRANS, EPI>(a, max_tiles, st); break;
+    case 16: rot_launch<16, TRANS, EPI, F32IN, F32OUT>(a, max_tiles, st); break;
+    case 32: rot_launch<32, TRANS, EPI, F32IN, F32OUT>(a, max_tiles, st); break;
+    case 64: rot_launch<64, TRANS, EPI, F32IN, F32OUT>(a, max_tiles, st); break;
+    default: rot_launch<128, TRANS, EPI, F32IN, F32OUT>(a, max_tiles, st); break;
     }
 }
 
-void launch_rotate_tc(int b, bool trans, bool swiglu_bwd, const uint16_t *src, int64_t src_ld,
-                      bool gather, const int32_t *perm, int k, const int32_t *idx_flat,
-                      const uint16_t *R, int64_t stride, int dim, uint16_t *out, int64_t out_ld,
-                      const Tile *tiles, const int32_t *tbeg, const int32_t *tend, int max_tiles,
-                      int nrows, const uint16_t *ctx, cudaStream_t st, const uint16_t *R_alt,
-                      const uint64_t *sel)
+void launch_rotate_tc(const RotCall &c, cudaStream_t st)
 {
-    RotArgs a{src, src_ld, gather ? 1 : 0, perm, k, idx_flat, R, stride, dim, out, out_ld, tiles,
-              tbeg, tend, nrows, ctx, R_alt, sel};
-    if (!tiles) max_tiles = (nrows + kRotRows - 1) / kRotRows;
-    if (swiglu_bwd) rot_dispatch<true, ROT_SWIGLU_BWD>(b, a, max_tiles, st);
-    else if (trans) rot_dispatch<true, ROT_STORE>(b, a, max_tiles, st);
-    else rot_dispatch<false, ROT_STORE>(b, a, max_tiles, st);
+    RotArgs a{c.src, c.src_ld, c.perm ? 1 : 0, c.perm, c.k, c.R, c.stride, c.dim, c.out, c.out_ld,
+              c.tiles, c.tbeg, c.tend, c.nrows, c.ctxf, c.R_alt, c.sel};
+    const int max_tiles = c.tiles ? c.max_tiles : (c.nrows + kRotRows - 1) / kRotRows;
+    if (c.swiglu_bwd) {
+        rot_dispatch<true, ROT_SWIGLU_BWD, true, false>(c.b, a, max_tiles, st);
+    } else if (c.trans) {
+        if (c.src_f32 && c.out_f32) rot_dispatch<true, ROT_STORE, true, true>(c.b, a, max_tiles, st);
+        else if (c.src_f32) rot_dispatch<true, ROT_STORE, true, false>(c.b, a, max_tiles, st);
+        else rot_dispatch<true, ROT_STORE, false, false>(c.b, a, max_tiles, st);
+    } else {
+        rot_dispatch<false, ROT_STORE, false, false>(c.b, a, max_tiles, st);
+    }
 }
 
 // ------------------------------------------------------------------ dR
 // dR[s][beta] = sum over the rows of set s (fixed order) of a_blk^T g_blk,
 // on mma.sync: A(m = i, k = row) = a[row][i] and B(k = row, n = j) =
-// g[row][j] both come from row-major [rows x b] tiles through transposed
-// 8x8 loads.  One CTA per (set, block); warp w owns output rows
-// i = 16w .. 16w+15 (b = 64: 4 warps; b = 128: 8 warps; b = 16, 32: one
-// warp per 16 rows, the rest idle).
+// g[row][j] both come from row-major [rows x b] BF16 tiles through
+// transposed 8x8 loads; an FP32 g is split into hi and lo tiles on the way
+// into shared memory, both multiplied.  One CTA per (set, block); warp w
+// owns output rows i = 16w .. 16w+15 (b = 64: 4 warps; b = 128: 8 warps;
+// b = 16, 32: one warp per 16 rows, the rest idle).
 struct OuterArgs {
     const uint16_t *a;         // rows of a (gathered: perm[r] / k)
     int64_t a_ld;
     int gather;
     const int32_t *perm;
     int k;
-    const uint16_t *g;         // rows of g, expert-sorted
+    const void *g;             // rows of g, expert-sorted, BF16 or FP32
     int64_t g_ld;
     const int32_t *offsets;    // rows of set s: offsets[s] .. offsets[s+1] (NULL: all rows)
     int nrows;
@@ -297,14 +344,25 @@ struct OuterArgs {
     float *dR;
 };
 
-template <int B>
+constexpr int kOuterRows = 64;   // rows per K stage
+template <int B, bool F32G>
+struct OuterSmem {
+    static constexpr int kPitch = B + 8;
+    static constexpr int kTile = kOuterRows * kPitch * 2;
+    static constexpr int kBytes = kTile * (F32G ? 3 : 2);   // a, g (hi), g lo
+};
+
+template <int B, bool F32G>
 __global__ void __launch_bounds__(256) k_outer_mma(OuterArgs p)
 {
-    constexpr int RB = 64;              // rows per K stage
-    constexpr int PITCH = B + 8;
-    __shared__ __align__(16) uint16_t as[RB * PITCH], gs[RB * PITCH];
+    using S = OuterSmem<B, F32G>;
+    constexpr int RB = kOuterRows;
+    constexpr int PITCH = S::kPitch;
+    extern __shared__ __align__(16) uint8_t osm[];
+    uint16_t *as = (uint16_t *)osm, *gs = as + RB * PITCH, *gl = gs + RB * PITCH;
     const uint32_t as_a = (uint32_t)__cvta_generic_to_shared(as);
     const uint32_t gs_a = (uint32_t)__cvta_generic_to_shared(gs);
+    const uint32_t gl_a = (uint32_t)__cvta_generic_to_shared(gl);
     const int nb = p.dim / B;
     const int s = blockIdx.x / nb, beta = blockIdx.x % nb;
     const int r0 = p.offsets ? p.offsets[s] : 0, r1 = p.offsets ? p.offsets[s + 1] : p.nrows;
@@ -323,8 +381,26 @@ __global__ void __launch_bounds__(256) k_outer_mma(OuterArgs p)
             const int r = rb + (live ? rr : 0);
             const int64_t arow = p.gather ? (int64_t)(p.perm[r] / p.k) : r;
             cp_async16(as_a + (rr * PITCH + c * 8) * 2, p.a + arow * p.a_ld + beta * B + c * 8, live);
-            cp_async16(gs_a + (rr * PITCH + c * 8) * 2, p.g + (int64_t)r * p.g_ld + beta * B + c * 8,
-                       live);
+            if constexpr (!F32G)
+                cp_async16(gs_a + (rr * PITCH + c * 8) * 2,
+                           (const uint16_t *)p.g + (int64_t)r * p.g_ld + beta * B + c * 8, live);
+        }
+        if constexpr (F32G) {
+            // 8 FP32 values per step -> 8 BF16 hi and 8 lo
+            for (int i = threadIdx.x; i < RB * CPR; i += 256) {
+                const int rr = i / CPR, c = i % CPR;
+                uint4 hv = make_uint4(0, 0, 0, 0), lv = hv;
+                if (rr < n_live) {
+                    const float *src = (const float *)p.g + (int64_t)(rb + rr) * p.g_ld + beta * B + c * 8;
+                    const float4 x0 = *(const float4 *)src, x1 = *(const float4 *)(src + 4);
+                    split2(x0.x, x0.y, hv.x, lv.x);
+                    split2(x0.z, x0.w, hv.y, lv.y);
+                    split2(x1.x, x1.y, hv.z, lv.z);
+                    split2(x1.z, x1.w, hv.w, lv.w);
+                }
+                *(uint4 *)(gs + rr * PITCH + c * 8) = hv;
+                *(uint4 *)(gl + rr * PITCH + c * 8) = lv;
+            }
         }
         cp_async_wait_all();
         __syncthreads();
@@ -346,6 +422,11 @@ __global__ void __launch_bounds__(256) k_outer_mma(OuterArgs p)
                     ldsm_x4_t(gs_a + (krow * PITCH + ncol) * 2, b0, b1, b2, b3);
                     mma16816(acc[n], a0, a1, a2, a3, b0, b1);
                     mma16816(acc[n + 1], a0, a1, a2, a3, b2, b3);
+                    if constexpr (F32G) {
+                        ldsm_x4_t(gl_a + (krow * PITCH + ncol) * 2, b0, b1, b2, b3);
+                        mma16816(acc[n], a0, a1, a2, a3, b0, b1);
+                        mma16816(acc[n + 1], a0, a1, a2, a3, b2, b3);
+                    }
                 }
             }
         }
@@ -363,19 +444,38 @@ __global__ void __launch_bounds__(256) k_outer_mma(OuterArgs p)
     }
 }
 
+template <int B, bool F32G>
+static void outer_launch(const OuterArgs &p, int grid, cudaStream_t st)
+{
+    using S = OuterSmem<B, F32G>;
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_outer_mma<B, F32G>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
+        attr = true;
+    }
+    k_outer_mma<B, F32G><<<grid, 256, S::kBytes, st>>>(p);
+}
+
+template <bool F32G>
+static void outer_dispatch(int b, const OuterArgs &p, int grid, cudaStream_t st)
+{
+    switch (b) {
+    case 16: outer_launch<16, F32G>(p, grid, st); break;
+    case 32: outer_launch<32, F32G>(p, grid, st); break;
+    case 64: outer_launch<64, F32G>(p, grid, st); break;
+    default: outer_launch<128, F32G>(p, grid, st); break;
+    }
+}
+
 void launch_outer_tc(int nsets, int nrows, int dim, int b, const uint16_t *a, int64_t a_ld,
-                     bool gather, const int32_t *perm, int k, const uint16_t *g, int64_t g_ld,
+                     bool gather, const int32_t *perm, int k, const void *g, bool g_f32, int64_t g_ld,
                      const int32_t *offsets, float *dR, cudaStream_t st)
 {
     OuterArgs p{a, a_ld, gather ? 1 : 0, perm, k, g, g_ld, offsets, nrows, dim, dR};
     int grid = nsets * (dim / b);
     if (grid <= 0) return;
-    switch (b) {
-    case 16: k_outer_mma<16><<<grid, 256, 0, st>>>(p); break;
-    case 32: k_outer_mma<32><<<grid, 256, 0, st>>>(p); break;
-    case 64: k_outer_mma<64><<<grid, 256, 0, st>>>(p); break;
-    default: k_outer_mma<128><<<grid, 256, 0, st>>>(p); break;
-    }
+    if (g_f32) outer_dispatch<true>(b, p, grid, st);
+    else outer_dispatch<false>(b, p, grid, st);
     note_launch();
 }
 

@@ -1,5 +1,5 @@
 // route_permute.cu -- router top-k and the grouping of (token, slot) pairs
-// by expert ("Active-expert-chunked dequantization", page 1, 技艺细节: the
+// by expert (Orbit announcement, 技艺细节, active-expert-chunked dequantization: the
 // router's selected experts are gathered into fixed-size batches).
 #include <algorithm>
 
@@ -7,6 +7,65 @@
 #include "launch.h"
 
 namespace pmoe {
+
+// ------------------------------------------------------------------ exact logits
+// The canonical router mode: FP32 logits on the CUDA cores in one fixed
+// summation order, independent of the batch and of the launch shape.  For
+// token t and expert e, lane i of the token's warp forms the partial
+// fmaf chain over the columns c = i, i + 32, ... in ascending order; the 32
+// partials are then added by the tree s[i] += s[i + h], h = 16, 8, 4, 2, 1
+// (shuffles down).  A CTA takes 8 tokens (one warp each) and 32 experts,
+// staging 64 rows of those experts' router weights at a time in shared
+// memory (row pitch 33: lanes reading different rows hit different banks).
+constexpr int kRxTok = 8, kRxE = 32, kRxRows = 64;
+
+__global__ void __launch_bounds__(kRxTok * 32) k_router_exact(int T, int d, int E,
+                                                               const uint16_t *__restrict__ X,
+                                                               const float *__restrict__ Wr,
+                                                               float *__restrict__ logits)
+{
+    __shared__ float ws[kRxRows][kRxE + 1];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kRxTok + warp, e0 = blockIdx.y * kRxE;
+    float acc[kRxE];
+#pragma unroll
+    for (int e = 0; e < kRxE; ++e) acc[e] = 0.f;
+    for (int c0 = 0; c0 < d; c0 += kRxRows) {
+        __syncthreads();
+        for (int i = threadIdx.x; i < kRxRows * kRxE; i += kRxTok * 32) {
+            const int r = i / kRxE, e = i % kRxE;
+            ws[r][e] = e0 + e < E ? Wr[(int64_t)(c0 + r) * E + e0 + e] : 0.f;
+        }
+        __syncthreads();
+        if (t < T) {
+#pragma unroll
+            for (int q = 0; q < kRxRows / 32; ++q) {
+                const int r = lane + 32 * q;   // column c0 + r: c = lane (mod 32), ascending
+                const float x = bf2f(X[(int64_t)t * d + c0 + r]);
+#pragma unroll
+                for (int e = 0; e < kRxE; ++e) acc[e] = fmaf(x, ws[r][e], acc[e]);
+            }
+        }
+    }
+#pragma unroll
+    for (int h = 16; h >= 1; h >>= 1)
+#pragma unroll
+        for (int e = 0; e < kRxE; ++e) acc[e] += __shfl_down_sync(0xffffffffu, acc[e], h);
+    if (t < T && lane == 0) {
+#pragma unroll
+        for (int e = 0; e < kRxE; ++e)
+            if (e0 + e < E) logits[(int64_t)t * E + e0 + e] = acc[e];
+    }
+}
+
+void launch_router_exact(int T, int d, int E, const uint16_t *X, const float *Wr, float *logits,
+                         cudaStream_t st)
+{
+    if (T <= 0) return;
+    dim3 grid((unsigned)cdiv(T, kRxTok), (unsigned)cdiv(E, kRxE));
+    k_router_exact<<<grid, kRxTok * 32, 0, st>>>(T, d, E, X, Wr, logits);
+    note_launch();
+}
 
 // ------------------------------------------------------------------ top-k
 // One warp per token.  Selection j picks the best element strictly after

@@ -7,7 +7,7 @@ Everything is generated on the host with numpy's PCG64 from an explicit
 seed, so x86 and Arm hosts produce identical bytes.
 
 Value recipes (the pages give the shapes of the workloads, not the values;
-see the design notes for the readings):
+these are the plainest distributions the shapes allow):
   X            ~ N(0, 1) rounded to BF16
   dY           ~ N(0, 0.1^2) rounded to BF16   (variance 1e-2)
   Wr           ~ N(0, 0.02^2), FP32 [d, E]

@@ -108,12 +108,18 @@ class DeviceLayer:
                        active=torch.zeros(cfg.E, **i32), num_active=torch.zeros(1, **i32))
 
     # -------------------------------------------------------------- steps
-    def route(self, X: torch.Tensor, rt: Routing, logits: torch.Tensor | None = None):
+    def route(self, X: torch.Tensor, rt: Routing, logits: torch.Tensor | None = None,
+              mode: int = pmoe.ROUTE_FAST):
         ws = self.workspace(pmoe.OP_PERMUTE)
-        pmoe.moe_route(self.dims, X, self.Wr, self.bias, logits, rt.idx, rt.w, ws)
+        pmoe.moe_route(self.dims, X, self.Wr, self.bias, logits, rt.idx, rt.w, ws, mode=mode)
 
     def permute(self, rt: Routing):
         pmoe.moe_permute(self.dims, rt.idx, rt.c(), self.workspace(pmoe.OP_PERMUTE))
+
+    def new_ctx(self) -> torch.Tensor:
+        """The forward's saved context for the backward (moe_ctx_bytes)."""
+        return torch.empty(max(pmoe.moe_ctx_bytes(self.dims), 16), dtype=torch.uint8,
+                           device=self.device)
 
     def forward(self, X, rt: Routing, Y, C=None, mode=pmoe.MODE_FUSED, ctx=None):
         C = C or self.cfg.C

@@ -19,16 +19,17 @@ PMOE_OK, PMOE_ERR_INVALID_ARG, PMOE_ERR_UNSUPPORTED, PMOE_ERR_WORKSPACE = 0, 1, 
 PMOE_ERR_CUDA, PMOE_ERR_BAD_INDEX, PMOE_ERR_TIMEOUT = 4, 5, 6
 W_INT4_G32_BF16, W_MXFP4_G32_E8M0, W_FP8_B128_F32 = 0, 1, 2
 MODE_FUSED, MODE_SCRATCH = 0, 1
-ROUTE_FAST = 0
+ROUTE_FAST, ROUTE_EXACT = 0, 1
 OP_PERMUTE, OP_FORWARD, OP_BACKWARD = 0, 1, 2
 
 EXPORTS = ("moe_route", "moe_permute", "moe_chunked_forward", "moe_backward_data", "moe_dequant",
            "adapter_apply", "adapter_grad", "adapter_cayley", "adapter_cayley_grad",
-           "moe_workspace_bytes", "moe_scratch_bytes", "moe_clear_status", "moe_query_status",
+           "moe_workspace_bytes", "moe_scratch_bytes", "moe_ctx_bytes", "moe_clear_status",
+           "moe_query_status",
            "pmoe_status_string", "pmoe_launch_count", "pmoe_kernel_timing", "pmoe_kernel_time",
            "moe_grouped_gemm", "moe_grouped_gemm_ws_bytes", "moe_permute_noalloc",
            "dense_linear_ws_bytes", "dense_linear_forward", "dense_linear_backward",
-           "moe_adapter_publish", "moe_chunked_forward_slots")
+           "moe_adapter_publish", "moe_chunked_forward_slots", "pmoe_debug_expire_gemm_wait")
 PERMUTE_NOALLOC_SCRATCH_BYTES = 1 << 20
 KT_GEMM_GATE_UP, KT_GEMM_DOWN, KT_GEMM_BWD_G, KT_GEMM_BWD_DX, KT_ROUTER = 0, 1, 2, 3, 4
 
@@ -119,6 +120,10 @@ def _declare(L):
     L.dense_linear_ws_bytes.restype = sz
     L.moe_scratch_bytes.argtypes = [D, i32, ctypes.c_int]
     L.moe_scratch_bytes.restype = sz
+    L.moe_ctx_bytes.argtypes = [D]
+    L.moe_ctx_bytes.restype = sz
+    L.pmoe_debug_expire_gemm_wait.argtypes = [ctypes.c_uint64]
+    L.pmoe_debug_expire_gemm_wait.restype = st
     L.pmoe_status_string.argtypes = [st]
     L.pmoe_status_string.restype = ctypes.c_char_p
     L.pmoe_launch_count.argtypes = []
@@ -184,6 +189,14 @@ def moe_workspace_bytes(dm: Dims, op: int, chunk_C: int = 1, mode: int = MODE_FU
 
 def moe_scratch_bytes(dm: Dims, chunk_C: int, mode: int) -> int:
     return lib().moe_scratch_bytes(dm, chunk_C, mode)
+
+
+def moe_ctx_bytes(dm: Dims) -> int:
+    return lib().moe_ctx_bytes(dm)
+
+
+def pmoe_debug_expire_gemm_wait(wait_ns: int):
+    _check(lib().pmoe_debug_expire_gemm_wait(wait_ns), "pmoe_debug_expire_gemm_wait")
 
 
 def moe_route(dm, X, Wr, bias, logits, idx, w, ws, mode=ROUTE_FAST, stream=None):

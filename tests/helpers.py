@@ -39,33 +39,62 @@ def assert_close(got, ref, what="", rel_fro=REL_FRO, max_abs=MAX_ABS):
     return rel
 
 
+def check_cayley(Rb_bits, Rf, R64, b):
+    """Device Cayley map against the FP64 one: R_f32 within 4 b 2^-24 (FP32
+    elimination on b x b blocks of norm about 1), and R_bf16 = bf16(R_f32):
+    rounding is monotone, so it lies between the roundings of R - eps and
+    R + eps, and equals bf16 of the exact R wherever those two agree.
+    Returns the number of elements where they do not (where the FP32 error
+    bound alone cannot fix the BF16 value)."""
+    eps = 4 * b * 2.0 ** -24
+    rf = np.asarray(Rf, np.float64)
+    assert np.max(np.abs(rf - R64)) < eps
+    rb = bits_to_f64(Rb_bits)
+    lo = bits_to_f64(oracle.bf16_round((R64 - eps).ravel())).reshape(R64.shape)
+    hi = bits_to_f64(oracle.bf16_round((R64 + eps).ravel())).reshape(R64.shape)
+    assert np.all((rb >= lo) & (rb <= hi))
+    ref = bits_to_f64(oracle.bf16_round(R64.ravel())).reshape(R64.shape)
+    assert np.all((rb == ref) | (lo != hi))
+    return int(np.sum(lo != hi))
+
+
+def check_topk(g_logits, g_idx, g_w, k, toks=None):
+    """The device's selection and weights against the oracle's top-k and
+    softmax applied to the device's own logits (bias included): idx bit for
+    bit, w within 1e-6 relative."""
+    o_idx, o_w = oracle.topk(g_logits, k, toks=toks)
+    rows = slice(None) if toks is None else np.asarray(toks)
+    assert np.array_equal(g_idx[rows], o_idx[rows])
+    assert np.all(np.abs(g_w[rows].astype(np.float64) - o_w[rows]) <= 1e-6 * np.abs(o_w[rows]))
+
+
 def check_routing(X, Wr, bias, k, g_logits, g_idx, g_w, toks=None):
-    """Logits within the FP32 bound; selections valid everywhere and equal
-    to the oracle's wherever the oracle's decision is certified unique.
-    Returns the tokens whose routing equals the oracle's exactly."""
+    """Device routing from the fast router mode:
+      - logits within the FP32 bound 1e-5 (1 + sum |x w|) of the oracle's
+        FP64 logits;
+      - idx bit-exact and w within 1e-6 relative against the oracle's top-k
+        and softmax applied to the device's own logits;
+      - against the oracle's own routing, a token may differ only where the
+        oracle's order near the k-th place is not certified (two logits
+        within twice the bound).
+    Returns the tokens whose routing equals the oracle's own exactly."""
     o_logits, o_idx, o_w = oracle.route(X, Wr, bias, k, toks=toks)
     T = X.shape[0]
     toks = np.arange(T) if toks is None else np.asarray(toks)
+    check_topk(g_logits, g_idx, g_w, k, toks=toks)
     x = bits_to_f64(X[toks])
     beta = 1e-5 * (1.0 + np.abs(x) @ np.abs(Wr.astype(np.float64)))       # [n, E]
     ol, gl = o_logits[toks].astype(np.float64), g_logits[toks].astype(np.float64)
     assert np.all(np.abs(gl - ol) <= beta), np.max(np.abs(gl - ol) / beta)
     exact = []
     for n, t in enumerate(toks):
-        b2 = 2 * beta[n].max()
-        sel = g_idx[t]
-        assert len(set(sel.tolist())) == k
-        rest = np.setdiff1d(np.arange(Wr.shape[1]), sel)
-        if len(rest):
-            assert ol[n][sel].min() >= ol[n][rest].max() - b2
-        assert np.all(np.diff(ol[n][sel]) <= b2)
-        order = np.lexsort((np.arange(Wr.shape[1]), -ol[n]))
-        srt = ol[n][order]
-        gaps = -np.diff(srt[:min(k + 1, len(srt))])
-        if np.all(gaps > b2):
-            assert np.array_equal(sel, o_idx[t]), t
-        if np.array_equal(sel, o_idx[t]):
+        if np.array_equal(g_idx[t], o_idx[t]):
             exact.append(t)
-            wb = 4 * b2 * g_w[t] + 2e-6
-            assert np.all(np.abs(g_w[t] - o_w[t]) <= wb)
+            continue
+        # a flip: the oracle's own order must have a near-tie within the
+        # first k + 1 places
+        b2 = 2 * beta[n].max()
+        order = np.lexsort((np.arange(Wr.shape[1]), -ol[n]))
+        gaps = -np.diff(ol[n][order][:min(k + 1, len(order))])
+        assert np.any(gaps <= b2), (t, gaps.min(), b2)
     return np.array(exact)

@@ -77,3 +77,26 @@ def test_step_bytes_count_only_active_experts():
     packed = 3 * d * I // 2 + 3 * d * (I // 32) * 2       # INT4 codes + BF16 scales
     adapters = (d + I) * cfg.b * 2
     assert per_expert == 2 * (packed + adapters)         # read once in each pass
+
+
+def test_peak_choice_burst_or_sustained():
+    """Burst BF16 peak for a timed region at the maximum SM clock without a
+    power cap; sustained otherwise (capped, or clocks well below maximum)."""
+    pk = dict(hbm=6788.3, bf16=1893.4, bf16_sus=1702.3, src="measured")
+    full = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 9}
+    assert bench.pick_peak(pk, full)[0] == 1893.4
+    assert bench.pick_peak(pk, dict(full, reasons=["sw_power_cap"]))[0] == 1702.3
+    assert bench.pick_peak(pk, dict(full, sm_mhz=1500.0))[0] == 1702.3
+    assert bench.pick_peak(pk, {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]})[0] == 1702.3
+
+
+def test_traffic_follows_the_gemm_sources(monkeypatch):
+    """The captured DRAM traffic is reported only while the GEMM sources
+    are the ones it was captured with."""
+    monkeypatch.setattr(bench, "TRAFFIC", {"digest": bench.gemm_digest(),
+                                           "bytes": {("kimi_k2", "fused", "gemm_gate_up"): 1e9}})
+    assert bench.traffic_of("kimi_k2", "fused", "gemm_gate_up", True) == 1e9
+    assert bench.traffic_of("kimi_k2", "fused", "gemm_gate_up", False) is None
+    monkeypatch.setattr(bench, "TRAFFIC", {"digest": "0" * 16,
+                                           "bytes": {("kimi_k2", "fused", "gemm_gate_up"): 1e9}})
+    assert bench.traffic_of("kimi_k2", "fused", "gemm_gate_up", True) is None

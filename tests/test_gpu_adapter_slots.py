@@ -30,6 +30,8 @@ def setup():
         Su = gi.gen_skew(cfg.E, cfg.d, cfg.b, seed, "S_up", 0.05)
         Sd = gi.gen_skew(cfg.E, cfg.I, cfg.b, seed, "S_down", 0.05)
         ad.append((rb(Su), rb(Sd)))
+    host = dict(w13=w13, s13=s13, w2=w2, s2=s2, idx=idx, w=w, X=gi.gen_x(cfg),
+                R=[tuple(t.cpu().numpy().view(np.uint16) for t in pair) for pair in ad])
     L = DeviceLayer(cfg, w13, s13, w2, s2)
     rt = L.new_routing()
     rt.idx.copy_(torch.from_numpy(idx))
@@ -47,18 +49,36 @@ def setup():
     slots = pmoe.adapter_slots(ad[0][0], ad[1][0], ad[0][1], ad[1][1], ad[0][0][0].numel(),
                                ad[0][1][0].numel(), ctrl)
     # the slot struct holds raw device pointers: keep their tensors alive
-    return cfg, L, rt, X, refs, ctrl, slots, ad
+    return cfg, L, rt, X, refs, ctrl, slots, ad, host
 
 
 def fwd(setup, Y, ver, stream=None):
-    cfg, L, rt, X, refs, ctrl, slots, _ = setup
+    cfg, L, rt, X, refs, ctrl, slots, _, _ = setup
     ws = L.workspace(pmoe.OP_FORWARD, cfg.C)
     pmoe.moe_chunked_forward_slots(L.dims, L.wts, slots, rt.c(), X, cfg.C, pmoe.MODE_FUSED, Y,
                                    None, ver, ws, stream)
 
 
+def test_each_slot_against_the_oracle(setup):
+    """Each slot's forward against the oracle's layer with that slot's
+    rotations, under the stated tolerance."""
+    from helpers import assert_close, bits_to_f64
+    cfg, L, rt, X, refs, ctrl, slots, _, h = setup
+    for version in (8, 9):
+        slot = version % 2
+        pmoe.moe_adapter_publish(ctrl, slot, version)
+        Y = torch.empty_like(X)
+        fwd(setup, Y, None)
+        torch.cuda.synchronize()
+        Ru, Rd = h["R"][slot]
+        OL = oracle.Layer(cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.b, cfg.fmt, h["w13"], h["s13"],
+                          h["w2"], h["s2"], R_up=Ru, R_down=Rd)
+        _, Y64 = OL.forward(h["X"], h["idx"], h["w"])
+        assert_close(bits_to_f64(Y.cpu().numpy().view(np.uint16)), Y64, f"slot {slot} Y")
+
+
 def test_each_slot_is_the_single_adapter_forward(setup):
-    cfg, L, rt, X, refs, ctrl, slots, _ = setup
+    cfg, L, rt, X, refs, ctrl, slots, _, _ = setup
     for version in (4, 5, 6):
         slot = version % 2
         pmoe.moe_adapter_publish(ctrl, slot, version)
@@ -76,7 +96,7 @@ def test_publishes_during_forwards_never_mix_versions(setup):
     another; each forward's output is the reference of the version it
     reports.  The time from a publish to the first forward that starts
     after it and uses it is the switch latency."""
-    cfg, L, rt, X, refs, ctrl, slots, _ = setup
+    cfg, L, rt, X, refs, ctrl, slots, _, _ = setup
     n = 48
     Ys = [torch.empty_like(X) for _ in range(n)]
     vers = torch.zeros(n, dtype=torch.int32, device="cuda")

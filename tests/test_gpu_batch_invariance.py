@@ -3,7 +3,7 @@ other tokens of the batch.
 
 The pages' point is train/rollout consistency: the same token must get the
 same numbers whether it is scored in a large training batch or generated in
-a small decode batch (page 3, token-mult-prob-error).  Every step of the
+a small decode batch (NeMo RL FP8 article: token-mult-prob-error).  Every step of the
 path here is per token or per (token, slot) pair with a fixed summation
 order -- the router logits, top-k, the rotations, each output element of the
 grouped GEMMs (the K order of a tile does not depend on how many tokens the

@@ -12,7 +12,7 @@ import oracle
 from precision_moe_adapter_gb300 import build, pmoe
 from precision_moe_adapter_gb300 import inputs as gi
 from precision_moe_adapter_gb300.layer import DeviceLayer
-from helpers import assert_close, bits_to_f64, t2np_bits
+from helpers import assert_close, bits_to_f64, check_cayley, t2np_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -57,7 +57,7 @@ def run_gpu(c, C=None, mode=pmoe.MODE_FUSED, backward=True, R_up="case", R_down=
     L.permute(rt)
     X = dev(c["X"])
     Y = torch.empty((cfg.T, cfg.d), dtype=torch.int16, device="cuda")
-    ctx = torch.empty((max(cfg.P, 1), 3 * cfg.I), dtype=torch.int16, device="cuda")
+    ctx = L.new_ctx()
     L.forward(X, rt, Y, C=C, mode=mode, ctx=ctx)
     out = dict(Y=t2np_bits(Y))
     if backward:
@@ -162,7 +162,7 @@ def test_runs_are_deterministic_and_base_is_untouched():
     rt.w.copy_(torch.from_numpy(c["w"]))
     L.permute(rt)
     Y = torch.empty((c["cfg"].T, c["cfg"].d), dtype=torch.int16, device="cuda")
-    ctx = torch.empty((c["cfg"].P, 3 * c["cfg"].I), dtype=torch.int16, device="cuda")
+    ctx = L.new_ctx()
     L.forward(X, rt, Y, ctx=ctx)
     dX = torch.empty_like(Y)
     L.backward(X, dev(c["dY"]), ctx, rt, dX, None, *L.grads())
@@ -172,39 +172,46 @@ def test_runs_are_deterministic_and_base_is_untouched():
 
 
 def test_tiny_end_to_end_from_the_router():
-    """The tiny configuration from X: device router -> grouping -> forward
-    -> backward, against the oracle with its own routing."""
+    """The tiny configuration from X: device router (exact mode) -> grouping
+    -> forward -> backward, against the oracle with its canonical-order
+    routing, which the device reproduces bit for bit."""
     cfg = gi.CONFIGS["tiny"]
     X, dY = gi.gen_x(cfg), gi.gen_dy(cfg)
     w13, s13, w2, s2 = gi.gen_weights(cfg)
     Wr, bias = gi.gen_router(cfg)
     Su, Sd = gi.gen_adapter_params(cfg)
-    L = DeviceLayer(cfg, w13, s13, w2, s2, Wr=Wr, bias=bias, S_up=Su, S_down=Sd)
+    # the device Cayley map of S, checked on its own; the layer then takes
+    # the oracle's BF16 rotations, so both sides multiply by the same R
+    Ld = DeviceLayer(cfg, w13, s13, w2, s2, S_up=Su, S_down=Sd)
+    torch.cuda.synchronize()
+    for S, Rb_, Rf_ in ((Su, Ld.R_up, Ld.Rf_up), (Sd, Ld.R_down, Ld.Rf_down)):
+        check_cayley(t2np_bits(Rb_).reshape(-1, cfg.b, cfg.b), Rf_.cpu().numpy().reshape(-1, cfg.b, cfg.b),
+                     oracle.cayley(S.reshape(-1, cfg.b, cfg.b)), cfg.b)
+    Ru, Rd = rbits(Su), rbits(Sd)
+    L = DeviceLayer(cfg, w13, s13, w2, s2, Wr=Wr, bias=bias, R_up=Ru, R_down=Rd)
     rt = L.new_routing()
     Xd = dev(X)
     logits = torch.zeros((cfg.T, cfg.E), dtype=torch.float32, device="cuda")
-    L.route(Xd, rt, logits)
+    L.route(Xd, rt, logits, mode=pmoe.ROUTE_EXACT)
     L.permute(rt)
     Y = torch.empty((cfg.T, cfg.d), dtype=torch.int16, device="cuda")
-    ctx = torch.empty((cfg.P, 3 * cfg.I), dtype=torch.int16, device="cuda")
+    ctx = L.new_ctx()
     L.forward(Xd, rt, Y, ctx=ctx)
     dX = torch.empty_like(Y)
     L.backward(Xd, dev(dY), ctx, rt, dX, None, *L.grads())
     torch.cuda.synchronize()
     assert L.status() == pmoe.PMOE_OK
-    from helpers import check_routing
-    exact = check_routing(X, Wr, bias, cfg.k, logits.cpu().numpy(), rt.idx.cpu().numpy(),
-                          rt.w.cpu().numpy())
-    assert len(exact) >= cfg.T - 2
-    o_logits, o_idx, o_w = oracle.route(X, Wr, bias, cfg.k)
-    Ru, Rd = rbits(Su), rbits(Sd)
+    # the exact router mode: logits, selection and weights equal the oracle's
+    # canonical-order routing for every token
+    o_logits = oracle.route_canonical(X, Wr, bias)
+    o_idx, o_w = oracle.topk(o_logits, cfg.k)
+    assert np.array_equal(logits.cpu().numpy().view(np.uint32), o_logits.view(np.uint32))
+    assert np.array_equal(rt.idx.cpu().numpy(), o_idx)
+    assert np.all(np.abs(rt.w.cpu().numpy().astype(np.float64) - o_w) <= 1e-6 * o_w)
+    exact = np.arange(cfg.T)
     OL = oracle.Layer(cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.b, cfg.fmt, w13, s13, w2, s2,
                       R_up=Ru, R_down=Rd)
     _, Y64 = OL.forward(X, o_idx, o_w)
     ob = OL.backward(X, dY, o_idx, o_w)
-    # the device rotations come from the device Cayley map (FP32): compare
-    # them first, then the outputs on the tokens routed identically
-    gRu = t2np_bits(L.R_up)
-    assert np.mean(gRu == Ru) > 0.99
     assert_close(bits_to_f64(t2np_bits(Y))[exact], Y64[exact], "tiny Y")
     assert_close(bits_to_f64(t2np_bits(dX))[exact], ob["dX64"][exact], "tiny dX")

@@ -46,6 +46,54 @@ def test_route_full_softmax_and_ties():
         assert np.allclose(w[t], want, rtol=1e-6, atol=1e-9)
 
 
+def test_topk_against_lexsort_and_softmax():
+    """or_topk on given logits: the order of numpy's lexsort by (logit
+    descending, id ascending), weights equal to scipy's softmax over the k
+    selected (rounded to FP32); planted ties go to the lower id."""
+    rng = np.random.default_rng(3)
+    T, E, k = 200, 37, 7
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    logits[:, 20] = logits[:, 3]             # ties between experts 3 and 20
+    logits[::3, 11] = logits[::3].max(axis=1)  # ties for the first slot
+    idx, w = oracle.topk(logits, k)
+    for t in range(T):
+        order = np.lexsort((np.arange(E), -logits[t].astype(np.float64)))[:k]
+        assert list(idx[t]) == list(order)
+        want = scipy.special.softmax(logits[t][order].astype(np.float64)).astype(np.float32)
+        assert np.allclose(w[t], want, rtol=2.5e-7, atol=0)
+
+
+def test_route_canonical_order():
+    """The canonical-order logits: (a) within the FP32 summation bound of
+    the exact logits; (b) d = 32: each partial is one rounded product, and
+    the tree s[i] += s[i + h] (h = 16 .. 1) reproduced with numpy float32
+    additions gives the same bits; (c) with inputs whose products and
+    partial sums are exact in FP32 the result is the exact dot product
+    (no term dropped or counted twice)."""
+    cfg = gi.LayerConfig("r", T=24, d=256, E=12, k=2, I=32, b=16, router="zipf")
+    X = gi.gen_x(cfg)
+    Wr, bias = gi.gen_router(cfg)
+    lc = oracle.route_canonical(X, Wr, bias)
+    x, W = bf(X), Wr.astype(np.float64)
+    exact = x @ W + bias.astype(np.float64)
+    bound = (cfg.d / 32 + 6) * 2.0 ** -24 * (np.abs(x) @ np.abs(W) + np.abs(bias))
+    assert np.all(np.abs(lc - exact) <= bound)
+    # (b) d = 32
+    X32, W32 = X[:, :32], np.ascontiguousarray(Wr[:32])
+    l32 = oracle.route_canonical(X32, W32, None)
+    prod = (bf(X32)[:, :, None] * W32.astype(np.float64)[None]).astype(np.float32)   # [T, 32, E]
+    s = prod.copy()
+    for h in (16, 8, 4, 2, 1):
+        s[:, :h] = (s[:, :h] + s[:, h:2 * h]).astype(np.float32)
+    assert np.array_equal(l32, s[:, 0])
+    # (c) small integers times eighths: every step exact in FP32
+    rng = np.random.default_rng(4)
+    Xi = gi.f32_to_bf16_bits(rng.integers(-8, 9, size=(9, 160)).astype(np.float32))
+    Wi = (rng.integers(-8, 9, size=(160, 5)) / 8.0).astype(np.float32)
+    li = oracle.route_canonical(Xi, Wi, None)
+    assert np.array_equal(li.astype(np.float64), bf(Xi) @ Wi.astype(np.float64))
+
+
 # ---------------------------------------------------------------- permute
 
 @pytest.mark.parametrize("T,E,k", [(50, 8, 2), (1, 16, 8), (0, 4, 2), (37, 64, 6)])

@@ -55,7 +55,9 @@ def test_oversized_problem_is_rejected_before_device_work():
 def test_two_calls_in_a_row_match_moe_permute():
     build.build()
     pmoe.lib()
-    cases = [(8192, 384, 8, 1.1, 3), (777, 4096, 32, 1.1, 4)]
+    # the last case fills the buffer exactly: 64 blocks of 1024 pairs x 4096
+    # experts x 4 bytes = 1 MiB
+    cases = [(8192, 384, 8, 1.1, 3), (777, 4096, 32, 1.1, 4), (2048, 4096, 32, 0.5, 5)]
     results = []
     for T, E, k, skew, seed in cases:
         cfg = gi.LayerConfig("p", T=T, d=64, E=E, k=k, I=64, b=16, seed=seed)
