@@ -47,6 +47,9 @@ def parse():
                     help="comma-separated chunk sizes (0: all active experts): after the main "
                          "line, one line per C with the step time in --mode and its dequant "
                          "scratch bytes")
+    ap.add_argument("--decode", action="store_true",
+                    help="decode sweep on the Kimi-K2 shape (forward only): one line per "
+                         "(T, weight format, C) with the achieved HBM bandwidth")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -270,6 +273,89 @@ def workload(cfg, args):
 
 # ---------------------------------------------------------------- GPU side
 
+def decode_bytes(cfg, counts):
+    """Algorithmic HBM bytes of one decode forward: the packed weights,
+    scales and adapter blocks of the active experts (each read once), the
+    router weights, X and Y."""
+    d, I, b = cfg.d, cfg.I, cfg.b
+    na = int((counts > 0).sum())
+    if cfg.fmt == gi.FP8:
+        wq = 3 * d * I + 3 * (d // 128) * (I // 128) * 4
+    else:
+        wq = 3 * d * I // 2 + 3 * d * (I // 32) * (2 if cfg.fmt == gi.INT4 else 1)
+    adp = (d + I) * b * 2
+    return na * (wq + adp) + d * cfg.E * 4 + 2 * cfg.T * d * 2
+
+
+def run_decode(args):
+    """Decode-sized forward on the Kimi-K2 shape, T in {1, 8, 64, 512}, INT4
+    and FP8 weights, C in {8, 32, all active}: latency of router + grouping
+    + forward (CUDA events, a 256 MB L2-flush write between iterations) and
+    the achieved bandwidth against the measured HBM copy rate."""
+    import torch
+    from precision_moe_adapter_gb300 import build as pbuild
+    from precision_moe_adapter_gb300 import pmoe
+    from precision_moe_adapter_gb300.layer import DeviceLayer
+    pbuild.build()
+    pmoe.lib()
+    pk = peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for fmt in (gi.INT4, gi.FP8):
+        base = gi.decode_config(1, fmt)
+        if fmt == gi.FP8:
+            w13, s13 = gi.gen_fp8_matrix_on_device(base.E, 2 * base.I, base.d, base.seed, "w13", "s13",
+                                                   "cuda")
+            w2, s2 = gi.gen_fp8_matrix_on_device(base.E, base.d, base.I, base.seed, "w2", "s2", "cuda")
+        else:
+            w13, s13, w2, s2 = gi.gen_weights(base)
+        Su, Sd = gi.gen_adapter_params(base)
+        for T in (1, 8, 64, 512):
+            cfg = gi.decode_config(T, fmt)
+            Wr, bias = gi.gen_router(cfg)
+            L = DeviceLayer(cfg, w13, s13, w2, s2, Wr=Wr, bias=bias, S_up=Su, S_down=Sd)
+            X = torch.from_numpy(gi.gen_x(cfg)).view(torch.int16).cuda()
+            Y = torch.empty_like(X)
+            rt = L.new_routing()
+            L.route(X, rt)
+            L.permute(rt)
+            torch.cuda.synchronize()
+            counts = rt.counts.cpu().numpy()
+            na = int((counts > 0).sum())
+            B = decode_bytes(cfg, counts)
+            for C in (8, 32, na):
+                def once():
+                    L.route(X, rt)
+                    L.permute(rt)
+                    L.forward(X, rt, Y, C=C)
+                for _ in range(max(args.warmup, 3)):
+                    once()
+                times = []
+                for _ in range(args.steps):
+                    flush.zero_()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    once()
+                    e1.record()
+                    torch.cuda.synchronize()
+                    times.append(e0.elapsed_time(e1))
+                ms = statistics.median(times)
+                gbs = B / (ms / 1e3) / 1e9
+                print(json.dumps({
+                    "metric": "decode forward latency and HBM bandwidth (router + grouping + forward)",
+                    "workload": cfg.name, "T": T, "weights": gi.FMT_NAMES[fmt], "C": C,
+                    "active_experts": na, "ms": ms, "tokens_per_s": T / (ms / 1e3),
+                    "bytes": B, "achieved_gbs": gbs, "peak_gbs": pk["hbm"],
+                    "frac": gbs / pk["hbm"], "bound": "hbm", "peak_source": f"{pk['src']} HBM copy",
+                    "timing": f"median of {args.steps}, 256 MB L2 flush between iterations"}), flush=True)
+            st = L.status()
+            if st != pmoe.PMOE_OK:
+                raise RuntimeError(f"device error: {pmoe.status_string(st)}")
+            del L
+            torch.cuda.empty_cache()
+        del w13, w2
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
     cfg = gi.CONFIGS[args.config]
@@ -285,6 +371,9 @@ def main():
 
     if args.impl == "reference":
         run_reference(args, cfg, rank)
+        return
+    if args.decode:
+        run_decode(args)
         return
 
     import torch

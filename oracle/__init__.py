@@ -114,6 +114,8 @@ def _declare(L):
     L.or_backward.argtypes = [ctypes.POINTER(_Layer), _p, _p, _p, _p, _p, _p, _i, _i,
                               _p, _p, _p, _p, _p]
     L.or_num_threads.restype = _i
+    L.or_pre_round.argtypes = [ctypes.POINTER(_Layer), _p, _p, _p, _i, _p]
+    L.or_pre_round.restype = None
 
 
 def _ptr(a):
@@ -351,6 +353,18 @@ class Layer:
         _L().or_forward(ctypes.byref(self.c), _ptr(X), _ptr(X64), _ptr(idx), _ptr(w), _ptr(toks_a), n,
                         NO_ROUND if no_round else 0, _ptr(Y), _ptr(Y64), _ptr(o))
         return (Y, Y64, o) if want_o else (Y, Y64)
+
+    def pre_round(self, X, idx, toks):
+        """For each pair of the listed tokens (row it*k + j): silu(g) u
+        before its rounding to h, and h R_down before its rounding to h~,
+        as double [n*k, 2I]."""
+        X = _c(X, np.uint16)
+        idx = _c(idx, np.int32)
+        toks_a = _c(toks, np.int32)
+        hx = np.zeros((len(toks_a) * self.k, 2 * self.I), np.float64)
+        _L().or_pre_round(ctypes.byref(self.c), _ptr(X), _ptr(idx), _ptr(toks_a), len(toks_a),
+                          _ptr(hx))
+        return hx
 
     def backward(self, X, dY, idx, w, toks=None, no_round=False, X64=None):
         """Returns dict(dX bf16 bits, dX64, d_topk_w f32 [T,k], dR_up,

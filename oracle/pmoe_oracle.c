@@ -592,6 +592,7 @@ static const void *ws(const or_layer *L, int which, int e)
 /* Per-pair forward state kept for the backward. */
 typedef struct {
     double *x, *xt, *g, *u, *h, *ht, *o;
+    double *hp, *htp;   /* nullable: h and h~ before their BF16 rounding */
 } pair_buf;
 
 static double silu(double g) { return g / (1.0 + exp(-g)); }
@@ -625,11 +626,13 @@ static void expert_forward(const or_layer *L, int e, const uint16_t *xrow, const
         }
         pb->g[n] = g;
         pb->u[n] = u;
+        if (pb->hp) pb->hp[n] = silu(g) * u;
         pb->h[n] = rbf(silu(g) * u, flags);
     }
     if (L->R_down) {
         int64_t o = (int64_t)e * L->stride_down;
         rotate_row64(pb->h, L->R_down + o, L->R_down64 ? L->R_down64 + o : NULL, I, L->b, pb->ht);
+        if (pb->htp) memcpy(pb->htp, pb->ht, sizeof(double) * (size_t)I);
         for (int n = 0; n < I; ++n)
             pb->ht[n] = rbf(pb->ht[n], flags);
     } else {
@@ -651,7 +654,33 @@ static pair_buf pb_alloc(int d, int I)
     double *m = malloc(sizeof(double) * (size_t)(3 * d + 5 * I));
     pb.x = m; pb.xt = m + d; pb.o = m + 2 * d;
     pb.g = m + 3 * d; pb.u = pb.g + I; pb.h = pb.u + I; pb.ht = pb.h + I;
+    pb.hp = pb.htp = NULL;
     return pb;
+}
+
+/*
+ * The values each BF16 rounding decision of the down path is taken on, per
+ * pair p = it*k + j of the listed tokens (it = position in toks): hx[p][n]
+ * = silu(g) u before it is rounded to h, and hx[p][I + n] = (h R_down)
+ * before it is rounded to h~ (h~ = h without an adapter).  Lets a test see
+ * which decisions lie near a BF16 rounding midpoint.
+ */
+void or_pre_round(const or_layer *L, const uint16_t *X, const int32_t *idx, const int32_t *toks,
+                  int n_toks, double *hx)
+{
+    int d = L->d, I = L->I, k = L->k;
+    int64_t np = (int64_t)n_toks * k;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t p = 0; p < np; ++p) {
+        int t = toks ? toks[p / k] : (int)(p / k);
+        int e = idx[(int64_t)t * k + p % k];
+        pair_buf pb = pb_alloc(d, I);
+        pb.hp = hx + p * 2 * I;
+        pb.htp = hx + p * 2 * I + I;
+        expert_forward(L, e, X + (int64_t)t * d, NULL, 0, &pb);
+        if (!L->R_down) memcpy(pb.htp, pb.hp, sizeof(double) * (size_t)I);
+        free(pb.x);
+    }
 }
 
 /*

@@ -113,7 +113,7 @@ static int max_rot_tiles_of(const pmoe_dims &d)
 {
     return (int)(cdiv((int64_t)d.T * d.k, kRotTileRows) + d.E);
 }
-constexpr int kGemmRows = 256, kGemmAlign = 16;
+constexpr int kGemmRows = 192, kGemmAlign = 16;   // token tile <= the GEMM tile width
 
 static pmoe_status run_gemm(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st)
 {

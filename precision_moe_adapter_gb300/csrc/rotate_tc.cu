@@ -79,6 +79,55 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_
     lo = pack_bf2(x0 - bf2f(hi & 0xFFFFu), x1 - bf2f(hi >> 16));
 }
 
+// Correctly rounded BF16 results of the rotation.  v is the tensor cores'
+// FP32 sum of b products and bound >= its error; when v is farther than
+// bound from the midpoint between its two BF16 neighbours, bf16_rne(v) is
+// the rounding of the exact sum.  Otherwise the warp recomputes that sum
+// error-free: each lane takes one or two of the b products (exact in FP32:
+// BF16 x BF16), and a TwoSum butterfly over the lanes carries every
+// addition's rounding error, so s + e is the sum to about 2^-44 of the sum of
+// magnitudes; rounding s decides unless s is a BF16 midpoint itself, where
+// the sign of e breaks the tie.
+__device__ __forceinline__ bool near_bf16_midpoint(float v, float bound)
+{
+    const float mid = __uint_as_float((__float_as_uint(v) & 0xFFFF0000u) | 0x8000u);
+    return fabsf(v - mid) <= bound;
+}
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &t)
+{
+    s = __fadd_rn(a, b);
+    const float z = __fsub_rn(s, a);
+    t = __fadd_rn(__fsub_rn(a, __fsub_rn(s, z)), __fsub_rn(b, z));
+}
+// Whole warp: the exact sum over r < B of x[r] * rc[r * rstride], rounded to
+// BF16 (x and rc in shared memory; every lane returns the same value).
+template <int B>
+__device__ __forceinline__ uint16_t warp_exact_dot_bf16(const uint16_t *x, const uint16_t *rc, int rstride,
+                                                        int lane)
+{
+    float p0 = 0.f, p1 = 0.f;
+    if (lane < B) p0 = __fmul_rn(bf2f(x[lane]), bf2f(rc[lane * rstride]));
+    if (lane + 32 < B) p1 = __fmul_rn(bf2f(x[lane + 32]), bf2f(rc[(lane + 32) * rstride]));
+    float s, e;
+    two_sum(p0, p1, s, e);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const float so = __shfl_xor_sync(0xffffffffu, s, off);
+        const float eo = __shfl_xor_sync(0xffffffffu, e, off);
+        float t;
+        two_sum(s, so, s, t);
+        e = __fadd_rn(__fadd_rn(e, eo), t);
+    }
+    float t;
+    two_sum(s, e, s, t);   // s + t = s + e, |t| <= ulp(s) / 2
+    const uint32_t sb = __float_as_uint(s);
+    if ((sb & 0xFFFFu) == 0x8000u && t != 0.f) {   // s is a BF16 midpoint: t decides
+        const bool away = (t > 0.f) == ((sb >> 31) == 0u);
+        return (uint16_t)((sb >> 16) + (away ? 1u : 0u));
+    }
+    return f2bf(s);
+}
+
 enum RotEpi { ROT_STORE = 0, ROT_SWIGLU_BWD = 1 };
 
 struct RotArgs {
@@ -177,10 +226,17 @@ __global__ void __launch_bounds__(kRotThreads, 2) k_rotate_mma(RotArgs a)
             const uint32_t xs_a = sm0 + buf * S::kStage, rs_a = xs_a + S::kXBytes;
             const uint8_t *xs_p = rsm + buf * S::kStage;
 
-            // warp w: rows 16w .. 16w+15, all B output columns
+            // warp w: rows 16w .. 16w+15, all B output columns.  kExact: BF16
+            // results rounded as the exact sum would be (accabs = |x| |R|
+            // bounds the FP32 error; see exact_dot_bf16)
+            constexpr bool kExact = EPI == ROT_STORE && !F32IN && !F32OUT && B <= 64;
             float acc[B / 8][4];
+            float accabs[kExact ? B / 8 : 1][4];
 #pragma unroll
             for (int n = 0; n < B / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+#pragma unroll
+            for (int n = 0; n < (kExact ? B / 8 : 1); ++n)
+                accabs[n][0] = accabs[n][1] = accabs[n][2] = accabs[n][3] = 0.f;
             if (Re) {
 #pragma unroll
                 for (int kk = 0; kk < B / 16; ++kk) {
@@ -215,6 +271,11 @@ __global__ void __launch_bounds__(kRotThreads, 2) k_rotate_mma(RotArgs a)
                         }
                         mma16816(acc[n], a0, a1, a2, a3, b0r, b1r);
                         mma16816(acc[n + 1], a0, a1, a2, a3, b2r, b3r);
+                        if constexpr (kExact) {
+                            constexpr uint32_t m = 0x7FFF7FFFu;   // |.| of both BF16 halves
+                            mma16816(accabs[n], a0 & m, a1 & m, a2 & m, a3 & m, b0r & m, b1r & m);
+                            mma16816(accabs[n + 1], a0 & m, a1 & m, a2 & m, a3 & m, b2r & m, b3r & m);
+                        }
                         if constexpr (F32IN) {
                             mma16816(acc[n], l0, l1, l2, l3, b0r, b1r);
                             mma16816(acc[n + 1], l0, l1, l2, l3, b2r, b3r);
@@ -249,11 +310,14 @@ __global__ void __launch_bounds__(kRotThreads, 2) k_rotate_mma(RotArgs a)
             for (int n = 0; n < B / 8; ++n)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
+                    // every lane stays in the loop (the exact path below is
+                    // warp-wide); only rows of the tile store
                     const int rl = 16 * warp + g + 8 * h;
-                    if (rl >= tl.nrows) continue;
+                    const bool live = rl < tl.nrows;
                     const int64_t r = tl.row0 + rl;
                     const int col = beta * B + n * 8 + 2 * t;
                     const float v0 = acc[n][2 * h], v1 = acc[n][2 * h + 1];
+                    if (!kExact && !live) continue;
                     if constexpr (EPI == ROT_SWIGLU_BWD) {
                         const float *c = a.ctxf + r * 2 * a.dim + col;
                         const float2 gg = *(const float2 *)c;
@@ -268,7 +332,38 @@ __global__ void __launch_bounds__(kRotThreads, 2) k_rotate_mma(RotArgs a)
                     } else if constexpr (F32OUT) {
                         *(float2 *)((float *)a.out + r * a.out_ld + col) = make_float2(v0, v1);
                     } else {
-                        *(uint32_t *)((uint16_t *)a.out + r * a.out_ld + col) = pack_bf2(v0, v1);
+                        uint32_t packed = pack_bf2(v0, v1);
+                        if constexpr (kExact) {
+                            // the FP32 sum of b <= 64 products over four MMAs
+                            // is within 2^-21 of the sum of their magnitudes;
+                            // 2^-20 of it decides which results may sit near a
+                            // rounding midpoint; those the warp recomputes
+                            if (Re) {
+                                const bool n0 = live && near_bf16_midpoint(v0, accabs[n][2 * h] * 9.5367431640625e-07f);
+                                const bool n1 = live && near_bf16_midpoint(v1, accabs[n][2 * h + 1] * 9.5367431640625e-07f);
+                                const uint16_t *rs = (const uint16_t *)(xs_p + S::kXBytes);
+                                const int cl = n * 8 + 2 * t;   // column in the block
+#pragma unroll
+                                for (int q = 0; q < 2; ++q) {
+                                    uint32_t want = __ballot_sync(0xffffffffu, q ? n1 : n0);
+                                    while (want) {
+                                        const int src = __ffs(want) - 1;
+                                        want &= want - 1;
+                                        const int srow = __shfl_sync(0xffffffffu, rl, src);
+                                        const int scol = __shfl_sync(0xffffffffu, cl, src) + q;
+                                        // column scol of R (x R), or row scol (x R^T)
+                                        const uint16_t *rc = TRANS ? rs + scol * S::kPitchR : rs + scol;
+                                        const uint16_t ex = warp_exact_dot_bf16<B>(
+                                            (const uint16_t *)xs_p + srow * S::kPitchX, rc,
+                                            TRANS ? 1 : S::kPitchR, lane);
+                                        if (lane == src)
+                                            packed = q ? (packed & 0xFFFFu) | ((uint32_t)ex << 16)
+                                                       : (packed & 0xFFFF0000u) | ex;
+                                    }
+                                }
+                            }
+                        }
+                        if (live) *(uint32_t *)((uint16_t *)a.out + r * a.out_ld + col) = packed;
                     }
                 }
             __syncthreads();   // buffer `buf` is restaged two blocks later

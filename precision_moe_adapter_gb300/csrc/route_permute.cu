@@ -472,7 +472,7 @@ int router_tile_rows(int T, int E, int splits, int num_sms)
     const int64_t nft = cdiv(E, 128);
     int64_t r = cdiv((int64_t)T * nft * splits, num_sms > 0 ? num_sms : 1);
     r = (r + 15) & ~(int64_t)15;
-    return (int)std::min<int64_t>(256, std::max<int64_t>(16, r));
+    return (int)std::min<int64_t>(192, std::max<int64_t>(16, r));   // at most the GEMM tile width
 }
 void launch_router_reduce(int T, int E, int splits, const float *part, float *logits, cudaStream_t st)
 {

@@ -98,3 +98,4 @@ def check_routing(X, Wr, bias, k, g_logits, g_idx, g_w, toks=None):
         gaps = -np.diff(ol[n][order][:min(k + 1, len(order))])
         assert np.any(gaps <= b2), (t, gaps.min(), b2)
     return np.array(exact)
+

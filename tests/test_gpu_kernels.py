@@ -193,7 +193,8 @@ def test_route_ties_to_lower_id():
 
 # ---------------------------------------------------------------- adapter
 
-@pytest.mark.parametrize("dim,b,rows", [(256, 32, 100), (7168, 64, 40), (512, 128, 33), (96, 16, 7)])
+@pytest.mark.parametrize("dim,b,rows", [(256, 32, 100), (7168, 64, 40), (2048, 64, 300), (512, 128, 33),
+                                        (96, 16, 7)])
 def test_adapter_apply_and_grad(dim, b, rows):
     rng = np.random.default_rng(dim + b)
     X = gi.f32_to_bf16_bits(rng.standard_normal((rows, dim)).astype(np.float32))
@@ -208,10 +209,16 @@ def test_adapter_apply_and_grad(dim, b, rows):
     torch.cuda.synchronize()
     want = oracle.adapter_apply(X, R, b)
     got = t2np_bits(Xr)
-    assert_close(bits_to_f64(got), bits_to_f64(want), "Xr", rel_fro=2e-3, max_abs=1e-2)
-    assert np.mean(got == want) > 0.95
     wdX, wdR = oracle.adapter_grad(X, dXr, R, b)
-    assert_close(bits_to_f64(t2np_bits(dX)), bits_to_f64(wdX), "dX", rel_fro=2e-3, max_abs=1e-2)
+    if b <= 64:
+        # BF16 outputs rounded as the exact sums are (near a rounding
+        # midpoint the sum is recomputed error-free): bit-exact
+        assert np.array_equal(got, want)
+        assert np.array_equal(t2np_bits(dX), wdX)
+    else:
+        assert_close(bits_to_f64(got), bits_to_f64(want), "Xr", rel_fro=2e-3, max_abs=1e-2)
+        assert np.mean(got == want) > 0.95
+        assert_close(bits_to_f64(t2np_bits(dX)), bits_to_f64(wdX), "dX", rel_fro=2e-3, max_abs=1e-2)
     assert_close(dR.cpu().numpy(), wdR, "dR", rel_fro=1e-5, max_abs=1e-4)
 
 

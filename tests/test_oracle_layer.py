@@ -379,6 +379,10 @@ def test_forward_rounding_points_against_torch():
     want = ht @ W2.T                 # each pair's output o keeps its precision
     assert np.allclose(Y64, want, rtol=1e-12, atol=1e-12)
     assert np.array_equal(bf(Y), r(want))
+    # the values the two down-path decisions are taken on
+    hx = L.pre_round(X, idx, np.arange(cfg.T))
+    assert np.allclose(hx[:, :cfg.I], g / (1 + np.exp(-g)) * u, rtol=1e-12, atol=1e-12)
+    assert np.allclose(hx[:, cfg.I:], h @ _blockdiag(bf(Rd[0])), rtol=1e-12, atol=1e-12)
 
 
 def test_backward_rounding_points_against_torch():
