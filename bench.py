@@ -140,7 +140,7 @@ def bytes_of(cfg, counts):
         wq = 3 * d * I // 2 + 3 * d * (I // 32) * (2 if cfg.fmt == gi.INT4 else 1)
     adp = (d + I) * b * 2 if cfg.adapter == "per_expert" else 0
     act_f = cfg.T * d * 2 * 2 + d * cfg.E * 4          # X, Y, Wr
-    act_b = cfg.T * d * 2 * 3 + cfg.P * I * 10         # X, dY, dX, ctx (g, u f32; h bf16)
+    act_b = cfg.T * d * 2 * 3 + cfg.P * I * 12         # X, dY, dX, ctx (g, u f32; h, h~ bf16)
     return na * (wq + adp) * 2 + act_f + act_b
 
 

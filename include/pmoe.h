@@ -216,7 +216,7 @@ pmoe_status moe_permute_noalloc(pmoe_dims dims, const int32_t *idx, const pmoe_r
  *   ctx NULL, or moe_ctx_bytes(dims) bytes: when given, receives what
  *       moe_backward_data needs, per pair in expert-sorted order (row i =
  *       pair perm[i]): first g | u as f32 [P, 2I] (g in columns 0..I-1,
- *       u in I..2I-1), then h as bf16 [P, I]
+ *       u in I..2I-1), then h as bf16 [P, I], then h~ as bf16 [P, I]
  *   chunk_C >= 1 experts per chunk (>= E means one chunk)
  *   ws  >= moe_workspace_bytes(dims, PMOE_OP_FORWARD, chunk_C, mode)
  * The result does not depend on chunk_C or mode (bit-identical).
@@ -225,7 +225,7 @@ pmoe_status moe_chunked_forward(pmoe_dims dims, const pmoe_weights *wts, const p
                                 const pmoe_routing *rt, const void *X, int32_t chunk_C, int mode,
                                 void *Y, void *ctx, void *ws, size_t ws_bytes,
                                 cudaStream_t stream);
-/* Bytes of the forward's saved context: P * I * (8 + 2); 0 for invalid dims. */
+/* Bytes of the forward's saved context: P * I * (8 + 2 + 2); 0 for invalid dims. */
 size_t moe_ctx_bytes(pmoe_dims dims);
 
 /*
@@ -270,7 +270,7 @@ pmoe_status moe_chunked_forward_slots(pmoe_dims dims, const pmoe_weights *wts,
  *   dh = dh~ R_down^T;  dg = dh u s(g)(1 + g(1 - s(g)));  du = dh silu(g)
  *   dx~ = dg W_gate + du W_up   dR_up[e] += x_blk^T dx~_blk
  *   dx_pair = dx~ R_up^T        dX_t = bf16(sum_j dx_pair), slots in order
- * with h~ = bf16(h blockdiag(R_down[e])) recomputed from the saved h.  Every
+ * with h and h~ = bf16(h blockdiag(R_down[e])) as the forward saved them.  Every
  * intermediate is FP32 (g, u from ctx; G, dh~, dh, dg, du, dx~, dx_pair),
  * except at the tensor cores: dh~ and dx~ enter the rotations and adapter
  * gradients as two BF16 parts hi = bf16(v), lo = bf16(v - hi), which carry

@@ -113,7 +113,9 @@ static int max_rot_tiles_of(const pmoe_dims &d)
 {
     return (int)(cdiv((int64_t)d.T * d.k, kRotTileRows) + d.E);
 }
-constexpr int kGemmRows = 192, kGemmAlign = 16;   // token tile <= the GEMM tile width
+// token tiles: the forward kinds (weights converted into tensor memory) take
+// at most 192 rows, the backward kinds 256
+constexpr int kGemmRowsFwd = 192, kGemmRowsBwd = 256, kGemmAlign = 16;
 
 static pmoe_status run_gemm(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st)
 {
@@ -137,9 +139,9 @@ static Lists carve_lists(Carver &c, const pmoe_dims &d, int C)
     return l;
 }
 static void build_lists(const Lists &l, const pmoe_dims &d, int C, const pmoe_routing *rt,
-                        cudaStream_t st)
+                        int gemm_rows, cudaStream_t st)
 {
-    launch_build_tiles(d.E, C, kGemmRows, kGemmAlign, rt->counts, rt->offsets, rt->active,
+    launch_build_tiles(d.E, C, gemm_rows, kGemmAlign, rt->counts, rt->offsets, rt->active,
                        rt->num_active, l.tiles, l.chunk_tiles, l.chunk_rows, st);
     launch_build_tiles(d.E, C, kRotTileRows, 1, rt->counts, rt->offsets, rt->active,
                        rt->num_active, l.rtiles, l.chunk_rtiles, l.chunk_rrows, st);
@@ -173,7 +175,7 @@ static FwdWs carve_fwd(void *ws, const pmoe_dims &d, int C, int mode, size_t *by
 struct BwdWs {
     DevErr *err;
     Lists l;
-    uint16_t *dyp, *ht;
+    uint16_t *dyp;
     uint16_t *dgu;          // [dg | du], FP16 [P, 2I]
     float *dht, *dxt, *dxp; // dh~ [P, I], dx~ [P, d], rotated dx [P, d], FP32
     float *dtw_part;
@@ -186,7 +188,6 @@ static BwdWs carve_bwd(void *ws, const pmoe_dims &d, int C, size_t *bytes)
     w.err = c.take<DevErr>(kHdrBytes / sizeof(DevErr));
     w.l = carve_lists(c, d, C);
     w.dyp = c.take<uint16_t>(P * d.d);      // gathered dY rows
-    w.ht = c.take<uint16_t>(P * d.inter);
     w.dht = c.take<float>(P * d.inter);
     w.dgu = c.take<uint16_t>(P * 2 * d.inter);
     w.dxt = c.take<float>(P * d.d);
@@ -290,7 +291,7 @@ size_t moe_workspace_bytes(pmoe_dims dims, int op, int32_t chunk_C, int mode)
 size_t moe_ctx_bytes(pmoe_dims dims)
 {
     if (!dims_ok(dims)) return 0;
-    return (size_t)dims.T * dims.k * dims.inter * (4 * 2 + 2);
+    return (size_t)dims.T * dims.k * dims.inter * (4 * 2 + 2 + 2);
 }
 
 size_t moe_scratch_bytes(pmoe_dims dims, int32_t chunk_C, int mode)
@@ -454,13 +455,15 @@ static pmoe_status forward_impl(pmoe_dims dims, const pmoe_weights *wts, const u
         launch_adapter_snapshot(ctrl, w.snap, version_out, stream);
         sel = w.snap;
     }
-    // the saved context: g | u rows (FP32, [P, 2I]) then h rows (BF16, [P, I])
+    // the saved context: g | u rows (FP32, [P, 2I]), then h and h~ rows (BF16,
+    // [P, I] each)
     float *ctx_gu = (float *)ctx;
     uint16_t *h = ctx ? (uint16_t *)(ctx_gu + (int64_t)P * 2 * I) : w.h;
+    uint16_t *ht = ctx ? h + (int64_t)P * I : w.ht;
     const int nch = nchunks_of(dims, C);
     const int maxrt = max_rot_tiles_of(dims);
     const Lists &L = w.l;
-    build_lists(L, dims, C, rt, stream);
+    build_lists(L, dims, C, rt, kGemmRowsFwd, stream);
     // x~ = bf16(x R_up[e]) for every pair, gathered into expert-sorted order
     {
         RotCall c = rot_rows(b, false, X, d, rt->perm, k, R_up, su, d, w.xt, d, L.rtiles,
@@ -485,7 +488,7 @@ static pmoe_status forward_impl(pmoe_dims dims, const pmoe_weights *wts, const u
     gu.nmat = dims.E;
     GemmArgs dn{};
     dn.kind = GK_FWD_DOWN;
-    dn.A = R_dn ? w.ht : h;
+    dn.A = R_dn ? ht : h;
     dn.K = I;
     dn.Nout = d;
     dn.Nst = d;
@@ -497,7 +500,7 @@ static pmoe_status forward_impl(pmoe_dims dims, const pmoe_weights *wts, const u
     dn.nmat = dims.E;
     pmoe_status gs;
     auto rot_down = [&](const int32_t *tb, const int32_t *te) {
-        RotCall c = rot_rows(b, false, h, I, nullptr, k, R_dn, sd, I, w.ht, I, L.rtiles, tb, te,
+        RotCall c = rot_rows(b, false, h, I, nullptr, k, R_dn, sd, I, ht, I, L.rtiles, tb, te,
                              maxrt, 0);
         c.R_alt = R_dn_alt;
         c.sel = sel;
@@ -649,19 +652,17 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
         return PMOE_OK;
     }
     const Lists &L = w.l;
-    // the forward's saved context: g | u rows (FP32, [P, 2I]) then h rows (BF16, [P, I])
+    // the forward's saved context: g | u rows (FP32, [P, 2I]), then h and h~
+    // rows (BF16, [P, I] each; h~ = h without an adapter's R_down)
     const float *ctx_gu = (const float *)ctx;
     const uint16_t *h = (const uint16_t *)(ctx_gu + (int64_t)P * 2 * I);
+    const uint16_t *ht = R_dn ? h + (int64_t)P * I : h;
     const int32_t *rtb = L.chunk_rtiles, *rte = L.chunk_rtiles + nch;
-    build_lists(L, dims, C, rt, stream);
-    // dY rows per pair (expert-sorted) and h~ = bf16(h R_down) from the saved h
+    build_lists(L, dims, C, rt, kGemmRowsBwd, stream);
+    // dY rows per pair (expert-sorted)
     launch_rotate_tc(rot_rows(b, false, dY, d, rt->perm, k, nullptr, 0, d, w.dyp, d, L.rtiles, rtb,
                               rte, maxrt, 0),
                      stream);
-    if (R_dn)
-        launch_rotate_tc(rot_rows(b, false, h, I, nullptr, k, R_dn, sd, I, w.ht, I, L.rtiles, rtb,
-                                  rte, maxrt, 0),
-                         stream);
     pmoe_status gs;
     GemmArgs g{};
     g.kind = GK_BWD_G;
@@ -683,7 +684,7 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
     g.I = I;
     g.w = rt->w;
     g.perm = rt->perm;
-    g.ht = R_dn ? w.ht : h;
+    g.ht = ht;
     g.dtw_part = w.dtw_part;
     g.nmat = E;
     {
@@ -810,7 +811,8 @@ pmoe_status moe_grouped_gemm(pmoe_wfmt fmt, const void *q, const void *s, int32_
     if (!ws || ws_bytes < need || !aligned16(ws)) return PMOE_ERR_WORKSPACE;
     if (rows == 0) return PMOE_OK;
     launch_offsets_to_active(E, rows, offsets, w.counts, w.active, w.num_active, w.err, stream);
-    launch_build_tiles(E, E, kGemmRows, kGemmAlign, w.counts, offsets, w.active, w.num_active,
+    launch_build_tiles(E, E, trans ? kGemmRowsBwd : kGemmRowsFwd, kGemmAlign, w.counts, offsets,
+                       w.active, w.num_active,
                        w.tiles, w.chunk_tiles, w.chunk_rows, stream);
     GemmArgs g{};
     g.kind = trans ? GK_BWD_DX : GK_FWD_DOWN;
@@ -902,7 +904,8 @@ static pmoe_status dense_gemm(pmoe_wfmt fmt, const void *q, const void *s, int N
 {
     launch_set_offsets(w.offsets, rows, st);
     launch_offsets_to_active(1, rows, w.offsets, w.g.counts, w.g.active, w.g.num_active, w.g.err, st);
-    launch_build_tiles(1, 1, kGemmRows, kGemmAlign, w.g.counts, w.offsets, w.g.active,
+    launch_build_tiles(1, 1, trans ? kGemmRowsBwd : kGemmRowsFwd, kGemmAlign, w.g.counts, w.offsets,
+                       w.g.active,
                        w.g.num_active, w.g.tiles, w.g.chunk_tiles, w.g.chunk_rows, st);
     GemmArgs g{};
     g.kind = trans ? GK_BWD_DX : GK_FWD_DOWN;

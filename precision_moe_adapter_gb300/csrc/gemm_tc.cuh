@@ -41,9 +41,9 @@ namespace tc {
 
 constexpr int kBK = 64;                      // K per stage: one 128-byte swizzle row of BF16
 constexpr int kM = 128;                      // MMA M (weight rows per tile)
-constexpr int kNmax = 192;                   // tokens per tile (MMA N)
+constexpr int kNmax = 256;                   // largest token tile (MMA N)
 constexpr int kABytes = kM * kBK * 2;        // 16 KB
-constexpr int kBBytes = kNmax * kBK * 2;     // 24 KB
+constexpr int kBBytes = kNmax * kBK * 2;     // 32 KB
 constexpr int kBoxRows = 32;                 // smallest TMA box: 32 token rows x 64 K
 constexpr int kEpiWarps = 4;
 #ifndef PMOE_PROD_SPLIT
@@ -259,7 +259,8 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 // total += partial over one warp's 32 TMEM lanes, columns [0, ncols): 16
-// columns of each buffer per step, FP32 additions (round to nearest)
+// columns of each buffer per step under one wait (a wider step needs more
+// registers than the kernel has), FP32 additions (round to nearest)
 __device__ __forceinline__ void tmem_drain(uint32_t part, uint32_t total, int ncols)
 {
     for (int c0 = 0; c0 < ncols; c0 += 16) {
@@ -377,7 +378,7 @@ struct TcArgs {
 };
 
 #ifndef PMOE_GU_CHUNK
-#define PMOE_GU_CHUNK 8
+#define PMOE_GU_CHUNK 16
 #endif
 // ------------------------------------------------------------------ pipeline sizes
 // Per kind and weight format.  Packed weight tiles come by TMA into a raw
@@ -400,12 +401,14 @@ struct Pipe {
     // FP16 operands: the converters write the weights' BF16 values in FP16
     // encoding and the token operand is FP16 (11 significant bits)
     static constexpr bool kF16 = KIND == GK_BWD_DX_F16;
-    static constexpr int kBStage = kBBytes;
     // Forward kinds with packed weights convert straight into tensor memory
     // (the MMA reads A from TMEM): no A tile passes through shared memory,
     // which the MMA's B reads and the TMA writes otherwise share.
-    // TMEM: A stages at columns [0, 32 kStagesA), accumulators after them.
+    // TMEM: A stages at columns [0, 32 kStagesA), accumulators after them,
+    // which caps their token tiles at 192 rows; the other kinds take 256.
     static constexpr bool kTmemA = !kTrans && FMT != kFmtBF16 && KIND != GK_ROUTER;
+    static constexpr int kTileN = kTmemA ? 192 : kNmax;
+    static constexpr int kBStage = kTileN * kBK * 2;
     // Chunked accumulation (gate/up, whose sums are rounded to BF16 in h):
     // the tensor cores' FP32 accumulation loses about one bit per 16-long K
     // step, so over thousands of steps g and u drift far beyond FP32 rounding
@@ -426,7 +429,7 @@ struct Pipe {
 #endif
     static constexpr int kASmem = kTmemA ? 0 : kABytes;      // shared memory per A stage
     static constexpr int kAccBase = kTmemA ? 32 * kStagesA : 0;   // first accumulator column
-    static constexpr int kAccCols = kTmemA ? kNmax : 256;   // columns per accumulator buffer
+    static constexpr int kAccCols = kTileN;                 // columns per accumulator buffer
     static_assert(kAccBase + 2 * kAccCols <= 512, "tensor memory budget");
 #ifdef PMOE_B_STAGES
     static constexpr int kStagesB = kFp8 ? 3 : PMOE_B_STAGES;
@@ -741,6 +744,19 @@ struct Dequant {
 // a few ulp in silu flips it near a rounding midpoint
 __device__ __forceinline__ float silu_f(float g) { return g / (1.f + expf(-g)); }
 
+// A work item's token rows, at most the kind's tile width: a longer tile
+// (a work list built for another width) is cut and reported, so no role
+// writes past its stage or accumulator.
+template <int W>
+__device__ __forceinline__ Tile clamp_tile(Tile t, DevErr *err)
+{
+    if (t.nrows > W) {
+        record_error(err, PMOE_ERR_INVALID_ARG, t.row0, t.nrows);
+        t.nrows = W;
+    }
+    return t;
+}
+
 // ------------------------------------------------------------------ kernel
 template <int KIND, int FMT>
 __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__ CUtensorMap tmB256,
@@ -821,7 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             uint32_t g = 0;
             bool ok = true;
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-                const Tile tl = a.tiles[tbeg + item / nft];
+                const Tile tl = clamp_tile<PP::kTileN>(a.tiles[tbeg + item / nft], a.err);
                 const int f0 = (item % nft) * a.m_tile;
                 const int64_t widx = a.slot_index ? (tl.chunk & 0xffff) : tl.expert;
                 for (int ks = 0; ks < nk; ++ks, ++g) {
@@ -893,7 +909,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
         uint32_t g = 0;
         bool ok = true;
         for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-            const Tile tl = a.tiles[tbeg + item / nft];
+            const Tile tl = clamp_tile<PP::kTileN>(a.tiles[tbeg + item / nft], a.err);
             // token rows covered: round up to 32, in boxes of 256/128/64/32 rows
             const int brows = (tl.nrows + kBoxRows - 1) & ~(kBoxRows - 1);
             const int f0 = (item % nft) * a.m_tile;
@@ -959,7 +975,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             // waits until the epilogue has consumed the previous one.
             uint32_t fills0 = 0u, fills1 = 0u;   // (scalars: no local-memory array)
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++li) {
-                const Tile tl = a.tiles[tbeg + item / nft];
+                const Tile tl = clamp_tile<PP::kTileN>(a.tiles[tbeg + item / nft], a.err);
                 const int N = (tl.nrows + 15) & ~15;
                 const uint32_t idesc = idesc_bf16(kM, N, PP::kTrans, PP::kF16);
                 const int tot = li & 1, par = tot ^ 1;
@@ -1140,7 +1156,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
         const int nchunks = (nk + PP::kChunk - 1) / PP::kChunk;
         const uint32_t lanes = (uint32_t)(32 * q) << 16;
         for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++li) {
-            const Tile tl = a.tiles[tbeg + item / nft];
+            const Tile tl = clamp_tile<PP::kTileN>(a.tiles[tbeg + item / nft], a.err);
             const int f0 = (item % nft) * a.m_tile;
             const int tot = li & 1, par = tot ^ 1;
             const int ncols = (tl.nrows + 15) & ~15;
