@@ -113,9 +113,7 @@ static int max_rot_tiles_of(const pmoe_dims &d)
 {
     return (int)(cdiv((int64_t)d.T * d.k, kRotTileRows) + d.E);
 }
-// token tiles: the forward kinds (weights converted into tensor memory) take
-// at most 192 rows, the backward kinds 256
-constexpr int kGemmRowsFwd = 192, kGemmRowsBwd = 256, kGemmAlign = 16;
+constexpr int kGemmRows = 256, kGemmAlign = 16;   // token tile <= the GEMM tile width
 
 static pmoe_status run_gemm(const GemmArgs &g, int64_t P, DevErr *err, cudaStream_t st)
 {
@@ -139,9 +137,9 @@ static Lists carve_lists(Carver &c, const pmoe_dims &d, int C)
     return l;
 }
 static void build_lists(const Lists &l, const pmoe_dims &d, int C, const pmoe_routing *rt,
-                        int gemm_rows, cudaStream_t st)
+                        cudaStream_t st)
 {
-    launch_build_tiles(d.E, C, gemm_rows, kGemmAlign, rt->counts, rt->offsets, rt->active,
+    launch_build_tiles(d.E, C, kGemmRows, kGemmAlign, rt->counts, rt->offsets, rt->active,
                        rt->num_active, l.tiles, l.chunk_tiles, l.chunk_rows, st);
     launch_build_tiles(d.E, C, kRotTileRows, 1, rt->counts, rt->offsets, rt->active,
                        rt->num_active, l.rtiles, l.chunk_rtiles, l.chunk_rrows, st);
@@ -463,7 +461,7 @@ static pmoe_status forward_impl(pmoe_dims dims, const pmoe_weights *wts, const u
     const int nch = nchunks_of(dims, C);
     const int maxrt = max_rot_tiles_of(dims);
     const Lists &L = w.l;
-    build_lists(L, dims, C, rt, kGemmRowsFwd, stream);
+    build_lists(L, dims, C, rt, stream);
     // x~ = bf16(x R_up[e]) for every pair, gathered into expert-sorted order
     {
         RotCall c = rot_rows(b, false, X, d, rt->perm, k, R_up, su, d, w.xt, d, L.rtiles,
@@ -658,11 +656,9 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
     const uint16_t *h = (const uint16_t *)(ctx_gu + (int64_t)P * 2 * I);
     const uint16_t *ht = R_dn ? h + (int64_t)P * I : h;
     const int32_t *rtb = L.chunk_rtiles, *rte = L.chunk_rtiles + nch;
-    build_lists(L, dims, C, rt, kGemmRowsBwd, stream);
+    build_lists(L, dims, C, rt, stream);
     // dY rows per pair (expert-sorted)
-    launch_rotate_tc(rot_rows(b, false, dY, d, rt->perm, k, nullptr, 0, d, w.dyp, d, L.rtiles, rtb,
-                              rte, maxrt, 0),
-                     stream);
+    launch_gather_rows(P, d, k, (const uint16_t *)dY, rt->perm, rt->offsets + E, w.dyp, stream);
     pmoe_status gs;
     GemmArgs g{};
     g.kind = GK_BWD_G;
@@ -811,8 +807,7 @@ pmoe_status moe_grouped_gemm(pmoe_wfmt fmt, const void *q, const void *s, int32_
     if (!ws || ws_bytes < need || !aligned16(ws)) return PMOE_ERR_WORKSPACE;
     if (rows == 0) return PMOE_OK;
     launch_offsets_to_active(E, rows, offsets, w.counts, w.active, w.num_active, w.err, stream);
-    launch_build_tiles(E, E, trans ? kGemmRowsBwd : kGemmRowsFwd, kGemmAlign, w.counts, offsets,
-                       w.active, w.num_active,
+    launch_build_tiles(E, E, kGemmRows, kGemmAlign, w.counts, offsets, w.active, w.num_active,
                        w.tiles, w.chunk_tiles, w.chunk_rows, stream);
     GemmArgs g{};
     g.kind = trans ? GK_BWD_DX : GK_FWD_DOWN;
@@ -904,8 +899,7 @@ static pmoe_status dense_gemm(pmoe_wfmt fmt, const void *q, const void *s, int N
 {
     launch_set_offsets(w.offsets, rows, st);
     launch_offsets_to_active(1, rows, w.offsets, w.g.counts, w.g.active, w.g.num_active, w.g.err, st);
-    launch_build_tiles(1, 1, trans ? kGemmRowsBwd : kGemmRowsFwd, kGemmAlign, w.g.counts, w.offsets,
-                       w.g.active,
+    launch_build_tiles(1, 1, kGemmRows, kGemmAlign, w.g.counts, w.offsets, w.g.active,
                        w.g.num_active, w.g.tiles, w.g.chunk_tiles, w.g.chunk_rows, st);
     GemmArgs g{};
     g.kind = trans ? GK_BWD_DX : GK_FWD_DOWN;

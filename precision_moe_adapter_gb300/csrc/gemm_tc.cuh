@@ -196,32 +196,6 @@ __device__ __forceinline__ void umma_step_warp(uint32_t d_tmem, const uint64_t (
         "r"(accum), "r"(idesc), "r"(bar)
         : "memory");
 }
-// The same K step with A in tensor memory (the four K = 16 slices at TMEM
-// addresses a0..a3: 8 columns apart, two BF16 per 32-bit column).
-__device__ __forceinline__ void umma_step_ts_warp(uint32_t d_tmem, const uint32_t (&a)[4], const uint64_t (&b)[4],
-                                                  uint32_t idesc, uint32_t accum, uint32_t bar)
-{
-    asm volatile(
-        "{ .reg .pred e, p, t; elect.sync _|e, 0xffffffff; setp.ne.b32 p, %9, 0; setp.eq.b32 t, %9, %9;\n"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %10, p;\n"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %6, %10, t;\n"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %10, t;\n"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %10, t;\n"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%11]; }" ::"r"(d_tmem),
-        "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]),
-        "r"(accum), "r"(idesc), "r"(bar)
-        : "memory");
-}
-__device__ __forceinline__ void tmem_st16_u(uint32_t taddr, const uint4 (&v)[4])
-{
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-            taddr),
-        "r"(v[0].x), "r"(v[0].y), "r"(v[0].z), "r"(v[0].w), "r"(v[1].x), "r"(v[1].y), "r"(v[1].z),
-        "r"(v[1].w), "r"(v[2].x), "r"(v[2].y), "r"(v[2].z), "r"(v[2].w), "r"(v[3].x), "r"(v[3].y),
-        "r"(v[3].z), "r"(v[3].w)
-        : "memory");
-}
 __device__ __forceinline__ void umma_commit_warp(uint32_t bar)
 {
     asm volatile(
@@ -401,13 +375,7 @@ struct Pipe {
     // FP16 operands: the converters write the weights' BF16 values in FP16
     // encoding and the token operand is FP16 (11 significant bits)
     static constexpr bool kF16 = KIND == GK_BWD_DX_F16;
-    // Forward kinds with packed weights convert straight into tensor memory
-    // (the MMA reads A from TMEM): no A tile passes through shared memory,
-    // which the MMA's B reads and the TMA writes otherwise share.
-    // TMEM: A stages at columns [0, 32 kStagesA), accumulators after them,
-    // which caps their token tiles at 192 rows; the other kinds take 256.
-    static constexpr bool kTmemA = !kTrans && FMT != kFmtBF16 && KIND != GK_ROUTER;
-    static constexpr int kTileN = kTmemA ? 192 : kNmax;
+    static constexpr int kTileN = kNmax;
     static constexpr int kBStage = kTileN * kBK * 2;
     // Chunked accumulation (gate/up, whose sums are rounded to BF16 in h):
     // the tensor cores' FP32 accumulation loses about one bit per 16-long K
@@ -423,14 +391,13 @@ struct Pipe {
     // different depths: the converters may run kStagesA steps ahead of the
     // MMA, the token producer kStagesB steps (kStagesB <= kStagesA)
 #ifdef PMOE_A_STAGES
-    static constexpr int kStagesA = kTmemA ? 4 : kFp8 ? 3 : PMOE_A_STAGES;
+    static constexpr int kStagesA = kFp8 ? 3 : PMOE_A_STAGES;
 #else
-    static constexpr int kStagesA = kTmemA ? 4 : kFp8 ? 3 : 4;
+    static constexpr int kStagesA = kFp8 ? 3 : 4;
 #endif
-    static constexpr int kASmem = kTmemA ? 0 : kABytes;      // shared memory per A stage
-    static constexpr int kAccBase = kTmemA ? 32 * kStagesA : 0;   // first accumulator column
+    static constexpr int kASmem = kABytes;                  // shared memory per A stage
     static constexpr int kAccCols = kTileN;                 // columns per accumulator buffer
-    static_assert(kAccBase + 2 * kAccCols <= 512, "tensor memory budget");
+    static_assert(2 * kAccCols <= 512, "tensor memory budget");
 #ifdef PMOE_B_STAGES
     static constexpr int kStagesB = kFp8 ? 3 : PMOE_B_STAGES;
 #else
@@ -628,44 +595,6 @@ struct Dequant {
             } else {
                 out[c] = chunk8(make_uint2(wv[2 * c], wv[2 * c + 1]), __uint_as_float(sw));
             }
-        }
-    }
-    // Forward kinds, A in tensor memory: the thread of TMEM lane m converts
-    // the 32 elements 32h .. 32h+31 of A row m (one scale group) into four
-    // 16-byte chunks, i.e. 16 TMEM columns.
-    __device__ static void compute_tm(const TcArgs &a, int f0, int ks, int m, int h, const uint8_t *rawt,
-                                      uint4 (&out)[4])
-    {
-        using PP = Pipe<KIND, FMT>;
-        const int rr = raw_row(m);
-        const bool lv = KIND == GK_FWD_GU || f0 + m < a.Mtot;
-        if (!lv) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) out[j] = make_uint4(0, 0, 0, 0);
-            return;
-        }
-        const uint8_t *row = rawt + rr * PP::kRowBytes;
-        const uint32_t sw = *(const uint32_t *)(rawt + PP::kScaleOff + 4 * rr);
-        if (FMT == PMOE_W_FP8_B128_F32) {
-            const uint4 q0 = *(const uint4 *)(row + 32 * h), q1 = *(const uint4 *)(row + 32 * h + 16);
-            const float sc = __uint_as_float(sw);
-            out[0] = chunk8(make_uint2(q0.x, q0.y), sc);
-            out[1] = chunk8(make_uint2(q0.z, q0.w), sc);
-            out[2] = chunk8(make_uint2(q1.x, q1.y), sc);
-            out[3] = chunk8(make_uint2(q1.z, q1.w), sc);
-        } else {
-            const uint4 q = *(const uint4 *)(row + 16 * h);
-            uint32_t sb;
-            if (FMT == PMOE_W_INT4_G32_BF16) {
-                sb = h ? sw >> 16 : sw & 0xFFFFu;
-            } else {
-                const int64_t gi = stored_row(a, f0, rr) * (a.Kst >> 5) + 2 * ks + h;
-                sb = (sw >> (8 * (gi & 3))) & 0xFFu;
-            }
-            out[0] = chunk4(q.x, sb);
-            out[1] = chunk4(q.y, sb);
-            out[2] = chunk4(q.z, sb);
-            out[3] = chunk4(q.w, sb);
         }
     }
     template <int EPT>
@@ -998,16 +927,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                     const uint64_t bd = bdesc0 + (uint32_t)((g % kStagesB) * (PP::kBStage >> 4));
                     static_assert(kBK == 64, "four MMAs of K = 16 per step");
                     const uint64_t bv[4] = {bd, bd + 2, bd + 4, bd + 6};
-                    const uint32_t dacc = tmem + PP::kAccBase + buf * PP::kAccCols;
-                    if constexpr (PP::kTmemA) {
-                        const uint32_t at = tmem + 32 * s;   // A stage s: 32 columns
-                        const uint32_t av[4] = {at, at + 8, at + 16, at + 24};
-                        umma_step_ts_warp(dacc, av, bv, idesc, !first, empty(fb(g)));
-                    } else {
-                        const uint64_t ad = adesc0 + (uint32_t)(s * (kABytes >> 4));
-                        const uint64_t av[4] = {ad, ad + kAStep, ad + 2 * kAStep, ad + 3 * kAStep};
-                        umma_step_warp(dacc, av, bv, idesc, !first, empty(fb(g)));
-                    }
+                    const uint32_t dacc = tmem + buf * PP::kAccCols;
+                    const uint64_t ad = adesc0 + (uint32_t)(s * (kABytes >> 4));
+                    const uint64_t av[4] = {ad, ad + kAStep, ad + 2 * kAStep, ad + 3 * kAStep};
+                    umma_step_warp(dacc, av, bv, idesc, !first, empty(fb(g)));
                     // a partial chunk is complete: hand it to the epilogue
                     if (buf == par && ((ks + 1) % PP::kChunk == 0 || ks + 1 == nk)) umma_commit_warp(tfull(par));
                 }
@@ -1018,65 +941,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
         }
     } else if (warp >= kDqWarp0) {
         const int td = threadIdx.x - kDqWarp0 * 32;
-        if constexpr (PP::kTmemA) {
-            // ---------------- converters into tensor memory.  Warp w writes
-            // TMEM lanes 32 (w % 4) .. +31 (a warp reaches only its quadrant);
-            // the group's two warps of a quadrant take the two halves of the
-            // K step.  Groups alternate K steps as in the shared-memory path.
-            static_assert(kDqWarps / kConvGroups == 8, "two warps per TMEM quadrant in a group");
-            const int wq = warp - kDqWarp0;
-            const int grp = wq / 8, half = (wq % 8) / 4, quad = warp % 4;
-            const int m = 32 * quad + lane;
-            const int my_items = n_items > (int)blockIdx.x ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-            const uint32_t total = (uint32_t)my_items * nk;
-            const uint32_t tlane = tmem + ((uint32_t)(32 * quad) << 16) + 16 * half;
-            struct Cur {
-                uint32_t j;
-                int ks, li, f0;
-            };
-            auto at = [&](uint32_t j) {
-                Cur c;
-                c.j = j;
-                c.li = (int)(j / nk);
-                c.ks = (int)(j - (uint32_t)c.li * nk);
-                c.f0 = (((int)blockIdx.x + c.li * (int)gridDim.x) % nft) * a.m_tile;
-                return c;
-            };
-            auto advance = [&](Cur &c) {
-                c.j += kConvGroups;
-                c.ks += kConvGroups;
-                if (c.ks >= nk) c = at(c.j);
-            };
-            auto compute = [&](const Cur &c, uint4 (&o)[4]) -> bool {
-                const int r = c.j % PP::kRawTma;
-                if (!mbar_wait(raw_full(r), (c.j / PP::kRawTma) & 1, a.err, 8, a.wait_ns)) return false;
-                Dequant<KIND, FMT>::compute_tm(a, c.f0, c.ks, m, half, smem + PP::kRawOff + r * PP::kRawTile, o);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(raw_empty(r));
-                return true;
-            };
-            uint4 bufa[4], bufb[4];
-            Cur nc = at((uint32_t)grp);
-            bool ok = (uint32_t)grp >= total || compute(nc, bufa);
-            auto body = [&](uint32_t g, const uint4 (&cur)[4], uint4 (&nxt)[4]) -> bool {
-                const int s = g % kStages;
-                if (!mbar_wait(empty(fb(g)), fph(g) ^ 1, a.err, 5, a.wait_ns)) return false;
-                tc_fence_after();   // after the MMAs that read this stage
-                tmem_st16_u(tlane + 32 * s, cur);
-                advance(nc);
-                const bool okc = nc.j >= total || compute(nc, nxt);
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(full_a(fb(g)));
-                return okc;
-            };
-            for (uint32_t g = grp; ok && g < total; g += 2 * kConvGroups) {
-                ok = body(g, bufa, bufb);
-                if (!ok || g + kConvGroups >= total) break;
-                ok = body(g + kConvGroups, bufb, bufa);
-            }
-        } else if constexpr (PP::kTmaRaw) {
+        if constexpr (PP::kTmaRaw) {
             // ---------------- converters: TMA raw tile -> BF16 A stage.  The
             // converter warps form kConvGroups groups; group G takes the steps
             // g = G (mod kConvGroups), so several stages are in conversion at
@@ -1167,8 +1032,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
                 const uint32_t u = par ? cons1++ : cons0++;
                 if (!(ok = mbar_wait(tfull(par), u & 1, a.err, 9, a.wait_ns))) break;
                 tc_fence_after();
-                tmem_drain(tmem + lanes + PP::kAccBase + par * PP::kAccCols,
-                           tmem + lanes + PP::kAccBase + tot * PP::kAccCols, ncols);
+                tmem_drain(tmem + lanes + par * PP::kAccCols, tmem + lanes + tot * PP::kAccCols, ncols);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty(par));
@@ -1177,7 +1041,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
             const uint32_t ut = tot ? cons1++ : cons0++;
             if (!mbar_wait(tfull(tot), ut & 1, a.err, 6, a.wait_ns)) break;
             tc_fence_after();
-            const uint32_t taddr = tmem + lanes + PP::kAccBase + tot * PP::kAccCols;
+            const uint32_t taddr = tmem + lanes + tot * PP::kAccCols;
             for (int c0 = 0; c0 < ncols; c0 += 16) {
                 float v[16];
                 tmem_ld16(taddr + c0, v);

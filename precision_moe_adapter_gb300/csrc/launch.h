@@ -142,7 +142,7 @@ void launch_adapter_publish(uint64_t *ctrl, uint32_t slot, uint32_t version, cud
 // offsets = [0, rows] (a single-matrix work list)
 void launch_set_offsets(int32_t *offsets, int rows, cudaStream_t st);
 void launch_gather_rows(int P, int d, int k, const uint16_t *src, const int32_t *perm,
-                        uint16_t *out, cudaStream_t st);
+                        const int32_t *nvalid, uint16_t *out, cudaStream_t st);
 // d_topk_w[p] = sum of pair p's partials (row inv_perm[p]); 0 for a pair
 // left out of the grouping
 void launch_dtw_reduce(int P, int nparts, const float *part, const int32_t *inv_perm, float *dtw,

@@ -43,20 +43,35 @@ void launch_combine(int T, int d, int k, const float *o, const int32_t *inv_perm
     note_launch();
 }
 
-__global__ void k_gather_rows(int P, int d, int k, const uint16_t *__restrict__ src,
-                              const int32_t *__restrict__ perm, uint16_t *__restrict__ out)
+// out[r] = src[perm[r] / k] for the grouped rows r < *nvalid (the rows past
+// it, pairs left out of the grouping, are not touched).  One CTA per row;
+// every thread issues its (up to four) 16-byte loads before its stores.
+__global__ void __launch_bounds__(256) k_gather_rows(int d, int k, const uint16_t *__restrict__ src,
+                                                     const int32_t *__restrict__ perm,
+                                                     const int32_t *__restrict__ nvalid,
+                                                     uint16_t *__restrict__ out)
 {
-    int r = blockIdx.x;
-    const uint16_t *s = src + (int64_t)(perm[r] / k) * d;
-    for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8)
-        *(uint4 *)(out + (int64_t)r * d + c) = *(const uint4 *)(s + c);
+    const int r = blockIdx.x;
+    if (r >= *nvalid) return;
+    const uint4 *s = (const uint4 *)(src + (int64_t)(perm[r] / k) * d);
+    uint4 *o = (uint4 *)(out + (int64_t)r * d);
+    const int n = d / 8;
+    for (int c0 = threadIdx.x; c0 < n; c0 += 4 * 256) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (c0 + u * 256 < n) v[u] = __ldg(s + c0 + u * 256);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (c0 + u * 256 < n) o[c0 + u * 256] = v[u];
+    }
 }
 
 void launch_gather_rows(int P, int d, int k, const uint16_t *src, const int32_t *perm,
-                        uint16_t *out, cudaStream_t st)
+                        const int32_t *nvalid, uint16_t *out, cudaStream_t st)
 {
     if (P <= 0) return;
-    k_gather_rows<<<P, 256, 0, st>>>(P, d, k, src, perm, out);
+    k_gather_rows<<<P, 256, 0, st>>>(d, k, src, perm, nvalid, out);
     note_launch();
 }
 

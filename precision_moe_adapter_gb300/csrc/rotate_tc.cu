@@ -27,6 +27,7 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "exact_bf16.cuh"
 #include "launch.h"
 
 namespace pmoe {
@@ -79,26 +80,6 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_
     lo = pack_bf2(x0 - bf2f(hi & 0xFFFFu), x1 - bf2f(hi >> 16));
 }
 
-// Correctly rounded BF16 results of the rotation.  v is the tensor cores'
-// FP32 sum of b products and bound >= its error; when v is farther than
-// bound from the midpoint between its two BF16 neighbours, bf16_rne(v) is
-// the rounding of the exact sum.  Otherwise the warp recomputes that sum
-// error-free: each lane takes one or two of the b products (exact in FP32:
-// BF16 x BF16), and a TwoSum butterfly over the lanes carries every
-// addition's rounding error, so s + e is the sum to about 2^-44 of the sum of
-// magnitudes; rounding s decides unless s is a BF16 midpoint itself, where
-// the sign of e breaks the tie.
-__device__ __forceinline__ bool near_bf16_midpoint(float v, float bound)
-{
-    const float mid = __uint_as_float((__float_as_uint(v) & 0xFFFF0000u) | 0x8000u);
-    return fabsf(v - mid) <= bound;
-}
-__device__ __forceinline__ void two_sum(float a, float b, float &s, float &t)
-{
-    s = __fadd_rn(a, b);
-    const float z = __fsub_rn(s, a);
-    t = __fadd_rn(__fsub_rn(a, __fsub_rn(s, z)), __fsub_rn(b, z));
-}
 // Whole warp: the exact sum over r < B of x[r] * rc[r * rstride], rounded to
 // BF16 (x and rc in shared memory; every lane returns the same value).
 template <int B>
@@ -108,24 +89,7 @@ __device__ __forceinline__ uint16_t warp_exact_dot_bf16(const uint16_t *x, const
     float p0 = 0.f, p1 = 0.f;
     if (lane < B) p0 = __fmul_rn(bf2f(x[lane]), bf2f(rc[lane * rstride]));
     if (lane + 32 < B) p1 = __fmul_rn(bf2f(x[lane + 32]), bf2f(rc[(lane + 32) * rstride]));
-    float s, e;
-    two_sum(p0, p1, s, e);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        const float so = __shfl_xor_sync(0xffffffffu, s, off);
-        const float eo = __shfl_xor_sync(0xffffffffu, e, off);
-        float t;
-        two_sum(s, so, s, t);
-        e = __fadd_rn(__fadd_rn(e, eo), t);
-    }
-    float t;
-    two_sum(s, e, s, t);   // s + t = s + e, |t| <= ulp(s) / 2
-    const uint32_t sb = __float_as_uint(s);
-    if ((sb & 0xFFFFu) == 0x8000u && t != 0.f) {   // s is a BF16 midpoint: t decides
-        const bool away = (t > 0.f) == ((sb >> 31) == 0u);
-        return (uint16_t)((sb >> 16) + (away ? 1u : 0u));
-    }
-    return f2bf(s);
+    return warp_sum_round_bf16(p0, p1);
 }
 
 enum RotEpi { ROT_STORE = 0, ROT_SWIGLU_BWD = 1 };
@@ -163,7 +127,7 @@ struct RotSmem {
 };
 
 template <int B, bool TRANS, int EPI, bool F32IN, bool F32OUT>
-__global__ void __launch_bounds__(kRotThreads, 2) k_rotate_mma(RotArgs a)
+__global__ void __launch_bounds__(kRotThreads, F32IN ? 2 : 3) k_rotate_mma(RotArgs a)
 {
     using S = RotSmem<B, F32IN>;
     extern __shared__ __align__(16) uint8_t rsm[];
@@ -226,146 +190,158 @@ __global__ void __launch_bounds__(kRotThreads, 2) k_rotate_mma(RotArgs a)
             const uint32_t xs_a = sm0 + buf * S::kStage, rs_a = xs_a + S::kXBytes;
             const uint8_t *xs_p = rsm + buf * S::kStage;
 
-            // warp w: rows 16w .. 16w+15, all B output columns.  kExact: BF16
-            // results rounded as the exact sum would be (accabs = |x| |R|
-            // bounds the FP32 error; see exact_dot_bf16)
+            // warp w: rows 16w .. 16w+15, the B output columns in NS slices
+            // of NB column groups of 8 (fewer live accumulators: more CTAs
+            // per SM).  kExact: BF16 results rounded as the exact sum would
+            // be (accabs = |x| |R| bounds the FP32 error; see
+            // warp_exact_dot_bf16)
             constexpr bool kExact = EPI == ROT_STORE && !F32IN && !F32OUT && B <= 64;
-            float acc[B / 8][4];
-            float accabs[kExact ? B / 8 : 1][4];
+            constexpr int NS = (B >= 32 && !F32IN) ? 2 : 1;   // FP32 sources: split once per block
+            constexpr int NB = B / 8 / NS;
+#pragma unroll 1
+            for (int ns = 0; ns < NS; ++ns) {
+                float acc[NB][4];
+                float accabs[kExact ? NB : 1][4];
 #pragma unroll
-            for (int n = 0; n < B / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+                for (int n = 0; n < NB; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 #pragma unroll
-            for (int n = 0; n < (kExact ? B / 8 : 1); ++n)
-                accabs[n][0] = accabs[n][1] = accabs[n][2] = accabs[n][3] = 0.f;
-            if (Re) {
+                for (int n = 0; n < (kExact ? NB : 1); ++n)
+                    accabs[n][0] = accabs[n][1] = accabs[n][2] = accabs[n][3] = 0.f;
+                if (Re) {
 #pragma unroll
-                for (int kk = 0; kk < B / 16; ++kk) {
-                    uint32_t a0, a1, a2, a3, l0 = 0, l1 = 0, l2 = 0, l3 = 0;
-                    if constexpr (F32IN) {
-                        const float *x0 = (const float *)xs_p + (16 * warp + g) * S::kPitchX + kk * 16 + 2 * t;
-                        const float *x1 = x0 + 8 * S::kPitchX;
-                        const float2 v00 = *(const float2 *)x0, v02 = *(const float2 *)(x0 + 8);
-                        const float2 v10 = *(const float2 *)x1, v12 = *(const float2 *)(x1 + 8);
-                        split2(v00.x, v00.y, a0, l0);
-                        split2(v10.x, v10.y, a1, l1);
-                        split2(v02.x, v02.y, a2, l2);
-                        split2(v12.x, v12.y, a3, l3);
-                    } else {
-                        const int row = 16 * warp + (lane & 15);
-                        const int col = kk * 16 + (lane >> 4) * 8;
-                        ldsm_x4(xs_a + (row * S::kPitchX + col) * 2, a0, a1, a2, a3);
-                    }
-#pragma unroll
-                    for (int n = 0; n < B / 8; n += 2) {
-                        uint32_t b0r, b1r, b2r, b3r;
-                        if (!TRANS) {
-                            // B(k, n) = R[k][n], row-major [k][n]: transposed 8x8 loads
-                            const int krow = kk * 16 + (lane & 15);
-                            const int ncol = n * 8 + (lane >> 4) * 8;
-                            ldsm_x4_t(rs_a + (krow * S::kPitchR + ncol) * 2, b0r, b1r, b2r, b3r);
-                        } else {
-                            // B(k, n) = R[n][k]: row-major [n][k] is the col layout
-                            const int nrow = n * 8 + (lane & 7) + ((lane >> 4) << 3);
-                            const int kcol = kk * 16 + ((lane >> 3) & 1) * 8;
-                            ldsm_x4(rs_a + (nrow * S::kPitchR + kcol) * 2, b0r, b1r, b2r, b3r);
-                        }
-                        mma16816(acc[n], a0, a1, a2, a3, b0r, b1r);
-                        mma16816(acc[n + 1], a0, a1, a2, a3, b2r, b3r);
-                        if constexpr (kExact) {
-                            constexpr uint32_t m = 0x7FFF7FFFu;   // |.| of both BF16 halves
-                            mma16816(accabs[n], a0 & m, a1 & m, a2 & m, a3 & m, b0r & m, b1r & m);
-                            mma16816(accabs[n + 1], a0 & m, a1 & m, a2 & m, a3 & m, b2r & m, b3r & m);
-                        }
+                    for (int kk = 0; kk < B / 16; ++kk) {
+                        uint32_t a0, a1, a2, a3, l0 = 0, l1 = 0, l2 = 0, l3 = 0;
                         if constexpr (F32IN) {
-                            mma16816(acc[n], l0, l1, l2, l3, b0r, b1r);
-                            mma16816(acc[n + 1], l0, l1, l2, l3, b2r, b3r);
-                        }
-                    }
-                }
-            } else {
-                // identity: C = A.  An FP32 source passes as hi + lo, exactly
-                // what the two MMAs give with R = I (hi + lo is exact in
-                // FP32), so a unit rotation and no rotation agree bit for bit
-#pragma unroll
-                for (int n = 0; n < B / 8; ++n)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int row = 16 * warp + g + 8 * h;
-                        if constexpr (F32IN) {
-                            const float2 v = *(const float2 *)((const float *)xs_p + row * S::kPitchX + n * 8 + 2 * t);
-                            uint32_t hi, lo;
-                            split2(v.x, v.y, hi, lo);
-                            acc[n][2 * h] = bf2f(hi & 0xFFFFu) + bf2f(lo & 0xFFFFu);
-                            acc[n][2 * h + 1] = bf2f(hi >> 16) + bf2f(lo >> 16);
+                            const float *x0 = (const float *)xs_p + (16 * warp + g) * S::kPitchX + kk * 16 + 2 * t;
+                            const float *x1 = x0 + 8 * S::kPitchX;
+                            const float2 v00 = *(const float2 *)x0, v02 = *(const float2 *)(x0 + 8);
+                            const float2 v10 = *(const float2 *)x1, v12 = *(const float2 *)(x1 + 8);
+                            split2(v00.x, v00.y, a0, l0);
+                            split2(v10.x, v10.y, a1, l1);
+                            split2(v02.x, v02.y, a2, l2);
+                            split2(v12.x, v12.y, a3, l3);
                         } else {
-                            const uint32_t v = *(const uint32_t *)((const uint16_t *)xs_p + row * S::kPitchX + n * 8 + 2 * t);
-                            acc[n][2 * h] = bf2f(v & 0xFFFFu);
-                            acc[n][2 * h + 1] = bf2f(v >> 16);
+                            const int row = 16 * warp + (lane & 15);
+                            const int col = kk * 16 + (lane >> 4) * 8;
+                            ldsm_x4(xs_a + (row * S::kPitchX + col) * 2, a0, a1, a2, a3);
                         }
-                    }
-            }
-            // epilogue straight from the fragments: each quad of lanes writes
-            // 2 consecutive columns of one row
 #pragma unroll
-            for (int n = 0; n < B / 8; ++n)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    // every lane stays in the loop (the exact path below is
-                    // warp-wide); only rows of the tile store
-                    const int rl = 16 * warp + g + 8 * h;
-                    const bool live = rl < tl.nrows;
-                    const int64_t r = tl.row0 + rl;
-                    const int col = beta * B + n * 8 + 2 * t;
-                    const float v0 = acc[n][2 * h], v1 = acc[n][2 * h + 1];
-                    if (!kExact && !live) continue;
-                    if constexpr (EPI == ROT_SWIGLU_BWD) {
-                        const float *c = a.ctxf + r * 2 * a.dim + col;
-                        const float2 gg = *(const float2 *)c;
-                        const float2 uu = *(const float2 *)(c + a.dim);
-                        const float s0 = 1.f / (1.f + expf(-gg.x)), s1 = 1.f / (1.f + expf(-gg.y));
-                        const float dg0 = v0 * uu.x * s0 * (1.f + gg.x * (1.f - s0));
-                        const float dg1 = v1 * uu.y * s1 * (1.f + gg.y * (1.f - s1));
-                        const float du0 = v0 * (gg.x * s0), du1 = v1 * (gg.y * s1);
-                        __half2 *o = (__half2 *)((uint16_t *)a.out + r * a.out_ld + col);
-                        o[0] = __floats2half2_rn(dg0, dg1);
-                        o[a.dim / 2] = __floats2half2_rn(du0, du1);
-                    } else if constexpr (F32OUT) {
-                        *(float2 *)((float *)a.out + r * a.out_ld + col) = make_float2(v0, v1);
-                    } else {
-                        uint32_t packed = pack_bf2(v0, v1);
-                        if constexpr (kExact) {
-                            // the FP32 sum of b <= 64 products over four MMAs
-                            // is within 2^-21 of the sum of their magnitudes;
-                            // 2^-20 of it decides which results may sit near a
-                            // rounding midpoint; those the warp recomputes
-                            if (Re) {
-                                const bool n0 = live && near_bf16_midpoint(v0, accabs[n][2 * h] * 9.5367431640625e-07f);
-                                const bool n1 = live && near_bf16_midpoint(v1, accabs[n][2 * h + 1] * 9.5367431640625e-07f);
-                                const uint16_t *rs = (const uint16_t *)(xs_p + S::kXBytes);
-                                const int cl = n * 8 + 2 * t;   // column in the block
-#pragma unroll
-                                for (int q = 0; q < 2; ++q) {
-                                    uint32_t want = __ballot_sync(0xffffffffu, q ? n1 : n0);
-                                    while (want) {
-                                        const int src = __ffs(want) - 1;
-                                        want &= want - 1;
-                                        const int srow = __shfl_sync(0xffffffffu, rl, src);
-                                        const int scol = __shfl_sync(0xffffffffu, cl, src) + q;
-                                        // column scol of R (x R), or row scol (x R^T)
-                                        const uint16_t *rc = TRANS ? rs + scol * S::kPitchR : rs + scol;
-                                        const uint16_t ex = warp_exact_dot_bf16<B>(
-                                            (const uint16_t *)xs_p + srow * S::kPitchX, rc,
-                                            TRANS ? 1 : S::kPitchR, lane);
-                                        if (lane == src)
-                                            packed = q ? (packed & 0xFFFFu) | ((uint32_t)ex << 16)
-                                                       : (packed & 0xFFFF0000u) | ex;
-                                    }
-                                }
+                        for (int n = 0; n < NB; n += 2) {
+                            const int nn = ns * NB + n;   // column group in the block
+                            uint32_t b0r, b1r, b2r, b3r;
+                            if (!TRANS) {
+                                // B(k, n) = R[k][n], row-major [k][n]: transposed 8x8 loads
+                                const int krow = kk * 16 + (lane & 15);
+                                const int ncol = nn * 8 + (lane >> 4) * 8;
+                                ldsm_x4_t(rs_a + (krow * S::kPitchR + ncol) * 2, b0r, b1r, b2r, b3r);
+                            } else {
+                                // B(k, n) = R[n][k]: row-major [n][k] is the col layout
+                                const int nrow = nn * 8 + (lane & 7) + ((lane >> 4) << 3);
+                                const int kcol = kk * 16 + ((lane >> 3) & 1) * 8;
+                                ldsm_x4(rs_a + (nrow * S::kPitchR + kcol) * 2, b0r, b1r, b2r, b3r);
+                            }
+                            mma16816(acc[n], a0, a1, a2, a3, b0r, b1r);
+                            mma16816(acc[n + 1], a0, a1, a2, a3, b2r, b3r);
+                            if constexpr (kExact) {
+                                constexpr uint32_t m = 0x7FFF7FFFu;   // |.| of both BF16 halves
+                                mma16816(accabs[n], a0 & m, a1 & m, a2 & m, a3 & m, b0r & m, b1r & m);
+                                mma16816(accabs[n + 1], a0 & m, a1 & m, a2 & m, a3 & m, b2r & m, b3r & m);
+                            }
+                            if constexpr (F32IN) {
+                                mma16816(acc[n], l0, l1, l2, l3, b0r, b1r);
+                                mma16816(acc[n + 1], l0, l1, l2, l3, b2r, b3r);
                             }
                         }
-                        if (live) *(uint32_t *)((uint16_t *)a.out + r * a.out_ld + col) = packed;
+                    }
+                } else {
+                    // identity: C = A.  An FP32 source passes as hi + lo, exactly
+                    // what the two MMAs give with R = I (hi + lo is exact in
+                    // FP32), so a unit rotation and no rotation agree bit for bit
+#pragma unroll
+                    for (int n = 0; n < NB; ++n)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int row = 16 * warp + g + 8 * h;
+                            const int col = (ns * NB + n) * 8 + 2 * t;
+                            if constexpr (F32IN) {
+                                const float2 v = *(const float2 *)((const float *)xs_p + row * S::kPitchX + col);
+                                uint32_t hi, lo;
+                                split2(v.x, v.y, hi, lo);
+                                acc[n][2 * h] = bf2f(hi & 0xFFFFu) + bf2f(lo & 0xFFFFu);
+                                acc[n][2 * h + 1] = bf2f(hi >> 16) + bf2f(lo >> 16);
+                            } else {
+                                const uint32_t v = *(const uint32_t *)((const uint16_t *)xs_p + row * S::kPitchX + col);
+                                acc[n][2 * h] = bf2f(v & 0xFFFFu);
+                                acc[n][2 * h + 1] = bf2f(v >> 16);
+                            }
+                        }
+                }
+                // epilogue straight from the fragments: each quad of lanes
+                // writes 2 consecutive columns of one row.  kExact: bit
+                // (n * 4 + h * 2 + q) of cand marks a result that may sit near
+                // a rounding midpoint; the warp recomputes those afterwards
+                uint32_t cand = 0;
+#pragma unroll
+                for (int n = 0; n < NB; ++n)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int rl = 16 * warp + g + 8 * h;
+                        if (rl >= tl.nrows) continue;
+                        const int64_t r = tl.row0 + rl;
+                        const int col = beta * B + (ns * NB + n) * 8 + 2 * t;
+                        const float v0 = acc[n][2 * h], v1 = acc[n][2 * h + 1];
+                        if constexpr (EPI == ROT_SWIGLU_BWD) {
+                            const float *c = a.ctxf + r * 2 * a.dim + col;
+                            const float2 gg = *(const float2 *)c;
+                            const float2 uu = *(const float2 *)(c + a.dim);
+                            const float s0 = 1.f / (1.f + expf(-gg.x)), s1 = 1.f / (1.f + expf(-gg.y));
+                            const float dg0 = v0 * uu.x * s0 * (1.f + gg.x * (1.f - s0));
+                            const float dg1 = v1 * uu.y * s1 * (1.f + gg.y * (1.f - s1));
+                            const float du0 = v0 * (gg.x * s0), du1 = v1 * (gg.y * s1);
+                            __half2 *o = (__half2 *)((uint16_t *)a.out + r * a.out_ld + col);
+                            o[0] = __floats2half2_rn(dg0, dg1);
+                            o[a.dim / 2] = __floats2half2_rn(du0, du1);
+                        } else if constexpr (F32OUT) {
+                            *(float2 *)((float *)a.out + r * a.out_ld + col) = make_float2(v0, v1);
+                        } else {
+                            if constexpr (kExact) {
+                                // the FP32 sum of b <= 64 products over four
+                                // MMAs is within 2^-21 of the sum of their
+                                // magnitudes; 2^-20 of it decides which
+                                // results may sit near a rounding midpoint
+                                if (Re) {
+                                    const int bit = n * 4 + h * 2;
+                                    cand |= (uint32_t)near_bf16_midpoint(v0, accabs[n][2 * h] * 9.5367431640625e-07f) << bit;
+                                    cand |= (uint32_t)near_bf16_midpoint(v1, accabs[n][2 * h + 1] * 9.5367431640625e-07f) << (bit + 1);
+                                }
+                            }
+                            *(uint32_t *)((uint16_t *)a.out + r * a.out_ld + col) = pack_bf2(v0, v1);
+                        }
+                    }
+                if constexpr (kExact) {
+                    // one candidate at a time, in a rolled loop (a single copy
+                    // of the warp-wide exact sum): the owning lane rewrites
+                    // its element after the pair store above
+                    const uint16_t *rs = (const uint16_t *)(xs_p + S::kXBytes);
+#pragma unroll 1
+                    while (true) {
+                        const uint32_t any = __ballot_sync(0xffffffffu, cand != 0u);
+                        if (!any) break;
+                        const int src = __ffs(any) - 1;
+                        const int bit = __shfl_sync(0xffffffffu, __ffs(cand) - 1, src);
+                        if (lane == src) cand &= cand - 1u;
+                        const int n = bit >> 2, h = (bit >> 1) & 1, q = bit & 1;
+                        const int srow = 16 * warp + (src >> 2) + 8 * h;
+                        const int scol = (ns * NB + n) * 8 + 2 * (src & 3) + q;   // column in the block
+                        // column scol of R (x R), or row scol (x R^T)
+                        const uint16_t *rc = TRANS ? rs + scol * S::kPitchR : rs + scol;
+                        const uint16_t ex = warp_exact_dot_bf16<B>((const uint16_t *)xs_p + srow * S::kPitchX, rc,
+                                                                   TRANS ? 1 : S::kPitchR, lane);
+                        if (lane == src)
+                            ((uint16_t *)a.out)[(tl.row0 + srow) * a.out_ld + beta * B + scol] = ex;
                     }
                 }
+            }
             __syncthreads();   // buffer `buf` is restaged two blocks later
         }
     }
@@ -403,6 +379,7 @@ static void rot_dispatch(int b, const RotArgs &a, int max_tiles, cudaStream_t st
 
 void launch_rotate_tc(const RotCall &c, cudaStream_t st)
 {
+
     RotArgs a{c.src, c.src_ld, c.perm ? 1 : 0, c.perm, c.k, c.R, c.stride, c.dim, c.out, c.out_ld,
               c.tiles, c.tbeg, c.tend, c.nrows, c.ctxf, c.R_alt, c.sel};
     const int max_tiles = c.tiles ? c.max_tiles : (c.nrows + kRotRows - 1) / kRotRows;

@@ -222,6 +222,29 @@ def test_adapter_apply_and_grad(dim, b, rows):
     assert_close(dR.cpu().numpy(), wdR, "dR", rel_fro=1e-5, max_abs=1e-4)
 
 
+@pytest.mark.parametrize("b,rows", [(64, 3001), (32, 517)])
+def test_rotation_exact_at_all_magnitudes(b, rows):
+    """x R and x R^T rounded to BF16 as the exact sums are, bit for bit,
+    with rows spread over 2^-40 .. 2^40 so that many results sit near a
+    rounding midpoint (those take the error-free recomputation)."""
+    dim = 1024
+    rng = np.random.default_rng(b * 7 + rows)
+    z = rng.standard_normal((rows, dim)) * np.exp2(rng.integers(-40, 41, (rows, 1)))
+    z[::7] *= np.exp2(rng.integers(-6, 7, (1, dim)))          # mixed magnitudes inside rows
+    X = gi.f32_to_bf16_bits(z.astype(np.float32))
+    S = gi.gen_skew(1, dim, b, seed=3, sid="S_up", std=0.02)[0]
+    R = gi.f32_to_bf16_bits(oracle.cayley(S).astype(np.float32))
+    Xr = torch.empty((rows, dim), dtype=torch.int16, device="cuda")
+    pmoe.adapter_apply(rows, dim, b, dev(X), dev(R), Xr)
+    dX = torch.empty((rows, dim), dtype=torch.int16, device="cuda")
+    dR = torch.empty((dim // b, b, b), dtype=torch.float32, device="cuda")
+    pmoe.adapter_grad(rows, dim, b, dev(X), dev(X), dev(R), dX, dR)
+    torch.cuda.synchronize()
+    assert np.array_equal(t2np_bits(Xr), oracle.adapter_apply(X, R, b))
+    wdX, _ = oracle.adapter_grad(X, X, R, b)
+    assert np.array_equal(t2np_bits(dX), wdX)
+
+
 @pytest.mark.parametrize("b,std", [(2, 0.5), (16, 0.3), (32, 0.01), (64, 0.01), (128, 0.05)])
 def test_cayley_and_grad(b, std):
     S = gi.gen_skew(3, 2 * b, b, seed=b, sid="S_up", std=std).reshape(-1, b, b)

@@ -60,6 +60,12 @@ def run_gpu(c, C=None, mode=pmoe.MODE_FUSED, backward=True, R_up="case", R_down=
     ctx = L.new_ctx()
     L.forward(X, rt, Y, C=C, mode=mode, ctx=ctx)
     out = dict(Y=t2np_bits(Y))
+    # the saved h and h~ rows (expert-sorted) and each row's expert
+    P, I = cfg.P, cfg.I
+    hb = ctx[P * 2 * I * 4:P * 2 * I * 4 + 2 * P * I * 2].view(torch.int16).view(2, P, I)
+    hb = hb.cpu().numpy().view(np.uint16)
+    out["h"], out["ht"] = hb[0], hb[1]
+    out["offsets"] = rt.offsets.cpu().numpy()
     if backward:
         dX = torch.empty_like(Y)
         dtw = torch.zeros((cfg.T, cfg.k), dtype=torch.float32, device="cuda")
@@ -107,6 +113,15 @@ def test_forward_backward_parity(name):
     g = run_gpu(c)
     o = run_oracle(c)
     assert_close(bits_to_f64(g["Y"]), o["Y64"], f"{name} Y")
+    if c["R_down"] is not None and CASES[name].b <= 64:
+        # h~ = bf16(h R_down[e]) rounded as the exact sum is, per expert
+        # (b <= 64: the rotations' exact rounding)
+        off, b = g["offsets"], CASES[name].b
+        for e in range(CASES[name].E):
+            r0, r1 = off[e], off[e + 1]
+            if r1 > r0:
+                Re = c["R_down"][0 if CASES[name].adapter == "shared" else e]
+                assert np.array_equal(g["ht"][r0:r1], oracle.adapter_apply(g["h"][r0:r1], Re, b)), e
     assert_close(bits_to_f64(g["dX"]), o["dX64"], f"{name} dX")
     assert_close(g["dtw"], o["d_topk_w"], f"{name} d_topk_w")
     if c["R_up"] is not None:
@@ -215,3 +230,30 @@ def test_tiny_end_to_end_from_the_router():
     ob = OL.backward(X, dY, o_idx, o_w)
     assert_close(bits_to_f64(t2np_bits(Y))[exact], Y64[exact], "tiny Y")
     assert_close(bits_to_f64(t2np_bits(dX))[exact], ob["dX64"][exact], "tiny dX")
+
+
+def test_full_tiles_and_chunked_k_are_deterministic():
+    """Token tiles up to the full 256 rows and a gate/up contraction long
+    enough for the chunked accumulation (d = 4096: 64 K steps): four forwards
+    with chunk sizes 2, 4, 16 and 4 again give bit-identical Y, and the
+    saved g | u, h and h~ are identical too."""
+    cfg = gi.LayerConfig("m", T=768, d=4096, E=16, k=8, I=512, b=64, C=4, seed=9)
+    c = make_case(cfg, skew=0.5)
+    L = DeviceLayer(cfg, c["w13"], c["s13"], c["w2"], c["s2"], R_up=c["R_up"], R_down=c["R_down"])
+    rt = L.new_routing()
+    rt.idx.copy_(torch.from_numpy(c["idx"]))
+    rt.w.copy_(torch.from_numpy(c["w"]))
+    L.permute(rt)
+    assert int(rt.counts.max()) > 256            # some experts span several full tiles
+    X = dev(c["X"])
+    outs = []
+    for C in (2, 4, 16, 4):
+        Y = torch.empty((cfg.T, cfg.d), dtype=torch.int16, device="cuda")
+        ctx = L.new_ctx()
+        L.forward(X, rt, Y, C=C, ctx=ctx)
+        torch.cuda.synchronize()
+        outs.append((t2np_bits(Y), ctx.cpu().numpy()))
+    assert L.status() == pmoe.PMOE_OK
+    for Y, ctx in outs[1:]:
+        assert np.array_equal(Y, outs[0][0])
+        assert np.array_equal(ctx, outs[0][1])
