@@ -689,18 +689,22 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
     }
     if (d_topk_w) launch_dtw_reduce(P, I / 32, w.dtw_part, rt->inv_perm, d_topk_w, stream);
     // dh = dh~ R_down^T (FP32 dh~ split into two BF16 parts), then the SwiGLU
-    // backward from the saved FP32 g, u into FP16 [dg | du]
-    {
+    // backward from the saved FP32 g, u into FP16 [dg | du]; and dR_down.
+    // Per-expert adapters of block 64 do both in one pass over dh~.
+    if (R_dn && sd && adapter_bwd_fused_ok(b)) {
+        launch_adapter_bwd_tc(E, P, I, w.dht, h, I, false, rt->perm, k, R_dn, sd, rt->offsets, w.dgu,
+                              true, ctx_gu, dR_down, stream);
+    } else {
         RotCall c = rot_rows(b, true, w.dht, I, nullptr, k, R_dn, sd, I, w.dgu, 2 * (int64_t)I,
                              L.rtiles, rtb, rte, maxrt, 0);
         c.src_f32 = true;
         c.swiglu_bwd = true;
         c.ctxf = ctx_gu;
         launch_rotate_tc(c, stream);
+        if (R_dn)
+            launch_outer_tc(nsets_dn, P, I, b, h, I, false, rt->perm, k, w.dht, true, I,
+                            sd ? rt->offsets : nullptr, dR_down, stream);
     }
-    if (R_dn)
-        launch_outer_tc(nsets_dn, P, I, b, h, I, false, rt->perm, k, w.dht, true, I,
-                        sd ? rt->offsets : nullptr, dR_down, stream);
 
     // dx~ = [dg | du] W13 on FP16 operands (dg, du to 11 significant bits)
     GemmArgs x{};
@@ -726,13 +730,16 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
         ScopedTimer tm(PMOE_KT_GEMM_BWD_DX, stream);
         if ((gs = run_gemm(x, P, w.err, stream)) != PMOE_OK) return gs;
     }
-    if (R_up)
-        launch_outer_tc(nsets_up, P, d, b, (const uint16_t *)X, d, true, rt->perm, k, w.dxt, true, d,
-                        su ? rt->offsets : nullptr, dR_up, stream);
-    // dx_pair = dx~ R_up^T (FP32; without an adapter the same pass as the
-    // identity, so that R = I and no adapter agree bit for bit), then the
-    // slot sum per token
-    {
+    // dR_up and dx_pair = dx~ R_up^T (FP32; without an adapter the same pass
+    // as the identity, so that R = I and no adapter agree bit for bit), then
+    // the slot sum per token.  Per-expert adapters of block 64: one pass.
+    if (R_up && su && adapter_bwd_fused_ok(b)) {
+        launch_adapter_bwd_tc(E, P, d, w.dxt, (const uint16_t *)X, d, true, rt->perm, k, R_up, su,
+                              rt->offsets, w.dxp, false, nullptr, dR_up, stream);
+    } else {
+        if (R_up)
+            launch_outer_tc(nsets_up, P, d, b, (const uint16_t *)X, d, true, rt->perm, k, w.dxt, true, d,
+                            su ? rt->offsets : nullptr, dR_up, stream);
         RotCall c = rot_rows(b, true, w.dxt, d, nullptr, k, R_up, su, d, w.dxp, d, L.rtiles, rtb, rte,
                              maxrt, 0);
         c.src_f32 = c.out_f32 = true;

@@ -128,6 +128,14 @@ void launch_rotate_tc(const RotCall &c, cudaStream_t st);
 void launch_outer_tc(int nsets, int nrows, int dim, int b, const uint16_t *a, int64_t a_ld,
                      bool gather, const int32_t *perm, int k, const void *g, bool g_f32, int64_t g_ld,
                      const int32_t *offsets, float *dR, cudaStream_t st);
+// Fused backward of the adapter for b = 64 (adapter_bwd_fused_ok): per (set,
+// block), out = g R^T (FP32 rows, or with swiglu the FP16 [dg | du] from
+// ctxf) and dR[set][block] = sum a^T g, reading the FP32 g once
+bool adapter_bwd_fused_ok(int b);
+void launch_adapter_bwd_tc(int nsets, int nrows, int dim, const float *g, const uint16_t *a, int64_t a_ld,
+                           bool gather, const int32_t *perm, int k, const uint16_t *R, int64_t stride,
+                           const int32_t *offsets, void *out, bool swiglu, const float *ctxf, float *dR,
+                           cudaStream_t st);
 constexpr int kRotTileRows = 128;
 
 // layer.cu

@@ -551,4 +551,214 @@ void launch_outer_tc(int nsets, int nrows, int dim, int b, const uint16_t *a, in
     note_launch();
 }
 
+// ------------------------------------------------------------------ fused backward, b = 64
+// One pass over an FP32 gradient g (dx~ or dh~, expert-sorted rows) per
+// (set s, block beta), in 64-row batches of the set:
+//   out  = g_blk R_beta^T         (FP32 dx rows; or, SWIGLU, the SwiGLU
+//                                  backward from the saved g, u into FP16
+//                                  [dg | du])
+//   dR[s][beta] = sum_r a_blk^T g_blk   (a = x gathered by perm / k, or h)
+// g is read once for both products (the separate kernels read it twice).
+// g is split into hi = bf16(g) and lo = bf16(g - hi), both multiplied.
+// Warp w: rows (rotation) or i (dR) 16 (w % 4) .., columns 32 (w / 4) ..
+struct AdapterBwdArgs {
+    const float *g;            // [rows, dim] FP32, expert-sorted
+    const uint16_t *a;         // [*, a_ld] BF16 (gathered rows: perm[r] / k)
+    int64_t a_ld;
+    int gather;
+    const int32_t *perm;
+    int k;
+    const uint16_t *R;         // [sets][dim/64][64][64] BF16 (stride elements per set)
+    int64_t stride;
+    const int32_t *offsets;    // rows of set s (NULL: all rows, one set)
+    int nrows;
+    int dim;
+    void *out;                 // FP32 [rows, dim], or SWIGLU: FP16 [rows, 2 dim]
+    const float *ctxf;         // SWIGLU: saved g | u rows [rows, 2 dim]
+    float *dR;                 // [sets][dim/64][64][64]
+};
+
+constexpr int kAbB = 64, kAbRows = 64, kAbPitch = kAbB + 8;
+struct AbSmem {
+    static constexpr int kG = kAbRows * kAbB * 4;       // FP32 staging
+    static constexpr int kA = kAbRows * kAbPitch * 2;   // a tile
+    static constexpr int kStage = kG + kA;
+    static constexpr int kT = kAbRows * kAbPitch * 2;   // hi, lo tiles
+    static constexpr int kR = kAbB * kAbPitch * 2;
+    static constexpr int kBytes = 2 * kStage + 2 * kT + kR;
+};
+
+template <int EPI>
+__global__ void __launch_bounds__(256, 2) k_adapter_bwd(AdapterBwdArgs p)
+{
+    using S = AbSmem;
+    extern __shared__ __align__(16) uint8_t absm[];
+    const uint32_t sm0 = (uint32_t)__cvta_generic_to_shared(absm);
+    const uint32_t hi_a = sm0 + 2 * S::kStage, lo_a = hi_a + S::kT, r_a = lo_a + S::kT;
+    uint16_t *hi_p = (uint16_t *)(absm + 2 * S::kStage), *lo_p = hi_p + kAbRows * kAbPitch;
+    const int nb = p.dim / kAbB;
+    const int s = blockIdx.x / nb, beta = blockIdx.x % nb;
+    const int r0 = p.offsets ? p.offsets[s] : 0, r1 = p.offsets ? p.offsets[s + 1] : p.nrows;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rg = warp & 3, ch = warp >> 2, gq = lane >> 2, tq = lane & 3;
+    const uint16_t *Rb = p.R + (int64_t)s * p.stride + (int64_t)beta * kAbB * kAbB;
+
+    // the rotation block (once), then batch staging: g FP32 rows and a rows
+    for (int i = threadIdx.x; i < kAbB * 8; i += 256)
+        cp_async16(r_a + ((i >> 3) * kAbPitch + (i & 7) * 8) * 2, Rb + (i >> 3) * kAbB + (i & 7) * 8, true);
+    auto stage = [&](int rb, int buf) {
+        const uint32_t ga = sm0 + buf * S::kStage, aa = ga + S::kG;
+        const int n_live = min(kAbRows, r1 - rb);
+        for (int i = threadIdx.x; i < kAbRows * 16; i += 256) {   // 16 chunks of 4 floats per row
+            const int rr = i >> 4, c = i & 15;
+            const bool live = rr < n_live;
+            const int64_t r = rb + (live ? rr : 0);
+            cp_async16(ga + (rr * kAbB + c * 4) * 4, p.g + r * p.dim + (int64_t)beta * kAbB + c * 4, live);
+        }
+        for (int i = threadIdx.x; i < kAbRows * 8; i += 256) {
+            const int rr = i >> 3, c = i & 7;
+            const bool live = rr < n_live;
+            const int r = rb + (live ? rr : 0);
+            const int64_t arow = p.gather ? (int64_t)(p.perm[r] / p.k) : r;
+            cp_async16(aa + (rr * kAbPitch + c * 8) * 2, p.a + arow * p.a_ld + (int64_t)beta * kAbB + c * 8, live);
+        }
+        cp_async_commit();
+    };
+
+    float dacc[4][4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n) dacc[n][0] = dacc[n][1] = dacc[n][2] = dacc[n][3] = 0.f;
+    if (r0 < r1) stage(r0, 0);
+    else cp_async_commit();
+    for (int rb = r0, it = 0; rb < r1; rb += kAbRows, ++it) {
+        const int buf = it & 1;
+        if (rb + kAbRows < r1) {
+            stage(rb + kAbRows, buf ^ 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        // split the FP32 rows into the hi and lo BF16 tiles
+        {
+            const float *gs = (const float *)(absm + buf * S::kStage);
+            for (int i = threadIdx.x; i < kAbRows * 16; i += 256) {
+                const int rr = i >> 4, c = i & 15;
+                const float4 v = *(const float4 *)(gs + rr * kAbB + c * 4);
+                uint32_t h0, l0, h1, l1;
+                split2(v.x, v.y, h0, l0);
+                split2(v.z, v.w, h1, l1);
+                *(uint2 *)(hi_p + rr * kAbPitch + c * 4) = make_uint2(h0, h1);
+                *(uint2 *)(lo_p + rr * kAbPitch + c * 4) = make_uint2(l0, l1);
+            }
+        }
+        __syncthreads();
+        const uint32_t aa = sm0 + buf * S::kStage + S::kG;
+        const int n_live = min(kAbRows, r1 - rb);
+
+        // out rows 16 rg .., columns 32 ch ..: g (hi + lo) R^T
+        float acc[4][4];
+#pragma unroll
+        for (int n = 0; n < 4; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < kAbB / 16; ++kk) {
+            uint32_t a0, a1, a2, a3, l0, l1, l2, l3;
+            const int row = 16 * rg + (lane & 15), col = kk * 16 + (lane >> 4) * 8;
+            ldsm_x4(hi_a + (row * kAbPitch + col) * 2, a0, a1, a2, a3);
+            ldsm_x4(lo_a + (row * kAbPitch + col) * 2, l0, l1, l2, l3);
+#pragma unroll
+            for (int n = 0; n < 4; n += 2) {
+                // B(k, n) = R[n][k]: row-major [n][k] is the col layout
+                const int nrow = 32 * ch + n * 8 + (lane & 7) + ((lane >> 4) << 3);
+                const int kcol = kk * 16 + ((lane >> 3) & 1) * 8;
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(r_a + (nrow * kAbPitch + kcol) * 2, b0, b1, b2, b3);
+                mma16816(acc[n], a0, a1, a2, a3, b0, b1);
+                mma16816(acc[n + 1], a0, a1, a2, a3, b2, b3);
+                mma16816(acc[n], l0, l1, l2, l3, b0, b1);
+                mma16816(acc[n + 1], l0, l1, l2, l3, b2, b3);
+            }
+        }
+#pragma unroll
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int rl = 16 * rg + gq + 8 * h;
+                if (rl >= n_live) continue;
+                const int64_t r = rb + rl;
+                const int col = beta * kAbB + 32 * ch + n * 8 + 2 * tq;
+                const float v0 = acc[n][2 * h], v1 = acc[n][2 * h + 1];
+                if constexpr (EPI == ROT_SWIGLU_BWD) {
+                    const float *c = p.ctxf + r * 2 * p.dim + col;
+                    const float2 gg = *(const float2 *)c;
+                    const float2 uu = *(const float2 *)(c + p.dim);
+                    const float s0 = 1.f / (1.f + expf(-gg.x)), s1 = 1.f / (1.f + expf(-gg.y));
+                    const float dg0 = v0 * uu.x * s0 * (1.f + gg.x * (1.f - s0));
+                    const float dg1 = v1 * uu.y * s1 * (1.f + gg.y * (1.f - s1));
+                    const float du0 = v0 * (gg.x * s0), du1 = v1 * (gg.y * s1);
+                    __half2 *o = (__half2 *)((uint16_t *)p.out + r * 2 * p.dim + col);
+                    o[0] = __floats2half2_rn(dg0, dg1);
+                    o[p.dim / 2] = __floats2half2_rn(du0, du1);
+                } else {
+                    *(float2 *)((float *)p.out + r * p.dim + col) = make_float2(v0, v1);
+                }
+            }
+
+        // dR rows i = 16 rg .., columns j = 32 ch ..: += a^T (hi + lo) over
+        // the batch's rows (dead rows are zero in both tiles)
+#pragma unroll
+        for (int kk = 0; kk < kAbRows / 16; ++kk) {
+            uint32_t a0, a1, a2, a3;
+            {
+                // A(m = i, k = row) = a[row][i]: transposed 8x8 loads
+                const int krow = kk * 16 + (lane & 7) + ((lane >> 4) << 3);
+                const int mcol = 16 * rg + ((lane >> 3) & 1) * 8;
+                ldsm_x4_t(aa + (krow * kAbPitch + mcol) * 2, a0, a1, a2, a3);
+            }
+#pragma unroll
+            for (int n = 0; n < 4; n += 2) {
+                const int krow = kk * 16 + (lane & 15);
+                const int ncol = 32 * ch + n * 8 + (lane >> 4) * 8;
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(hi_a + (krow * kAbPitch + ncol) * 2, b0, b1, b2, b3);
+                mma16816(dacc[n], a0, a1, a2, a3, b0, b1);
+                mma16816(dacc[n + 1], a0, a1, a2, a3, b2, b3);
+                ldsm_x4_t(lo_a + (krow * kAbPitch + ncol) * 2, b0, b1, b2, b3);
+                mma16816(dacc[n], a0, a1, a2, a3, b0, b1);
+                mma16816(dacc[n + 1], a0, a1, a2, a3, b2, b3);
+            }
+        }
+        __syncthreads();   // the tiles and this stage are refilled next
+    }
+    cp_async_wait<0>();   // (an empty set still loaded its rotation block)
+    float *D = p.dR + ((int64_t)s * nb + beta) * kAbB * kAbB;
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int i = 16 * rg + gq + 8 * h, j = 32 * ch + n * 8 + 2 * tq;
+            *(float2 *)(D + i * kAbB + j) = make_float2(dacc[n][2 * h], dacc[n][2 * h + 1]);
+        }
+}
+
+bool adapter_bwd_fused_ok(int b) { return b == kAbB; }
+
+void launch_adapter_bwd_tc(int nsets, int nrows, int dim, const float *g, const uint16_t *a, int64_t a_ld,
+                           bool gather, const int32_t *perm, int k, const uint16_t *R, int64_t stride,
+                           const int32_t *offsets, void *out, bool swiglu, const float *ctxf, float *dR,
+                           cudaStream_t st)
+{
+    AdapterBwdArgs p{g, a, a_ld, gather ? 1 : 0, perm, k, R, stride, offsets, nrows, dim, out, ctxf, dR};
+    const int grid = nsets * (dim / kAbB);
+    if (grid <= 0) return;
+    auto kern = swiglu ? k_adapter_bwd<ROT_SWIGLU_BWD> : k_adapter_bwd<ROT_STORE>;
+    static bool attr[2] = {false, false};
+    if (!attr[swiglu]) {
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, AbSmem::kBytes);
+        attr[swiglu] = true;
+    }
+    kern<<<grid, 256, AbSmem::kBytes, st>>>(p);
+    note_launch();
+}
+
 }  // namespace pmoe
