@@ -59,7 +59,11 @@ def parse():
 # of the GEMM classes on the default workload, from one ncu capture, keyed
 # by the digest of the GEMM sources it was taken with: once those sources
 # change the figure no longer describes the kernel and is reported as null.
-TRAFFIC = {"digest": "", "bytes": {}}
+TRAFFIC = {"digest": "80a4dc6f4381af7e", "bytes": {
+    ("kimi_k2", "fused", "gemm_gate_up"): 9.234523e9,
+    ("kimi_k2", "fused", "gemm_down"): 5.281668e9,
+    ("kimi_k2", "fused", "gemm_bwd_g"): 5.070333e9,
+    ("kimi_k2", "fused", "gemm_bwd_dx"): 9.113973e9}}
 
 
 def gemm_digest() -> str:
