@@ -606,7 +606,17 @@ __global__ void __launch_bounds__(256, 2) k_adapter_bwd(AdapterBwdArgs p)
     // the rotation block (once), then batch staging: g FP32 rows and a rows
     for (int i = threadIdx.x; i < kAbB * 8; i += 256)
         cp_async16(r_a + ((i >> 3) * kAbPitch + (i & 7) * 8) * 2, Rb + (i >> 3) * kAbB + (i & 7) * 8, true);
-    auto stage = [&](int rb, int buf) {
+    // source rows of thread t's two a-chunks (rows t/8 and t/8 + 32 of a
+    // batch), read one batch ahead so that the gather's index loads do not
+    // stall the batch being multiplied
+    auto rows_of = [&](int rb, int (&ar)[2]) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = rb + (threadIdx.x >> 3) + 32 * h;
+            ar[h] = r < r1 ? (p.gather ? p.perm[r] / p.k : r) : 0;
+        }
+    };
+    auto stage = [&](int rb, int buf, const int (&ar)[2]) {
         const uint32_t ga = sm0 + buf * S::kStage, aa = ga + S::kG;
         const int n_live = min(kAbRows, r1 - rb);
         for (int i = threadIdx.x; i < kAbRows * 16; i += 256) {   // 16 chunks of 4 floats per row
@@ -615,12 +625,12 @@ __global__ void __launch_bounds__(256, 2) k_adapter_bwd(AdapterBwdArgs p)
             const int64_t r = rb + (live ? rr : 0);
             cp_async16(ga + (rr * kAbB + c * 4) * 4, p.g + r * p.dim + (int64_t)beta * kAbB + c * 4, live);
         }
-        for (int i = threadIdx.x; i < kAbRows * 8; i += 256) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int i = threadIdx.x + 256 * h;
             const int rr = i >> 3, c = i & 7;
-            const bool live = rr < n_live;
-            const int r = rb + (live ? rr : 0);
-            const int64_t arow = p.gather ? (int64_t)(p.perm[r] / p.k) : r;
-            cp_async16(aa + (rr * kAbPitch + c * 8) * 2, p.a + arow * p.a_ld + (int64_t)beta * kAbB + c * 8, live);
+            cp_async16(aa + (rr * kAbPitch + c * 8) * 2, p.a + (int64_t)ar[h] * p.a_ld + (int64_t)beta * kAbB + c * 8,
+                       rr < n_live);
         }
         cp_async_commit();
     };
@@ -628,12 +638,16 @@ __global__ void __launch_bounds__(256, 2) k_adapter_bwd(AdapterBwdArgs p)
     float dacc[4][4];
 #pragma unroll
     for (int n = 0; n < 4; ++n) dacc[n][0] = dacc[n][1] = dacc[n][2] = dacc[n][3] = 0.f;
-    if (r0 < r1) stage(r0, 0);
+    int ar[2], ar_next[2];
+    rows_of(r0, ar);
+    if (r0 < r1) stage(r0, 0, ar);
     else cp_async_commit();
+    rows_of(r0 + kAbRows, ar_next);
     for (int rb = r0, it = 0; rb < r1; rb += kAbRows, ++it) {
         const int buf = it & 1;
         if (rb + kAbRows < r1) {
-            stage(rb + kAbRows, buf ^ 1);
+            stage(rb + kAbRows, buf ^ 1, ar_next);
+            rows_of(rb + 2 * kAbRows, ar_next);
             cp_async_wait<1>();
         } else {
             cp_async_wait<0>();
@@ -656,6 +670,20 @@ __global__ void __launch_bounds__(256, 2) k_adapter_bwd(AdapterBwdArgs p)
         const uint32_t aa = sm0 + buf * S::kStage + S::kG;
         const int n_live = min(kAbRows, r1 - rb);
 
+        // SWIGLU: the saved g, u of this thread's outputs, loaded before the
+        // MMAs so that their latency overlaps them
+        float2 cg[4][2], cu[4][2];
+        if constexpr (EPI == ROT_SWIGLU_BWD) {
+#pragma unroll
+            for (int n = 0; n < 4; ++n)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int rl = min(16 * rg + gq + 8 * h, n_live - 1);
+                    const float *c = p.ctxf + (int64_t)(rb + rl) * 2 * p.dim + beta * kAbB + 32 * ch + n * 8 + 2 * tq;
+                    cg[n][h] = *(const float2 *)c;
+                    cu[n][h] = *(const float2 *)(c + p.dim);
+                }
+        }
         // out rows 16 rg .., columns 32 ch ..: g (hi + lo) R^T
         float acc[4][4];
 #pragma unroll
@@ -689,9 +717,7 @@ __global__ void __launch_bounds__(256, 2) k_adapter_bwd(AdapterBwdArgs p)
                 const int col = beta * kAbB + 32 * ch + n * 8 + 2 * tq;
                 const float v0 = acc[n][2 * h], v1 = acc[n][2 * h + 1];
                 if constexpr (EPI == ROT_SWIGLU_BWD) {
-                    const float *c = p.ctxf + r * 2 * p.dim + col;
-                    const float2 gg = *(const float2 *)c;
-                    const float2 uu = *(const float2 *)(c + p.dim);
+                    const float2 gg = cg[n][h], uu = cu[n][h];
                     const float s0 = 1.f / (1.f + expf(-gg.x)), s1 = 1.f / (1.f + expf(-gg.y));
                     const float dg0 = v0 * uu.x * s0 * (1.f + gg.x * (1.f - s0));
                     const float dg1 = v1 * uu.y * s1 * (1.f + gg.y * (1.f - s1));
