@@ -257,3 +257,34 @@ def test_full_tiles_and_chunked_k_are_deterministic():
     for Y, ctx in outs[1:]:
         assert np.array_equal(Y, outs[0][0])
         assert np.array_equal(ctx, outs[0][1])
+
+
+def test_dropped_pair_gets_zero_routing_gradient():
+    """An expert id outside [0, E) leaves its pair out of the grouping (the
+    permute reports PMOE_ERR_BAD_INDEX); the backward still runs, writes
+    d_topk_w = 0 for that pair and finite values everywhere else, and writes
+    nothing out of bounds."""
+    cfg = gi.CONFIGS["tiny"]
+    c = make_case(cfg)
+    idx = c["idx"].copy()
+    idx[5, 1] = cfg.E                       # out of range
+    L = DeviceLayer(cfg, c["w13"], c["s13"], c["w2"], c["s2"], R_up=c["R_up"], R_down=c["R_down"])
+    rt = L.new_routing()
+    rt.idx.copy_(torch.from_numpy(idx))
+    rt.w.copy_(torch.from_numpy(c["w"]))
+    L.permute(rt)
+    assert int(rt.offsets[cfg.E]) == cfg.P - 1
+    X = dev(c["X"])
+    Y = torch.empty((cfg.T, cfg.d), dtype=torch.int16, device="cuda")
+    ctx = L.new_ctx()
+    L.forward(X, rt, Y, ctx=ctx)
+    dX = torch.empty_like(Y)
+    dtw = torch.full((cfg.T, cfg.k), float("nan"), dtype=torch.float32, device="cuda")
+    dRu, dRd = L.grads()
+    L.backward(X, dev(c["dY"]), ctx, rt, dX, dtw, dRu, dRd)
+    torch.cuda.synchronize()
+    assert L.status() == pmoe.PMOE_ERR_BAD_INDEX
+    d = dtw.cpu().numpy()
+    assert d[5, 1] == 0.0
+    assert np.all(np.isfinite(d))
+    assert np.all(np.isfinite(bits_to_f64(t2np_bits(dX))))
