@@ -3,6 +3,7 @@
 // adapter is a local orthogonal transform; S skew-symmetric makes each
 // block orthogonal).
 #include "common.cuh"
+#include "mma_sync.cuh"
 #include "launch.h"
 
 namespace pmoe {
@@ -481,6 +482,151 @@ __global__ void __launch_bounds__(256) k_cayley_grad4(const float *__restrict__ 
     }
 }
 
+// The same gradient for b = 32, 64 on the tensor cores: both products are
+// B x B x B contractions, so they run on mma.sync with every FP32 operand
+// split into three BF16 terms x = hi + mid + lo (hi = bf16(x), mid =
+// bf16(x - hi), lo = bf16(x - hi - mid): together within 2^-24 |x|).  The
+// six products whose terms sum to at most 2^-16 of the leading one are
+// accumulated in FP32 (smallest first), which keeps FP32 accuracy.
+// Warp w computes output rows 16 w .. 16 w + 15, all B columns.
+//   T  = (I+R)^T G         A(m, k) = (I+R)[k][m], B(k, n) = G[k][n]
+//   2M = T (I+R)^T         A(m, k) = T[m][k],     B(k, n) = (I+R)[n][k]
+//   dS = M - M^T
+__device__ __forceinline__ void split3(float x, uint16_t &h, uint16_t &m, uint16_t &l)
+{
+    h = f2bf(x);
+    const float r1 = x - bf2f(h);
+    m = f2bf(r1);
+    l = f2bf(r1 - bf2f(m));
+}
+
+template <int B>
+struct CgMma {
+    static constexpr int kWarps = B / 16;
+    static constexpr int kNT = B / 8;          // 8-wide output column tiles
+    static constexpr int kPB = B + 8;          // BF16 plane pitch (conflict-free ldmatrix)
+    static constexpr int kPF = B + 4;          // FP32 pitch of M
+    static constexpr int kPlane = B * kPB;     // elements per plane
+    static constexpr int kBytes = 2 * 3 * kPlane * 2;   // planes of I + R, of G then T (M over the first)
+    static_assert(B * kPF * 4 <= 3 * kPlane * 2, "M fits over the I + R planes");
+};
+
+template <int B>
+__global__ void __launch_bounds__(B * 2) k_cayley_grad_mma(const float *__restrict__ Rf,
+                                                           const float *__restrict__ G,
+                                                           float *__restrict__ dS)
+{
+    using C = CgMma<B>;
+    extern __shared__ __align__(16) uint8_t cgsm[];
+    uint16_t *Pp = (uint16_t *)cgsm, *Qp = Pp + 3 * C::kPlane;
+    const uint32_t P_a = (uint32_t)__cvta_generic_to_shared(Pp), Q_a = P_a + 3 * C::kPlane * 2;
+    const int64_t off = (int64_t)blockIdx.x * B * B;
+    for (int i = threadIdx.x * 4; i < B * B; i += blockDim.x * 4) {
+        const int r = i / B, c = i % B;
+        const float4 rv = *(const float4 *)(Rf + off + i), gv = *(const float4 *)(G + off + i);
+        const float x[4] = {rv.x + (r == c ? 1.f : 0.f), rv.y + (r == c + 1 ? 1.f : 0.f),
+                            rv.z + (r == c + 2 ? 1.f : 0.f), rv.w + (r == c + 3 ? 1.f : 0.f)};
+        const float y[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint16_t h, m, l;
+            split3(x[q], h, m, l);
+            Pp[r * C::kPB + c + q] = h;
+            Pp[C::kPlane + r * C::kPB + c + q] = m;
+            Pp[2 * C::kPlane + r * C::kPB + c + q] = l;
+            split3(y[q], h, m, l);
+            Qp[r * C::kPB + c + q] = h;
+            Qp[C::kPlane + r * C::kPB + c + q] = m;
+            Qp[2 * C::kPlane + r * C::kPB + c + q] = l;
+        }
+    }
+    __syncthreads();
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    // the six term pairs (a, b) with a + b <= 2, smallest first
+    constexpr int kTa[6] = {2, 1, 0, 1, 0, 0}, kTb[6] = {0, 1, 2, 0, 1, 0};
+    float acc[C::kNT][4];
+#pragma unroll
+    for (int n = 0; n < C::kNT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    // T = (I+R)^T G
+#pragma unroll
+    for (int kk = 0; kk < B / 16; ++kk) {
+        uint32_t a[3][4];
+        const int krow = kk * 16 + (lane & 7) + ((lane >> 4) << 3);
+        const int mcol = 16 * w + ((lane >> 3) & 1) * 8;
+#pragma unroll
+        for (int pa = 0; pa < 3; ++pa)
+            ldsm_x4_t(P_a + (pa * C::kPlane + krow * C::kPB + mcol) * 2, a[pa][0], a[pa][1], a[pa][2], a[pa][3]);
+#pragma unroll
+        for (int n = 0; n < C::kNT; n += 2) {
+            uint32_t bq[3][4];
+            const int brow = kk * 16 + (lane & 15), bcol = n * 8 + (lane >> 4) * 8;
+#pragma unroll
+            for (int pb = 0; pb < 3; ++pb)
+                ldsm_x4_t(Q_a + (pb * C::kPlane + brow * C::kPB + bcol) * 2, bq[pb][0], bq[pb][1], bq[pb][2], bq[pb][3]);
+#pragma unroll
+            for (int u = 0; u < 6; ++u) {
+                const uint32_t *A = a[kTa[u]], *Bv = bq[kTb[u]];
+                mma16816(acc[n], A[0], A[1], A[2], A[3], Bv[0], Bv[1]);
+                mma16816(acc[n + 1], A[0], A[1], A[2], A[3], Bv[2], Bv[3]);
+            }
+        }
+    }
+    __syncthreads();   // every warp is done with the planes of G
+#pragma unroll
+    for (int n = 0; n < C::kNT; ++n)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int row = 16 * w + g + 8 * h, col = n * 8 + 2 * t;
+            uint16_t h0, m0, l0, h1, m1, l1;
+            split3(acc[n][2 * h], h0, m0, l0);
+            split3(acc[n][2 * h + 1], h1, m1, l1);
+            uint32_t *q = (uint32_t *)(Qp + row * C::kPB + col);
+            q[0] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+            q[C::kPlane / 2] = (uint32_t)m0 | ((uint32_t)m1 << 16);
+            q[C::kPlane] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+            acc[n][2 * h] = acc[n][2 * h + 1] = 0.f;
+        }
+    __syncthreads();
+    // 2M = T (I+R)^T
+#pragma unroll
+    for (int kk = 0; kk < B / 16; ++kk) {
+        uint32_t a[3][4];
+        const int arow = 16 * w + (lane & 15), acol = kk * 16 + (lane >> 4) * 8;
+#pragma unroll
+        for (int pa = 0; pa < 3; ++pa)
+            ldsm_x4(Q_a + (pa * C::kPlane + arow * C::kPB + acol) * 2, a[pa][0], a[pa][1], a[pa][2], a[pa][3]);
+#pragma unroll
+        for (int n = 0; n < C::kNT; n += 2) {
+            uint32_t bq[3][4];
+            const int nrow = n * 8 + (lane & 7) + ((lane >> 4) << 3);
+            const int kcol = kk * 16 + ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int pb = 0; pb < 3; ++pb)
+                ldsm_x4(P_a + (pb * C::kPlane + nrow * C::kPB + kcol) * 2, bq[pb][0], bq[pb][1], bq[pb][2], bq[pb][3]);
+#pragma unroll
+            for (int u = 0; u < 6; ++u) {
+                const uint32_t *A = a[kTa[u]], *Bv = bq[kTb[u]];
+                mma16816(acc[n], A[0], A[1], A[2], A[3], Bv[0], Bv[1]);
+                mma16816(acc[n + 1], A[0], A[1], A[2], A[3], Bv[2], Bv[3]);
+            }
+        }
+    }
+    __syncthreads();   // every warp is done with the planes of I + R: M goes over them
+    float *Mf = (float *)cgsm;
+#pragma unroll
+    for (int n = 0; n < C::kNT; ++n)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int row = 16 * w + g + 8 * h, col = n * 8 + 2 * t;
+            *(float2 *)(Mf + row * C::kPF + col) = make_float2(0.5f * acc[n][2 * h], 0.5f * acc[n][2 * h + 1]);
+        }
+    __syncthreads();
+    for (int i = threadIdx.x; i < B * B; i += blockDim.x) {
+        const int r = i / B, c = i % B;
+        dS[off + i] = Mf[r * C::kPF + c] - Mf[c * C::kPF + r];
+    }
+}
+
 template <int B>
 static void cayley_b(int nblk, const float *S, uint16_t *Rb, float *Rf, cudaStream_t st)
 {
@@ -499,7 +645,14 @@ static void cayley_grad_b(int nblk, const float *Rf, const float *dR, float *dS,
 {
     const size_t sm = 3 * (size_t)B * (B + 4) * sizeof(float);
     static bool attr = false;
-    if constexpr (B >= 8) {
+    if constexpr (B == 32 || B == 64) {
+        if (!attr) {
+            cudaFuncSetAttribute(k_cayley_grad_mma<B>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 CgMma<B>::kBytes);
+            attr = true;
+        }
+        k_cayley_grad_mma<B><<<nblk, 2 * B, CgMma<B>::kBytes, st>>>(Rf, dR, dS);
+    } else if constexpr (B >= 8) {
         if (!attr) {
             cudaFuncSetAttribute(k_cayley_grad4<B>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
             attr = true;
