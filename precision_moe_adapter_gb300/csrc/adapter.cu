@@ -527,17 +527,18 @@ __global__ void __launch_bounds__(B * 2) k_cayley_grad_mma(const float *__restri
         const float x[4] = {rv.x + (r == c ? 1.f : 0.f), rv.y + (r == c + 1 ? 1.f : 0.f),
                             rv.z + (r == c + 2 ? 1.f : 0.f), rv.w + (r == c + 3 ? 1.f : 0.f)};
         const float y[4] = {gv.x, gv.y, gv.z, gv.w};
+        uint16_t xs[3][4], ys[3][4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            uint16_t h, m, l;
-            split3(x[q], h, m, l);
-            Pp[r * C::kPB + c + q] = h;
-            Pp[C::kPlane + r * C::kPB + c + q] = m;
-            Pp[2 * C::kPlane + r * C::kPB + c + q] = l;
-            split3(y[q], h, m, l);
-            Qp[r * C::kPB + c + q] = h;
-            Qp[C::kPlane + r * C::kPB + c + q] = m;
-            Qp[2 * C::kPlane + r * C::kPB + c + q] = l;
+            split3(x[q], xs[0][q], xs[1][q], xs[2][q]);
+            split3(y[q], ys[0][q], ys[1][q], ys[2][q]);
+        }
+#pragma unroll
+        for (int pl = 0; pl < 3; ++pl) {
+            *(uint2 *)(Pp + pl * C::kPlane + r * C::kPB + c) =
+                make_uint2((uint32_t)xs[pl][0] | ((uint32_t)xs[pl][1] << 16), (uint32_t)xs[pl][2] | ((uint32_t)xs[pl][3] << 16));
+            *(uint2 *)(Qp + pl * C::kPlane + r * C::kPB + c) =
+                make_uint2((uint32_t)ys[pl][0] | ((uint32_t)ys[pl][1] << 16), (uint32_t)ys[pl][2] | ((uint32_t)ys[pl][3] << 16));
         }
     }
     __syncthreads();
