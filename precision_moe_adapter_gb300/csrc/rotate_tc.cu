@@ -158,13 +158,12 @@ __global__ void __launch_bounds__(kRotThreads, F32IN ? 2 : 3) k_rotate_mma(RotAr
         stage(b0, 0);
         for (int beta = b0; beta < b1; ++beta) {
             const int buf = (beta - b0) & 1;
-            if (beta + 1 < b1) {
-                stage(beta + 1, buf ^ 1);
-                cp_async_wait<1>();
-            } else {
-                cp_async_wait<0>();
-            }
+            // one barrier per block: after it, block beta's copies are visible
+            // and every warp is done with block beta - 1, whose buffer then
+            // takes block beta + 1
+            cp_async_wait<0>();
             __syncthreads();
+            if (beta + 1 < b1) stage(beta + 1, buf ^ 1);
             const uint32_t xs_a = sm0 + buf * S::kStage, rs_a = xs_a + S::kXBytes;
             const uint8_t *xs_p = rsm + buf * S::kStage;
 
@@ -320,8 +319,8 @@ __global__ void __launch_bounds__(kRotThreads, F32IN ? 2 : 3) k_rotate_mma(RotAr
                     }
                 }
             }
-            __syncthreads();   // buffer `buf` is restaged two blocks later
         }
+        __syncthreads();   // the next item restages buffer 0
     }
 }
 
