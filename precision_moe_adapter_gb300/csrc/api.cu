@@ -426,7 +426,10 @@ static RotCall rot_rows(int b, bool trans, const void *src, int64_t src_ld, cons
     c.tbeg = tbeg;
     c.tend = tend;
     c.max_tiles = max_tiles;
-    c.nrows = nrows;
+    // tile mode: nrows is the number of rows the tiles cover (an upper bound
+    // on the tile count); otherwise the plain row count
+    c.rows_ub = tiles ? nrows : 0;
+    c.nrows = tiles ? 0 : nrows;
     return c;
 }
 
@@ -465,7 +468,7 @@ static pmoe_status forward_impl(pmoe_dims dims, const pmoe_weights *wts, const u
     // x~ = bf16(x R_up[e]) for every pair, gathered into expert-sorted order
     {
         RotCall c = rot_rows(b, false, X, d, rt->perm, k, R_up, su, d, w.xt, d, L.rtiles,
-                             L.chunk_rtiles, L.chunk_rtiles + nch, maxrt, 0);
+                             L.chunk_rtiles, L.chunk_rtiles + nch, maxrt, (int)P);
         c.R_alt = R_up_alt;
         c.sel = sel;
         launch_rotate_tc(c, stream);
@@ -499,7 +502,7 @@ static pmoe_status forward_impl(pmoe_dims dims, const pmoe_weights *wts, const u
     pmoe_status gs;
     auto rot_down = [&](const int32_t *tb, const int32_t *te) {
         RotCall c = rot_rows(b, false, h, I, nullptr, k, R_dn, sd, I, ht, I, L.rtiles, tb, te,
-                             maxrt, 0);
+                             maxrt, (int)P);
         c.R_alt = R_dn_alt;
         c.sel = sel;
         launch_rotate_tc(c, stream);
@@ -696,7 +699,7 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
                               true, ctx_gu, dR_down, stream);
     } else {
         RotCall c = rot_rows(b, true, w.dht, I, nullptr, k, R_dn, sd, I, w.dgu, 2 * (int64_t)I,
-                             L.rtiles, rtb, rte, maxrt, 0);
+                             L.rtiles, rtb, rte, maxrt, (int)P);
         c.src_f32 = true;
         c.swiglu_bwd = true;
         c.ctxf = ctx_gu;
@@ -741,7 +744,7 @@ pmoe_status moe_backward_data(pmoe_dims dims, const pmoe_weights *wts, const pmo
             launch_outer_tc(nsets_up, P, d, b, (const uint16_t *)X, d, true, rt->perm, k, w.dxt, true, d,
                             su ? rt->offsets : nullptr, dR_up, stream);
         RotCall c = rot_rows(b, true, w.dxt, d, nullptr, k, R_up, su, d, w.dxp, d, L.rtiles, rtb, rte,
-                             maxrt, 0);
+                             maxrt, (int)P);
         c.src_f32 = c.out_f32 = true;
         launch_rotate_tc(c, stream);
     }

@@ -117,6 +117,7 @@ struct RotCall {
     const Tile *tiles;
     const int32_t *tbeg, *tend;
     int max_tiles;
+    int rows_ub;              // tiles: upper bound on the rows they hold (0: unknown)
     int nrows;
     const float *ctxf;        // swiglu_bwd: saved [g | u] rows, FP32
     const uint16_t *R_alt;

@@ -8,13 +8,14 @@ namespace pmoe {
 
 // Y[t] = bf16(sum_j w[t,j] o[inv_perm[t*k + j]]), slots in order, over the
 // FP32 pair outputs o (w NULL: unit weights, the slot sum of the backward).
-__global__ void __launch_bounds__(256) k_combine(int T, int d, int k, const float *__restrict__ o,
+__global__ void __launch_bounds__(128) k_combine(int T, int d, int k, const float *__restrict__ o,
                                                  const int32_t *__restrict__ inv_perm,
                                                  const float *__restrict__ w,
                                                  uint16_t *__restrict__ Y)
 {
+    // CTA (t, y): columns 1024 y .. of token t (8 per thread)
     int t = blockIdx.x;
-    for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+    for (int c = blockIdx.y * 1024 + threadIdx.x * 8; c < d; c += gridDim.y * 1024) {
         float acc[8] = {};
         for (int j = 0; j < k; ++j) {
             int r = inv_perm[(int64_t)t * k + j];
@@ -39,7 +40,7 @@ void launch_combine(int T, int d, int k, const float *o, const int32_t *inv_perm
                     const float *w, uint16_t *Y, cudaStream_t st)
 {
     if (T <= 0) return;
-    k_combine<<<T, 256, 0, st>>>(T, d, k, o, inv_perm, w, Y);
+    k_combine<<<dim3(T, (d + 1023) / 1024), 128, 0, st>>>(T, d, k, o, inv_perm, w, Y);
     note_launch();
 }
 

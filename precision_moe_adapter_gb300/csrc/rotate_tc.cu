@@ -34,7 +34,7 @@
 namespace pmoe {
 
 constexpr int kRotRows = kRotTileRows;   // rows per tile (8 warps x 16)
-constexpr int kRotBlocks = 8;            // b-blocks per work item
+constexpr int kRotBlocks = 8;            // b-blocks per work item (fewer when few tiles exist)
 constexpr int kRotThreads = 256;
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool pred)
@@ -89,6 +89,7 @@ struct RotArgs {
     const float *ctxf;         // SWIGLU: saved [g | u] rows of 2*dim FP32
     const uint16_t *R_alt;     // second adapter slot (NULL: none)
     const uint64_t *sel;       // adapter snapshot: low bit of the low word picks R_alt
+    int gblk;                  // b-blocks per work item
 };
 
 // Shared memory of one stage: the source tile (BF16 rows of b + 8
@@ -112,7 +113,7 @@ __global__ void __launch_bounds__(kRotThreads, F32IN ? 2 : 3) k_rotate_mma(RotAr
     const uint32_t sm0 = (uint32_t)__cvta_generic_to_shared(rsm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nblk = a.dim / B;
-    const int ngroups = (nblk + kRotBlocks - 1) / kRotBlocks;
+    const int ngroups = (nblk + a.gblk - 1) / a.gblk;
     const int t0 = a.tiles ? *a.tbeg : 0;
     const int nt = a.tiles ? *a.tend - t0 : (a.nrows + kRotRows - 1) / kRotRows;
     const int64_t items = (int64_t)nt * ngroups;
@@ -133,7 +134,7 @@ __global__ void __launch_bounds__(kRotThreads, F32IN ? 2 : 3) k_rotate_mma(RotAr
         const int bg = (int)(it % ngroups);
         const uint16_t *Re = (a.sel && (*a.sel & 1u)) ? a.R_alt : a.R;
         if (Re && a.stride) Re += (int64_t)tl.expert * a.stride;
-        const int b0 = bg * kRotBlocks, b1 = min(nblk, b0 + kRotBlocks);
+        const int b0 = bg * a.gblk, b1 = min(nblk, b0 + a.gblk);
 
         // stage block beta (source tile and rotation block) into buffer buf
         auto stage = [&](int beta, int buf) {
@@ -335,11 +336,16 @@ static void rot_launch(const RotArgs &a, int max_tiles, cudaStream_t st)
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRotThreads, S::kBytes);
         if (per_sm <= 0) per_sm = 1;
     }
-    const int ngroups = (a.dim / B + kRotBlocks - 1) / kRotBlocks;
-    const int64_t items = (int64_t)max_tiles * ngroups;
-    const int grid = (int)std::min<int64_t>(items, (int64_t)gemm_num_sms() * per_sm);
+    // work items of kRotBlocks blocks, or fewer when the tiles are too few to
+    // fill the GPU (decode: a handful of one-row tiles)
+    const int nblk = a.dim / B, cap = gemm_num_sms() * per_sm;
+    RotArgs ar = a;
+    ar.gblk = kRotBlocks;
+    while (ar.gblk > 1 && (int64_t)max_tiles * ((nblk + ar.gblk - 1) / ar.gblk) < cap) ar.gblk >>= 1;
+    const int64_t items = (int64_t)max_tiles * ((nblk + ar.gblk - 1) / ar.gblk);
+    const int grid = (int)std::min<int64_t>(items, (int64_t)cap);
     if (grid <= 0) return;
-    kern<<<grid, kRotThreads, S::kBytes, st>>>(a);
+    kern<<<grid, kRotThreads, S::kBytes, st>>>(ar);
     note_launch();
 }
 
@@ -358,8 +364,10 @@ void launch_rotate_tc(const RotCall &c, cudaStream_t st)
 {
 
     RotArgs a{c.src, c.src_ld, c.perm ? 1 : 0, c.perm, c.k, c.R, c.stride, c.dim, c.out, c.out_ld,
-              c.tiles, c.tbeg, c.tend, c.nrows, c.ctxf, c.R_alt, c.sel};
-    const int max_tiles = c.tiles ? c.max_tiles : (c.nrows + kRotRows - 1) / kRotRows;
+              c.tiles, c.tbeg, c.tend, c.nrows, c.ctxf, c.R_alt, c.sel, kRotBlocks};
+    // tiles hold at least one row each: at most rows_ub of them
+    const int max_tiles = c.tiles ? (c.rows_ub > 0 ? std::min(c.max_tiles, c.rows_ub) : c.max_tiles)
+                                  : (c.nrows + kRotRows - 1) / kRotRows;
     if (c.swiglu_bwd) {
         rot_dispatch<true, ROT_SWIGLU_BWD, true, false>(c.b, a, max_tiles, st);
     } else if (c.trans) {
